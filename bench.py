@@ -1,0 +1,437 @@
+"""Benchmark: FP32 SGEMM GFLOP/s on one GB300 (and % of the FP32 FFMA peak).
+
+One step = one C = alpha*A*B + beta*C call of the workload (default: the
+4096^3 square problem, A,B ~ U[-1,1], seed 1, alpha 1, beta 0) through the
+library's C ABI, inputs already resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--config VARIANT] [--kernel-only]
+
+Timing: W >= 3 untimed warm-up steps, then K steps; before every step a
+256 MiB buffer is written to flush the 129 MB L2, outside that step's CUDA
+event pair on the launching stream.  ms_per_step is the mean event time;
+under torchrun the max over ranks (each rank runs its own independent
+problem: weak scaling, no collective on the data path).
+
+Also reported: the end-to-end rate through sgemm_run_host (pinned host
+buffers, H2D + kernel + D2H every step), cuBLAS SGEMM via torch.matmul with
+TF32 off (context), the SM clock sampled with nvidia-smi during the timed
+steps, the FFMA-peak fraction at that clock, and the CPU oracle timed on a
+bounded sample on this host's cores.
+
+--impl reference times the fp64 CPU oracle (the reference arm) on the same
+workload, one bounded row-band per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP32 SGEMM GFLOP/s at 4096^3 on 1 GB300; % of FP32 FFMA peak"
+FMA_LANES_PER_SM = 128          # FP32 lanes per SM (4 sub-partitions x 32)
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ["kernel_tma.cu", "kernel_skinny.cu", "kernel_generic.cu", "ptx.cuh", "kernels.h"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        p = os.path.join(ROOT, "dense_fp32_matrix_sm_gb300", "csrc", name)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str, period_ms: int = 100):
+        self.gpu_id = gpu_id
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+               "--format=csv,noheader,nounits", "-lms", str(self.period_ms)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if not self.proc:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+
+    def summary(self, min_load_mhz: float = 0.0):
+        rows = []
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                rows.append({"sm": float(parts[0]), "max": float(parts[1]),
+                             "power": float(parts[2]) if parts[2] not in ("[N/A]", "N/A") else None,
+                             "active": parts[3], "hw": parts[4], "hwt": parts[5], "swt": parts[6],
+                             "swp": parts[7]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        sm = [r["sm"] for r in rows]
+        powers = [r["power"] for r in rows if r["power"] is not None]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r["max"] for r in rows),
+                "sm_mhz_min": min(sm), "power_w_max": max(powers) if powers else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def gpu_id_for(torch, dev: int) -> str:
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
+    dom = getattr(props, "pci_domain_id", None)
+    pdev = getattr(props, "pci_device_id", None)
+    if bus is not None and dom is not None and pdev is not None:
+        return f"{dom:08X}:{bus:02X}:{pdev:02X}.0"
+    return str(dev)
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def time_oracle_rows(A, B, C0, w, rows: int, threads: int) -> float:
+    import oracle
+
+    Cs = C0[:rows] if w.beta != 0.0 else None
+    t0 = time.perf_counter()
+    oracle.sgemm_ref(A[:rows], B, Cs, w.alpha, w.beta, threads=threads)
+    return time.perf_counter() - t0
+
+
+def size_oracle_sample(A, B, C0, w, threads: int, target_s: float) -> int:
+    """Rows per sample so that one oracle call takes about target_s seconds."""
+    probe = min(w.M, max(threads, 1))
+    t = time_oracle_rows(A, B, C0, w, probe, threads)
+    per_row = t / probe
+    rows = int(target_s / max(per_row, 1e-9))
+    rows = max(min(w.M, threads), min(w.M, rows))
+    if rows > threads:
+        rows = rows // threads * threads
+    return max(1, min(w.M, rows))
+
+
+# ---------------------------------------------------------------- main
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="square4096")
+    ap.add_argument("--config", default=None, help="force a kernel variant by name")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="time only the library kernel (no e2e, cuBLAS or CPU legs)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="size of the CPU-baseline sample")
+    return ap.parse_args()
+
+
+def dist_setup(torch):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return dist, rank, world, local
+    return None, rank, world, local
+
+
+def max_over_ranks(torch, dist, value: float) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(torch, dist):
+    if dist is not None:
+        dist.barrier()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
+
+
+def run_reference(args):
+    """The reference arm: the fp64 CPU oracle on bounded row-band samples."""
+    import torch
+
+    dist, rank, world, _ = dist_setup(torch)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    import oracle
+    from dense_fp32_matrix_sm_gb300.inputs import WORKLOADS, workload_inputs
+
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    A, B, C0 = workload_inputs(w)
+    threads = host_cores()
+    total_steps = max(1, args.steps + args.warmup)
+    per_step = max(0.05, min(5.0, 120.0 / total_steps))
+    rows = size_oracle_sample(A, B, C0, w, threads, per_step)
+    for _ in range(args.warmup):
+        time_oracle_rows(A, B, C0, w, rows, threads)
+    times = [time_oracle_rows(A, B, C0, w, rows, threads) for _ in range(max(1, args.steps))]
+    t = sum(times) / len(times)
+    flops = 2.0 * rows * w.N * w.K
+    gflops = flops / t / 1e9
+    sample = f"rows 0..{rows - 1} of {w.M} (all {w.N} columns, K={w.K}) per step"
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{w.name}: {w.describe()}", "M": w.M, "N": w.N, "K": w.K},
+        "cpu_baseline": {"value": round(gflops, 3), "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gflops, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def time_steps(torch, fn, steps: int, flush, stream):
+    """Per-step CUDA-event times (ms) of fn() on `stream`, flushing L2 before each."""
+    evs = []
+    for _ in range(steps):
+        flush()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        evs.append((s, e))
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    dist, rank, world, local = dist_setup(torch)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.cuda.current_device()
+    from dense_fp32_matrix_sm_gb300 import build as b
+
+    b.build()
+    import dense_fp32_matrix_sm_gb300 as sg
+    from dense_fp32_matrix_sm_gb300.inputs import WORKLOADS, workload_inputs
+
+    w = WORKLOADS[args.workload]
+    warmup = max(3, args.warmup)
+    steps = max(1, args.steps)
+    A, B, C0 = workload_inputs(w)
+    dA = torch.from_numpy(A).to(dev)
+    dB = torch.from_numpy(B).to(dev)
+    dC0 = torch.from_numpy(C0).to(dev)
+    dC = dC0.clone()
+    flush_buf = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MiB > 129 MB L2
+    stream = torch.cuda.current_stream()
+
+    plan = sg.Plan(w.M, w.N, w.K, config=args.config)
+    info = plan.info()
+    launches_per_step = plan.launches
+
+    def step():
+        plan.run(w.alpha, dA, dB, w.beta, dC, stream)
+
+    def flush():
+        flush_buf.zero_()
+
+    for _ in range(warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+
+    sampler = None
+    if rank == 0:
+        sampler = ClockSampler(gpu_id_for(torch, dev))
+        sampler.start()
+    barrier(torch, dist)
+    times = time_steps(torch, step, steps, flush, stream)
+    barrier(torch, dist)
+    if sampler:
+        sampler.stop()
+    if sg.device_status() != sg.SGEMM_OK:
+        raise SystemExit("kernel status word set during the timed steps (a wait timed out)")
+
+    ms = statistics.fmean(times)
+    ms_max = max_over_ranks(torch, dist, ms)
+    gflops_total = world * w.flops / (ms_max * 1e-3) / 1e9
+    clocks = sampler.summary() if sampler else {}
+
+    # the FP32 FFMA peak at the clock measured during the timed steps
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peaks = json.load(open(PEAKS_FILE)) if os.path.exists(PEAKS_FILE) else {}
+    sm_mhz = clocks.get("sm_mhz") or None
+    sm_max = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
+    peak_tflops = sms * FMA_LANES_PER_SM * 2 * (sm_mhz or sm_max) * 1e6 / 1e12
+    peak_max_tflops = sms * FMA_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    achieved_tflops = w.flops / (ms * 1e-3) / 1e12
+
+    out = {
+        "metric": METRIC, "value": round(gflops_total, 1), "unit": "GFLOP/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.describe()}", "M": w.M, "N": w.N, "K": w.K,
+                   "variant": info.get("variant"), "grid": info.get("grid"),
+                   "l2": "flushed (256 MiB write) before every timed step, outside its event pair",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "pct_ffma_peak": round(100.0 * achieved_tflops / peak_tflops, 2),
+        "ffma_peak": {"sms": sms, "lanes_per_sm": FMA_LANES_PER_SM, "sm_mhz": sm_mhz,
+                      "tflops_at_measured_clock": round(peak_tflops, 2),
+                      "tflops_at_max_clock": round(peak_max_tflops, 2)},
+        "step_ms": {"mean": round(ms, 4), "median": round(statistics.median(times), 4),
+                    "min": round(min(times), 4), "max": round(max(times), 4)},
+        "gpu_launches": launches_per_step * steps,
+    }
+
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        try:
+            rec = json.load(open(TRAFFIC_FILE)).get(f"{info.get('variant')}|{w.name}")
+            if rec and rec.get("kernel_source_sha") == kernel_source_hash():
+                traffic = rec.get("dram_bytes_per_launch")
+        except (ValueError, OSError):
+            traffic = None
+    out["roofline"] = {"bound": "alu", "achieved": round(achieved_tflops, 3),
+                       "peak": round(peak_tflops, 3), "unit": "TFLOP/s",
+                       "frac": round(achieved_tflops / peak_tflops, 4), "traffic": traffic,
+                       "peak_basis": "SMs x 128 FP32 lanes x 2 FLOP x median SM clock sampled during the "
+                                     "timed steps (FFMA pipe; not a tensor-core path)",
+                       "algorithmic_bytes": w.algorithmic_bytes()}
+    out["clocks"] = {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "sm_mhz_min",
+                                                 "power_w_max", "samples")}
+
+    if not args.kernel_only:
+        # end to end through sgemm_run_host: pinned host in, pinned host out, every step
+        hA = torch.from_numpy(A).pin_memory()
+        hB = torch.from_numpy(B).pin_memory()
+        hC = torch.from_numpy(C0.copy()).pin_memory()
+        h2d = hA.numel() * 4 + hB.numel() * 4 + (hC.numel() * 4 if w.beta != 0.0 else 0)
+        d2h = hC.numel() * 4
+
+        def e2e_step():
+            plan.run_host(w.alpha, hA, hB, w.beta, hC, dA, dB, dC, stream)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_steps = max(3, min(steps, 50))
+        e2e_times = time_steps(torch, e2e_step, e2e_steps, flush, stream)
+        e2e_ms = max_over_ranks(torch, dist, statistics.fmean(e2e_times))
+        out["e2e"] = {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GFLOP/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                      "steps": e2e_steps, "path": "sgemm_run_host (cudaMemcpy2DAsync H2D, kernel, D2H)"}
+        out["gpu_launches"] += launches_per_step * (e2e_steps)
+
+        # cuBLAS SGEMM as context (TF32 off: plain FP32 results)
+        torch.backends.cuda.matmul.allow_tf32 = False
+        torch.backends.cudnn.allow_tf32 = False
+        tA, tB = dA, dB
+        tC = torch.empty_like(dC)
+        if w.beta == 0.0:
+            def cublas_step():
+                torch.matmul(tA, tB, out=tC)
+        else:
+            def cublas_step():
+                torch.addmm(dC0, tA, tB, beta=w.beta, alpha=w.alpha, out=tC)
+        for _ in range(warmup):
+            cublas_step()
+        cb = time_steps(torch, cublas_step, min(steps, 100), flush, stream)
+        cb_ms = statistics.fmean(cb)
+        out["cublas_context"] = {"gflops": round(w.flops / (cb_ms * 1e-3) / 1e9, 1), "ms": round(cb_ms, 4),
+                                 "call": "torch.matmul/addmm fp32, allow_tf32=False",
+                                 "float32_matmul_precision": torch.get_float32_matmul_precision()}
+
+        if rank == 0 and world == 1:
+            import oracle
+
+            oracle.build()
+            threads = host_cores()
+            rows = size_oracle_sample(A, B, C0, w, threads, args.cpu_seconds)
+            t = time_oracle_rows(A, B, C0, w, rows, threads)
+            out["cpu_baseline"] = {"value": round(2.0 * rows * w.N * w.K / t / 1e9, 3), "unit": "GFLOP/s",
+                                   "cores": threads, "kind": "oracle",
+                                   "sample": f"rows 0..{rows - 1} of {w.M} (all {w.N} columns, K={w.K}), "
+                                             f"fp64 with the |A||B| bound, {t:.1f} s"}
+    out["plan"] = plan.describe()
+    plan.close()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

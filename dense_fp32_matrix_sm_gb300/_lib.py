@@ -1,0 +1,261 @@
+"""ctypes binding for libsgemm_gb300.so (the C ABI in include/sgemm.h).
+
+Argument marshalling only: every step of the product runs in the library's
+CUDA kernels.  PyTorch is used for device memory and streams.  If the
+library has not been built this module raises on first use; there is no
+fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
+
+SGEMM_OK = 0
+SGEMM_ERR_INVALID_ARG = -1
+SGEMM_ERR_UNSUPPORTED = -2
+SGEMM_ERR_CUDA = -3
+SGEMM_ERR_TIMEOUT = -4
+SGEMM_ERR_NOMEM = -5
+
+# Every function include/sgemm.h declares, with (restype, argtypes).
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+_int = ctypes.c_int
+_f32 = ctypes.c_float
+SIGNATURES = {
+    "sgemm_plan": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, ctypes.POINTER(_vp)]),
+    "sgemm_plan_with_config": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _int, ctypes.POINTER(_vp)]),
+    "sgemm_run": (_int, [_vp, _f32, _vp, _vp, _f32, _vp, _vp]),
+    "sgemm_run_host": (_int, [_vp, _f32, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp]),
+    "sgemm_plan_destroy": (_int, [_vp]),
+    "sgemm_plan_describe": (_int, [_vp, ctypes.c_char_p, ctypes.c_size_t]),
+    "sgemm_plan_launches": (_int, [_vp, ctypes.POINTER(_int)]),
+    "sgemm_plan_config_id": (_int, [_vp, ctypes.POINTER(_int)]),
+    "sgemm_num_configs": (_int, []),
+    "sgemm_config_name": (ctypes.c_char_p, [_int]),
+    "sgemm_status_string": (ctypes.c_char_p, [_int]),
+    "sgemm_device_status": (_int, [_int]),
+    "sgemm_set_wait_timeout_ns": (_int, [ctypes.c_uint64]),
+    "sgemm_selftest_wait_timeout": (_int, [ctypes.c_uint64, _vp]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class SgemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libsgemm_gb300.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()' or "
+                    "python dense_fp32_matrix_sm_gb300/build.py). There is no fallback path.")
+            l = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(l, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = l
+    return _lib
+
+
+def status_string(status: int) -> str:
+    s = lib().sgemm_status_string(int(status))
+    return s.decode() if s else f"status {status}"
+
+
+def _check(status: int, where: str):
+    if status != SGEMM_OK:
+        raise SgemmError(status, where)
+
+
+def num_configs() -> int:
+    return int(lib().sgemm_num_configs())
+
+
+def config_name(config_id: int) -> Optional[str]:
+    s = lib().sgemm_config_name(int(config_id))
+    return s.decode() if s else None
+
+
+def config_names():
+    return [config_name(i) for i in range(num_configs())]
+
+
+def config_id(name: str) -> int:
+    names = config_names()
+    if name not in names:
+        raise KeyError(f"unknown variant {name!r}; have {names}")
+    return names.index(name)
+
+
+def device_status(reset: bool = True) -> int:
+    """Read (and clear) the current device's kernel status word: SGEMM_OK or SGEMM_ERR_TIMEOUT."""
+    return int(lib().sgemm_device_status(1 if reset else 0))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _check(lib().sgemm_set_wait_timeout_ns(int(ns)), "sgemm_set_wait_timeout_ns")
+
+
+def selftest_wait_timeout(ns: int, stream=None) -> int:
+    return int(lib().sgemm_selftest_wait_timeout(int(ns), _stream_handle(stream)))
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        try:
+            import torch
+
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream or None
+        except Exception:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream or None
+    return getattr(stream, "cuda_stream", None) or None
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    return x.data_ptr() or None
+
+
+class Plan:
+    """A plan for one (M, N, K, lda, ldb, ldc) on the current CUDA device.
+
+    config: None for the library's per-shape table, or a variant name / id.
+    """
+
+    def __init__(self, M: int, N: int, K: int, lda: Optional[int] = None, ldb: Optional[int] = None,
+                 ldc: Optional[int] = None, config=None):
+        l = lib()
+        self.M, self.N, self.K = int(M), int(N), int(K)
+        self.lda = int(lda) if lda is not None else max(1, self.K)
+        self.ldb = int(ldb) if ldb is not None else max(1, self.N)
+        self.ldc = int(ldc) if ldc is not None else max(1, self.N)
+        h = ctypes.c_void_p()
+        if config is None:
+            st = l.sgemm_plan(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, ctypes.byref(h))
+        else:
+            cid = config if isinstance(config, int) else config_id(config)
+            st = l.sgemm_plan_with_config(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, cid,
+                                          ctypes.byref(h))
+        _check(st, "sgemm_plan")
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def run(self, alpha: float, A, B, beta: float, C, stream=None) -> None:
+        """Enqueue C = alpha*A*B + beta*C.  A, B, C: CUDA tensors (or raw device addresses)."""
+        _check(lib().sgemm_run(self._h, float(alpha), _ptr(A), _ptr(B), float(beta), _ptr(C),
+                               _stream_handle(stream)), "sgemm_run")
+
+    def run_host(self, alpha: float, hA, hB, beta: float, hC, dA, dB, dC, stream=None) -> None:
+        """Host buffers in, host result out: H2D copies, the kernel, D2H copy, all on `stream`."""
+        _check(lib().sgemm_run_host(self._h, float(alpha), _ptr(hA), _ptr(hB), float(beta), _ptr(hC),
+                                    _ptr(dA), _ptr(dB), _ptr(dC), _stream_handle(stream)), "sgemm_run_host")
+
+    def describe(self) -> str:
+        buf = ctypes.create_string_buffer(512)
+        _check(lib().sgemm_plan_describe(self._h, buf, 512), "sgemm_plan_describe")
+        return buf.value.decode()
+
+    def info(self) -> dict:
+        out = {}
+        for tok in self.describe().split():
+            k, _, v = tok.partition("=")
+            out[k] = int(v) if v.lstrip("-").isdigit() else v
+        return out
+
+    @property
+    def launches(self) -> int:
+        n = ctypes.c_int()
+        _check(lib().sgemm_plan_launches(self._h, ctypes.byref(n)), "sgemm_plan_launches")
+        return n.value
+
+    @property
+    def config_id(self) -> int:
+        n = ctypes.c_int()
+        _check(lib().sgemm_plan_config_id(self._h, ctypes.byref(n)), "sgemm_plan_config_id")
+        return n.value
+
+    @property
+    def config_name(self) -> str:
+        return config_name(self.config_id)
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().sgemm_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def _ld(t) -> int:
+    if t.dim() != 2:
+        raise ValueError("expected a 2-D tensor")
+    if t.shape[0] > 0 and t.shape[1] > 0 and t.stride(1) != 1:
+        raise ValueError("rows must be contiguous (stride(1) == 1); row-major layout only")
+    return max(1, t.stride(0), t.shape[1]) if t.shape[0] > 1 else max(1, t.shape[1])
+
+
+def sgemm(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, stream=None, config=None):
+    """C = alpha*A*B + beta*C for row-major float32 CUDA tensors; returns C.
+
+    C is allocated (and beta must be 0) when not given.  Runs on the current
+    stream unless `stream` is given; does not synchronise.
+    """
+    import torch
+
+    for name, t in (("A", A), ("B", B)):
+        if t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{name} must be a float32 CUDA tensor")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {tuple(A.shape)} x {tuple(B.shape)}")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if C.dtype != torch.float32 or not C.is_cuda or tuple(C.shape) != (M, N):
+        raise TypeError("C must be an M x N float32 CUDA tensor")
+    plan = Plan(M, N, K, _ld(A) if K > 0 else 1, _ld(B), _ld(C), config=config)
+    try:
+        plan.run(alpha, A, B, beta, C, stream)
+    finally:
+        plan.close()
+    return C

@@ -1,0 +1,176 @@
+// kernel_generic.cu -- the any-layout SGEMM kernel, the C = beta*C kernel
+// and the wait-limit self-test kernel.
+//
+// The generic kernel takes any alignment and any leading dimension: every
+// global access is a predicated scalar load, so it serves the inputs the
+// TMA-fed kernels cannot (unaligned base pointers, lda or ldb not a
+// multiple of 4).  It is the pages' shared-memory tiled kernel with 2-D
+// register blocking ("Learn: Optimizing GEMM", sections 5 and 6; "Writing a
+// Fast Matmul in CUDA, Step by Step", Steps 3 and 4):
+//  * a 64 x 64 CTA tile, k-slices of 16 staged in shared memory, A stored
+//    transposed (As[k][m], padded by one column so the transposing stores do
+//    not collide in a bank) and B as is;
+//  * 256 threads, each owning a 4 x 4 thread tile at rows ty + 16i and
+//    columns tx + 16j, so a warp's shared reads are broadcasts (A) or 16
+//    consecutive words (B);
+//  * threadIdx maps to the contiguous dimension of every global load and
+//    store ("Learn: Optimizing GEMM", section 4, coalescing);
+//  * the next slice is loaded into registers while the current one is
+//    multiplied (register-staged double buffering).
+// Each output is a chain of fp32 fmas in ascending k, like the TMA kernels.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sgemm {
+namespace {
+
+constexpr int kGBM = 64, kGBN = 64, kGBK = 16, kGThreads = 256;
+
+struct GenericParams {
+  const float* A;
+  const float* B;
+  float* C;
+  int64_t lda, ldb, ldc;
+  int M, N, K;
+  float alpha, beta;
+};
+
+__global__ void __launch_bounds__(kGThreads) sgemm_generic_kernel(const GenericParams p) {
+  __shared__ float As[kGBK][kGBM + 1];
+  __shared__ float Bs[kGBK][kGBN];
+
+  const int tiles_n = (p.N + kGBN - 1) / kGBN;
+  const int tm = blockIdx.x / tiles_n;
+  const int tn = blockIdx.x % tiles_n;
+  const int m0 = tm * kGBM, n0 = tn * kGBN;
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+
+  float ra[4], rb[4];
+  auto load_slice = [&](int k0) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int idx = tid + kGThreads * r;
+      const int am = idx / kGBK, ak = idx % kGBK;  // consecutive threads: consecutive k of one row
+      const int gm = m0 + am, gk = k0 + ak;
+      ra[r] = (gm < p.M && gk < p.K) ? p.A[static_cast<int64_t>(gm) * p.lda + gk] : 0.f;
+      const int bk = idx / kGBN, bn = idx % kGBN;  // consecutive threads: consecutive n
+      const int gkb = k0 + bk, gn = n0 + bn;
+      rb[r] = (gkb < p.K && gn < p.N) ? p.B[static_cast<int64_t>(gkb) * p.ldb + gn] : 0.f;
+    }
+  };
+  auto store_slice = [&]() {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int idx = tid + kGThreads * r;
+      As[idx % kGBK][idx / kGBK] = ra[r];
+      Bs[idx / kGBN][idx % kGBN] = rb[r];
+    }
+  };
+
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+  load_slice(0);
+  for (int k0 = 0; k0 < p.K; k0 += kGBK) {
+    store_slice();
+    __syncthreads();
+    if (k0 + kGBK < p.K) load_slice(k0 + kGBK);
+#pragma unroll
+    for (int k = 0; k < kGBK; ++k) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[k][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[k][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = m0 + ty + 16 * i;
+    if (row >= p.M) continue;
+    float* crow = p.C + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = n0 + tx + 16 * j;
+      if (col < p.N) crow[col] = p.beta == 0.f ? p.alpha * acc[i][j] : fmaf(p.alpha, acc[i][j], p.beta * crow[col]);
+    }
+  }
+}
+
+cudaError_t generic_prepare() { return cudaSuccess; }
+
+cudaError_t generic_occupancy(int* ctas) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, sgemm_generic_kernel, kGThreads, 0);
+}
+
+cudaError_t generic_launch(const LaunchArgs& a, cudaStream_t stream) {
+  GenericParams p{a.A, a.B, a.C, a.lda, a.ldb, a.ldc, a.M, a.N, a.K, a.alpha, a.beta};
+  const int64_t tiles = static_cast<int64_t>((a.M + kGBM - 1) / kGBM) * ((a.N + kGBN - 1) / kGBN);
+  if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  sgemm_generic_kernel<<<static_cast<unsigned>(tiles), kGThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+const Variant kGenericVariants[] = {
+    Variant{"generic_64x64x16", kKindGeneric, kGBM, kGBN, kGBK, 1, 0, kGThreads, 0, 0, &generic_prepare,
+            &generic_occupancy, &generic_launch},
+};
+
+// C = beta*C over an M x N window with row stride ldc; beta == 0 writes zeros
+// without reading C.
+__global__ void scale_kernel(float* C, int64_t ldc, int M, int N, float beta) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = e / N, j = e % N;
+    float* d = C + i * ldc + j;
+    *d = beta == 0.f ? 0.f : beta * *d;
+  }
+}
+
+// One thread waits on phase 0 of a barrier that expects one arrival nobody
+// makes; the wait must give up after timeout_ns and record it.
+__global__ void wait_selftest_kernel(unsigned int* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = ptx::smem_addr(&bar);
+  ptx::mbar_init(b, 1);
+  ptx::fence_barrier_init();
+  if (!ptx::mbar_wait(b, 0, timeout_ns)) atomicOr(status, kStatusTimeoutSelftest);
+}
+
+}  // namespace
+
+const Variant* generic_variants(int* count) {
+  *count = static_cast<int>(sizeof(kGenericVariants) / sizeof(kGenericVariants[0]));
+  return kGenericVariants;
+}
+
+cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  int blocks = static_cast<int>((total + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  scale_kernel<<<blocks, 256, 0, stream>>>(C, ldc, M, N, beta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace sgemm

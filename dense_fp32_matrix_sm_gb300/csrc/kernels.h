@@ -1,0 +1,69 @@
+// kernels.h -- host-side interface between the C-ABI layer (sgemm_api.cu)
+// and the kernel translation units.  Internal; not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sgemm {
+
+enum VariantKind : int {
+  kKindGeneric = 0,  // scalar predicated loads, any alignment / leading dimension
+  kKindTma = 1,      // TMA-fed multi-stage pipeline, needs 16-byte aligned A/B rows
+  kKindSkinny = 2,   // small-M streaming kernel, needs 16-byte aligned A/B rows
+};
+
+// Everything one launch needs.  Tensor maps are encoded by the caller per
+// run (they hold the A/B addresses) and passed by value to the kernel.
+struct LaunchArgs {
+  const float* A;
+  const float* B;
+  float* C;
+  int64_t lda, ldb, ldc;
+  int M, N, K;
+  float alpha, beta;
+  CUtensorMap tmA;       // used by TMA-fed variants only
+  CUtensorMap tmB;
+  int grid;              // CTAs to launch (persistent variants: <= tiles)
+  int split_k;           // skinny variant: CTAs per cluster along K
+  unsigned int* status;  // per-device status word (error bits)
+  uint64_t timeout_ns;   // limit for every in-kernel wait
+};
+
+struct Variant {
+  const char* name;
+  int kind;
+  int bm, bn, bk;        // CTA tile (bk: k-slice per pipeline stage)
+  int stages;            // shared-memory pipeline depth (1 = register-staged)
+  int ffma2;             // 1: inner product issued as paired fp32 FMAs
+  int threads;           // threads per CTA
+  int smem_bytes;        // dynamic shared memory per CTA
+  int tma_swizzle_a;     // 0 none, 128: A tile uses the 128-byte swizzle
+  // set kernel attributes for the current device (idempotent)
+  cudaError_t (*prepare)();
+  // resident CTAs per SM for this variant on the current device
+  cudaError_t (*occupancy)(int* ctas_per_sm);
+  cudaError_t (*launch)(const LaunchArgs& args, cudaStream_t stream);
+};
+
+// Variant tables, one per kernel translation unit.
+const Variant* generic_variants(int* count);
+const Variant* tma_variants(int* count);
+const Variant* skinny_variants(int* count);
+
+// C = beta * C (K == 0 or alpha == 0), any leading dimension.
+cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaStream_t stream);
+
+// One-thread kernel that waits on a barrier phase nothing completes.
+cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream);
+
+// Status bits written by kernels.
+enum : unsigned int {
+  kStatusTimeoutFull = 1u,    // a consumer gave up waiting for a filled stage
+  kStatusTimeoutEmpty = 2u,   // the producer gave up waiting for a free stage
+  kStatusTimeoutSelftest = 4u,
+  kStatusTimeoutCluster = 8u,
+};
+
+}  // namespace sgemm

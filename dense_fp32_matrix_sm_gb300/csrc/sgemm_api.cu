@@ -1,0 +1,406 @@
+// sgemm_api.cu -- the C ABI declared in include/sgemm.h: argument checks,
+// the per-shape config table, TMA descriptor encoding, launches, the
+// per-device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "kernels.h"
+#include "sgemm.h"
+
+using namespace sgemm;
+
+struct sgemm_plan_s {
+  int64_t M, N, K, lda, ldb, ldc;
+  int device;
+  int num_sms;
+  int config_id;
+  int generic_id;   // scalar-load variant used when A or B is not 16-byte aligned
+  int ctas_per_sm;
+  int grid;
+  int64_t tiles;
+};
+
+// Per-device status word written by kernels (timeouts).  Its device address
+// is looked up once per device with that device current.
+__device__ unsigned int g_sgemm_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
+
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+std::mutex g_status_mutex;
+unsigned int* g_status_addr[kMaxDevices] = {};
+
+struct Registry {
+  std::vector<const Variant*> all;
+  int first_generic = -1;
+  Registry() {
+    int n = 0;
+    const Variant* v = generic_variants(&n);
+    first_generic = static_cast<int>(all.size());
+    for (int i = 0; i < n; ++i) all.push_back(&v[i]);
+    v = tma_variants(&n);
+    for (int i = 0; i < n; ++i) all.push_back(&v[i]);
+    v = skinny_variants(&n);
+    for (int i = 0; i < n; ++i) all.push_back(&v[i]);
+  }
+};
+
+const Registry& registry() {
+  static Registry r;
+  return r;
+}
+
+int find_variant(const char* name) {
+  const Registry& r = registry();
+  for (size_t i = 0; i < r.all.size(); ++i)
+    if (strcmp(r.all[i]->name, name) == 0) return static_cast<int>(i);
+  return -1;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+sgemm_status_t status_addr(int device, unsigned int** out) {
+  if (device < 0 || device >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_status_mutex);
+  if (!g_status_addr[device]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sgemm_status_word) != cudaSuccess) return SGEMM_ERR_CUDA;
+    g_status_addr[device] = static_cast<unsigned int*>(p);
+  }
+  *out = g_status_addr[device];
+  return SGEMM_OK;
+}
+
+sgemm_status_t check_dims(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc) {
+  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1)) return SGEMM_ERR_INVALID_ARG;
+  const int64_t lim = 0x7fffffff;
+  if (M > lim || N > lim || K > lim) return SGEMM_ERR_UNSUPPORTED;
+  // element offsets must fit in int64 with room to spare
+  if (lda > (int64_t(1) << 40) || ldb > (int64_t(1) << 40) || ldc > (int64_t(1) << 40)) return SGEMM_ERR_UNSUPPORTED;
+  return SGEMM_OK;
+}
+
+bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb) {
+  (void)N;
+  (void)K;
+  if (v->kind == kKindGeneric) return true;
+  if (lda % 4 != 0 || ldb % 4 != 0) return false;  // TMA row strides must be multiples of 16 bytes
+  if (v->kind == kKindSkinny) return M <= v->bm;
+  return true;
+}
+
+// The per-shape config table.  Keys are shape classes; values are variant
+// names.  The entries come from the measured sweeps on GB300.
+const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms) {
+  (void)K;
+  (void)num_sms;
+  if (lda % 4 != 0 || ldb % 4 != 0) return "generic_64x64x16";
+  if (M <= 32 && find_variant("skinny_16") >= 0 && M <= 16) return "skinny_16";
+  if (M * N <= 256 * 256) return "tma_128x64x32_s4_ffma2";
+  return "tma_128x128x32_s4_ffma2";
+}
+
+sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int config_id,
+                         sgemm_plan_t* out) {
+  if (!out) return SGEMM_ERR_INVALID_ARG;
+  sgemm_status_t st = check_dims(M, N, K, lda, ldb, ldc);
+  if (st != SGEMM_OK) return st;
+  const Registry& reg = registry();
+  if (config_id >= static_cast<int>(reg.all.size())) return SGEMM_ERR_INVALID_ARG;
+
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return SGEMM_ERR_CUDA;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return SGEMM_ERR_CUDA;
+
+  if (config_id < 0) {
+    const char* forced = getenv("SGEMM_FORCE_CONFIG");
+    if (forced && *forced) {
+      config_id = find_variant(forced);
+      if (config_id < 0) return SGEMM_ERR_INVALID_ARG;
+    } else {
+      config_id = find_variant(table_choice(M, N, K, lda, ldb, sms));
+      if (config_id < 0) config_id = reg.first_generic;
+    }
+  }
+  const Variant* v = reg.all[config_id];
+  if (!variant_supports(v, M, N, K, lda, ldb)) return SGEMM_ERR_UNSUPPORTED;
+  if (v->kind != kKindGeneric && !encode_fn()) return SGEMM_ERR_CUDA;
+
+  unsigned int* status = nullptr;
+  st = status_addr(device, &status);
+  if (st != SGEMM_OK) return st;
+
+  if (v->prepare() != cudaSuccess) return SGEMM_ERR_CUDA;
+  int ctas = 0;
+  if (v->occupancy(&ctas) != cudaSuccess || ctas < 1) return SGEMM_ERR_CUDA;
+  const Variant* gv = reg.all[reg.first_generic];
+  if (gv->prepare() != cudaSuccess) return SGEMM_ERR_CUDA;
+
+  sgemm_plan_s* p = new (std::nothrow) sgemm_plan_s;
+  if (!p) return SGEMM_ERR_NOMEM;
+  p->M = M;
+  p->N = N;
+  p->K = K;
+  p->lda = lda;
+  p->ldb = ldb;
+  p->ldc = ldc;
+  p->device = device;
+  p->num_sms = sms;
+  p->config_id = config_id;
+  p->generic_id = reg.first_generic;
+  p->ctas_per_sm = ctas;
+  p->tiles = ((M + v->bm - 1) / v->bm) * ((N + v->bn - 1) / v->bn);
+  int64_t grid = p->tiles;
+  if (v->kind == kKindTma) {
+    const int64_t slots = static_cast<int64_t>(sms) * ctas;
+    if (grid > slots) grid = slots;
+  }
+  p->grid = static_cast<int>(grid > 0x7fffffff ? 0x7fffffff : grid);
+  *out = p;
+  return SGEMM_OK;
+}
+
+sgemm_status_t encode_maps(const Variant* v, const sgemm_plan_s* p, const float* A, const float* B,
+                           LaunchArgs* a) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return SGEMM_ERR_CUDA;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->lda) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(v->bk), static_cast<cuuint32_t>(v->bm)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&a->tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     v->tma_swizzle_a == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->N), static_cast<cuuint64_t>(p->K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->ldb) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(v->bn), static_cast<cuuint32_t>(v->bk)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&a->tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
+  }
+  return SGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sgemm_status_t sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                          sgemm_plan_t* out) {
+  return make_plan(M, N, K, lda, ldb, ldc, -1, out);
+}
+
+sgemm_status_t sgemm_plan_with_config(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                      int config_id, sgemm_plan_t* out) {
+  if (config_id < 0) return SGEMM_ERR_INVALID_ARG;
+  return make_plan(M, N, K, lda, ldb, ldc, config_id, out);
+}
+
+sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const float* B, float beta, float* C,
+                         void* stream_) {
+  if (!plan) return SGEMM_ERR_INVALID_ARG;
+  const sgemm_plan_s* p = plan;
+  if (p->M == 0 || p->N == 0) return SGEMM_OK;
+  if (!C) return SGEMM_ERR_INVALID_ARG;
+  const bool product = p->K > 0 && alpha != 0.f;
+  if (product && (!A || !B)) return SGEMM_ERR_INVALID_ARG;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) return SGEMM_ERR_CUDA;
+  if (device != p->device) return SGEMM_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+  if (!product) {
+    return launch_scale(C, p->ldc, static_cast<int>(p->M), static_cast<int>(p->N), beta, stream) == cudaSuccess
+               ? SGEMM_OK
+               : SGEMM_ERR_CUDA;
+  }
+
+  const Registry& reg = registry();
+  const Variant* v = reg.all[p->config_id];
+  int grid = p->grid;
+  if (v->kind != kKindGeneric &&
+      ((reinterpret_cast<uintptr_t>(A) & 15) != 0 || (reinterpret_cast<uintptr_t>(B) & 15) != 0)) {
+    v = reg.all[p->generic_id];
+    grid = 0;
+  }
+
+  LaunchArgs a;
+  memset(&a, 0, sizeof(a));
+  a.A = A;
+  a.B = B;
+  a.C = C;
+  a.lda = p->lda;
+  a.ldb = p->ldb;
+  a.ldc = p->ldc;
+  a.M = static_cast<int>(p->M);
+  a.N = static_cast<int>(p->N);
+  a.K = static_cast<int>(p->K);
+  a.alpha = alpha;
+  a.beta = beta;
+  a.grid = grid;
+  a.split_k = 1;
+  a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  sgemm_status_t st = status_addr(device, &a.status);
+  if (st != SGEMM_OK) return st;
+  if (v->kind != kKindGeneric) {
+    st = encode_maps(v, p, A, B, &a);
+    if (st != SGEMM_OK) return st;
+  }
+  return v->launch(a, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+
+sgemm_status_t sgemm_run_host(sgemm_plan_t plan, float alpha, const float* hA, const float* hB, float beta,
+                              float* hC, float* dA, float* dB, float* dC, void* stream_) {
+  if (!plan) return SGEMM_ERR_INVALID_ARG;
+  const sgemm_plan_s* p = plan;
+  if (p->M == 0 || p->N == 0) return SGEMM_OK;
+  if (!hC || !dC) return SGEMM_ERR_INVALID_ARG;
+  const bool product = p->K > 0 && alpha != 0.f;
+  if (product && (!hA || !hB || !dA || !dB)) return SGEMM_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const size_t fs = sizeof(float);
+  if (product) {
+    if (cudaMemcpy2DAsync(dA, p->lda * fs, hA, p->lda * fs, p->K * fs, p->M, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+      return SGEMM_ERR_CUDA;
+    if (cudaMemcpy2DAsync(dB, p->ldb * fs, hB, p->ldb * fs, p->N * fs, p->K, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+      return SGEMM_ERR_CUDA;
+  }
+  if (beta != 0.f) {
+    if (cudaMemcpy2DAsync(dC, p->ldc * fs, hC, p->ldc * fs, p->N * fs, p->M, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+      return SGEMM_ERR_CUDA;
+  }
+  sgemm_status_t st = sgemm_run(plan, alpha, dA, dB, beta, dC, stream_);
+  if (st != SGEMM_OK) return st;
+  if (cudaMemcpy2DAsync(hC, p->ldc * fs, dC, p->ldc * fs, p->N * fs, p->M, cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return SGEMM_ERR_CUDA;
+  return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_plan_destroy(sgemm_plan_t plan) {
+  delete plan;
+  return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
+  if (!plan || !buf || n == 0) return SGEMM_ERR_INVALID_ARG;
+  const Variant* v = registry().all[plan->config_id];
+  snprintf(buf, n,
+           "variant=%s kind=%s tile=%dx%dx%d stages=%d ffma2=%d threads=%d smem=%d grid=%d ctas_per_sm=%d "
+           "tiles=%lld sms=%d k_order=sequential M=%lld N=%lld K=%lld",
+           v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : "skinny", v->bm, v->bn,
+           v->bk, v->stages, v->ffma2, v->threads, v->smem_bytes, plan->grid, plan->ctas_per_sm,
+           static_cast<long long>(plan->tiles), plan->num_sms, static_cast<long long>(plan->M),
+           static_cast<long long>(plan->N), static_cast<long long>(plan->K));
+  return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_plan_launches(sgemm_plan_t plan, int* out) {
+  if (!plan || !out) return SGEMM_ERR_INVALID_ARG;
+  *out = (plan->M == 0 || plan->N == 0) ? 0 : 1;
+  return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_plan_config_id(sgemm_plan_t plan, int* out) {
+  if (!plan || !out) return SGEMM_ERR_INVALID_ARG;
+  *out = plan->config_id;
+  return SGEMM_OK;
+}
+
+int sgemm_num_configs(void) { return static_cast<int>(registry().all.size()); }
+
+const char* sgemm_config_name(int config_id) {
+  const Registry& r = registry();
+  if (config_id < 0 || config_id >= static_cast<int>(r.all.size())) return nullptr;
+  return r.all[config_id]->name;
+}
+
+const char* sgemm_status_string(sgemm_status_t s) {
+  switch (s) {
+    case SGEMM_OK: return "SGEMM_OK";
+    case SGEMM_ERR_INVALID_ARG: return "SGEMM_ERR_INVALID_ARG: bad dimension, leading dimension, pointer or id";
+    case SGEMM_ERR_UNSUPPORTED: return "SGEMM_ERR_UNSUPPORTED: valid but not handled by this build";
+    case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: a CUDA call failed";
+    case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a kernel wait ran past its time limit";
+    case SGEMM_ERR_NOMEM: return "SGEMM_ERR_NOMEM: host allocation failed";
+  }
+  return "unknown sgemm status";
+}
+
+sgemm_status_t sgemm_device_status(int reset) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return SGEMM_ERR_CUDA;
+  unsigned int* addr = nullptr;
+  sgemm_status_t st = status_addr(device, &addr);
+  if (st != SGEMM_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, addr, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SGEMM_ERR_CUDA;
+  if (reset && v != 0) {
+    if (cudaMemset(addr, 0, sizeof(v)) != cudaSuccess) return SGEMM_ERR_CUDA;
+  }
+  return v ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
+}
+
+sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns) {
+  g_timeout_ns.store(timeout_ns ? timeout_ns : kDefaultTimeoutNs, std::memory_order_relaxed);
+  return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_selftest_wait_timeout(uint64_t timeout_ns, void* stream_) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return SGEMM_ERR_CUDA;
+  unsigned int* addr = nullptr;
+  sgemm_status_t st = status_addr(device, &addr);
+  if (st != SGEMM_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (launch_wait_selftest(addr, timeout_ns, stream) != cudaSuccess) return SGEMM_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SGEMM_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, addr, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SGEMM_ERR_CUDA;
+  if (!(v & kStatusTimeoutSelftest)) return SGEMM_OK;
+  if (cudaMemset(addr, 0, sizeof(v)) != cudaSuccess) return SGEMM_ERR_CUDA;
+  return SGEMM_ERR_TIMEOUT;
+}
+
+}  // extern "C"

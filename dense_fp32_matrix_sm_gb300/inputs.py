@@ -150,3 +150,34 @@ def sample_entries(M: int, N: int, n: int, seed: int, tile_m: int = 128, tile_n:
     c = np.concatenate(cols)
     key = np.unique(r * N + c)
     return key // N, key % N
+
+
+def _sample_line(L: int, n: int, rng: np.random.Generator, tile: int) -> np.ndarray:
+    """Up to n distinct indices in [0, L): both ends, one inside every tile
+    of size `tile` (evenly thinned if there are more tiles than n/2), the
+    rest uniform."""
+    if n >= L:
+        return np.arange(L, dtype=np.int64)
+    picks = {0, L - 1}
+    if L > 2:
+        picks.add(L - 2)
+    tiles = (L + tile - 1) // tile
+    chosen = range(tiles) if tiles <= n // 2 else np.linspace(0, tiles - 1, n // 2).astype(int)
+    for t in chosen:
+        picks.add(int(min(L - 1, t * tile + rng.integers(0, tile))))
+    while len(picks) < n:
+        picks.update(int(x) for x in rng.integers(0, L, size=n - len(picks)))
+    return np.array(sorted(picks)[:n] if len(picks) > n else sorted(picks), dtype=np.int64)
+
+
+def sample_rows_cols(M: int, N: int, n_rows: int = 256, n_cols: int = 256, seed: int = 0,
+                     tile_m: int = 128, tile_n: int = 128):
+    """Row and column index sets whose cross product is a large-size parity
+    sample (256 x 256 = 65,536 entries by default).  Both ends and one index
+    inside every edge tile are always present.  Every entry (i, j) depends
+    only on row i of A and column j of B, so the oracle can compute the whole
+    sample as one small product A[rows] x B[:, cols]."""
+    rng = np.random.default_rng(seed + 1000)
+    if M <= n_rows:
+        n_cols = max(n_cols, (n_rows * n_cols) // max(1, M))
+    return _sample_line(M, n_rows, rng, tile_m), _sample_line(N, n_cols, rng, tile_n)

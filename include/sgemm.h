@@ -1,0 +1,152 @@
+/*
+ * sgemm.h -- C ABI of the GB300 FP32 SGEMM library (libsgemm_gb300.so).
+ *
+ * The operation (all entry points): C = alpha * A * B + beta * C on
+ * row-major float32 matrices, A is M x K, B is K x N, C is M x N; element
+ * [i][j] of a matrix with leading dimension ld sits at base + i*ld + j.
+ *   -- "How a Matmul Kernel Gets Fast", section 1 "The problem, and what
+ *      cuBLAS is" (GEMM is C = alpha*A*B + beta*C);
+ *   -- "Learn: Optimizing GEMM", section 3 "Rung 0 -- Naive (recap)" (the
+ *      row-major layout and one output as a length-K dot product scaled by
+ *      alpha, plus beta times the old C).
+ *
+ * Arithmetic: IEEE float32 fused multiply-adds on the CUDA cores, each
+ * output summed in ascending k unless the plan's description says
+ * "k_order=split" (a split-K plan adds fixed-order partial sums).  The
+ * epilogue is out = alpha*acc (beta == 0) or fmaf(alpha, acc, beta*C_old).
+ *
+ * Conventions (BLAS readings where the pages are silent):
+ *   - lda >= max(1, K), ldb >= max(1, N), ldc >= max(1, N), else
+ *     SGEMM_ERR_INVALID_ARG.  Dimensions above 2^31 - 1 give
+ *     SGEMM_ERR_UNSUPPORTED.
+ *   - M == 0 or N == 0: nothing is launched, SGEMM_OK.
+ *   - K == 0 or alpha == 0: C = beta * C; A and B are not read.
+ *   - beta == 0: C is not read (NaN or garbage in C does not propagate).
+ *   - A, B and C must not overlap; the library does not check this.
+ *   - Any alignment and any leading dimension is accepted.  Fast paths
+ *     need A and B 16-byte aligned with lda % 4 == 0 and ldb % 4 == 0; other
+ *     inputs run a GPU kernel with scalar loads (there is no CPU path).
+ *
+ * Memory and threads: A, B and C are DEVICE pointers owned by the caller,
+ * on the device that was current when the plan was made.  sgemm_run only
+ * enqueues work on `stream` (a cudaStream_t; NULL is the legacy default
+ * stream) and returns; results are ready when the stream reaches that point.
+ * A plan is immutable after sgemm_plan returns and may be used from several
+ * host threads and streams at once.  No entry point allocates device
+ * memory inside sgemm_run.
+ *
+ * Errors: every entry point returns a status and never aborts.  Launch
+ * failures map to SGEMM_ERR_CUDA.  Faults during execution surface at the
+ * caller's next synchronisation, as with any CUDA launch.  Every wait inside
+ * a kernel has a time limit (default 4 s, see sgemm_set_wait_timeout_ns);
+ * a wait that runs out records SGEMM_ERR_TIMEOUT in a per-device status
+ * word that sgemm_device_status reads.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct sgemm_plan_s *sgemm_plan_t;
+
+typedef enum {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_ARG = -1,  /* bad dimension, leading dimension, pointer or id */
+    SGEMM_ERR_UNSUPPORTED = -2,  /* valid but outside what this build handles */
+    SGEMM_ERR_CUDA = -3,         /* a CUDA runtime or driver call failed */
+    SGEMM_ERR_TIMEOUT = -4,      /* a kernel wait ran past its time limit */
+    SGEMM_ERR_NOMEM = -5         /* host allocation failed */
+} sgemm_status_t;
+
+/*
+ * Make a plan for one problem shape on the current device: validates the
+ * dimensions, picks a kernel variant from the per-shape config table
+ * (measured on GB300) and prepares it.  Allocates only host memory.
+ * The environment variable SGEMM_FORCE_CONFIG=<variant name> overrides the
+ * table choice.  *out is set only on SGEMM_OK.
+ */
+sgemm_status_t sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                          sgemm_plan_t *out);
+
+/*
+ * As sgemm_plan, but with variant `config_id` (0 .. sgemm_num_configs()-1)
+ * instead of the table's choice.  SGEMM_ERR_UNSUPPORTED if that variant
+ * cannot run this shape (for example a skinny-M variant with large M).
+ */
+sgemm_status_t sgemm_plan_with_config(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                      int64_t ldc, int config_id, sgemm_plan_t *out);
+
+/*
+ * Enqueue C = alpha*A*B + beta*C on `stream` (a cudaStream_t, may be NULL).
+ * A, B, C are device pointers with the plan's shape and leading dimensions.
+ * A and B may be NULL only when K == 0 or alpha == 0; C may be NULL only
+ * when M == 0 or N == 0.  If A or B is not 16-byte aligned, a variant that
+ * needs alignment falls back to the scalar-load kernel for this call.
+ */
+sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float *A, const float *B, float beta,
+                         float *C, void *stream);
+
+/*
+ * The same product from HOST buffers: copies hA and hB (and hC when
+ * beta != 0) into the caller's device buffers dA, dB, dC with
+ * cudaMemcpyAsync, runs sgemm_run on them, and copies dC back into hC, all
+ * on `stream`; returns after enqueueing (synchronise the stream before
+ * reading hC).  Host matrices are dense with the plan's leading
+ * dimensions.  Pinned host memory makes the copies asynchronous.
+ */
+sgemm_status_t sgemm_run_host(sgemm_plan_t plan, float alpha, const float *hA, const float *hB,
+                              float beta, float *hC, float *dA, float *dB, float *dC, void *stream);
+
+/* Free a plan (host memory only).  NULL is accepted. */
+sgemm_status_t sgemm_plan_destroy(sgemm_plan_t plan);
+
+/*
+ * Write a one-line description of the plan's choice into buf (at most n
+ * bytes, NUL-terminated): variant name, tile sizes, grid, k order.
+ */
+sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char *buf, size_t n);
+
+/* Number of kernel launches one sgemm_run of this plan makes (into *out). */
+sgemm_status_t sgemm_plan_launches(sgemm_plan_t plan, int *out);
+
+/* The chosen variant's id (into *out). */
+sgemm_status_t sgemm_plan_config_id(sgemm_plan_t plan, int *out);
+
+/* Number of kernel variants in this build, and the name of one. */
+int sgemm_num_configs(void);
+const char *sgemm_config_name(int config_id);
+
+/* Static text for a status code. */
+const char *sgemm_status_string(sgemm_status_t status);
+
+/*
+ * Read (and with reset != 0, clear) the current device's kernel status
+ * word.  Synchronises the device.  Returns SGEMM_OK, SGEMM_ERR_TIMEOUT if a
+ * kernel wait ran out since the last reset, or SGEMM_ERR_CUDA.
+ */
+sgemm_status_t sgemm_device_status(int reset);
+
+/*
+ * Time limit, in nanoseconds, for every wait inside the library's kernels
+ * on later launches (process-wide; default 4e9).  0 restores the default.
+ */
+sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/*
+ * Self-test of the wait limit: launches one thread that waits, with limit
+ * timeout_ns, on a barrier phase that nothing completes, then synchronises
+ * the stream.  Returns SGEMM_ERR_TIMEOUT (and clears the status word) when
+ * the wait gave up as designed; SGEMM_OK would mean the wait never ran out.
+ */
+sgemm_status_t sgemm_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

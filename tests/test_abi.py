@@ -1,0 +1,94 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/*.h declares, and rejects bad arguments before it
+touches CUDA."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_fp32_matrix_sm_gb300 import build as b
+
+    b.build()
+    import dense_fp32_matrix_sm_gb300 as s
+
+    return s.lib()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b(sgemm_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert "sgemm_plan" in declared and "sgemm_run" in declared
+    missing = [n for n in sorted(declared) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_header():
+    from dense_fp32_matrix_sm_gb300._lib import SIGNATURES
+
+    assert set(SIGNATURES) == _declared_functions()
+
+
+def test_invalid_arguments_rejected_without_gpu(lib):
+    h = ctypes.c_void_p()
+    bad = [
+        (-1, 4, 4, 4, 4, 4),    # negative M
+        (4, -1, 4, 4, 4, 4),    # negative N
+        (4, 4, -2, 4, 4, 4),    # negative K
+        (4, 4, 8, 7, 4, 4),     # lda < K
+        (4, 8, 4, 4, 7, 8),     # ldb < N
+        (4, 8, 4, 4, 8, 7),     # ldc < N
+        (4, 4, 0, 0, 4, 4),     # lda < 1
+    ]
+    for args in bad:
+        assert lib.sgemm_plan(*args, ctypes.byref(h)) == -1, args
+        assert not h.value
+    assert lib.sgemm_plan(2 ** 31, 4, 4, 4, 4, 4, ctypes.byref(h)) == -2
+    assert lib.sgemm_plan(4, 4, 4, 4, 4, 4, None) == -1
+    assert lib.sgemm_plan_with_config(4, 4, 4, 4, 4, 4, -1, ctypes.byref(h)) == -1
+    assert lib.sgemm_plan_with_config(4, 4, 4, 4, 4, 4, 10 ** 6, ctypes.byref(h)) == -1
+    # run / describe / destroy on a NULL plan
+    assert lib.sgemm_run(None, 1.0, None, None, 0.0, None, None) == -1
+    assert lib.sgemm_run_host(None, 1.0, None, None, 0.0, None, None, None, None, None) == -1
+    assert lib.sgemm_plan_describe(None, ctypes.create_string_buffer(8), 8) == -1
+    assert lib.sgemm_plan_destroy(None) == 0
+
+
+def test_status_strings_and_configs(lib):
+    import dense_fp32_matrix_sm_gb300 as s
+
+    for code in (0, -1, -2, -3, -4, -5):
+        assert s.status_string(code).startswith("SGEMM_")
+    assert "unknown" in s.status_string(7)
+    names = s.config_names()
+    assert len(names) == s.num_configs() >= 2
+    assert len(set(names)) == len(names)
+    assert names[0].startswith("generic")
+    assert any(n.startswith("tma_") for n in names)
+    assert s.config_name(-1) is None
+    assert lib.sgemm_set_wait_timeout_ns(0) == 0
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The library package never imports the oracle and has no CPU path."""
+    pkg = os.path.join(ROOT, "dense_fp32_matrix_sm_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*.py"), recursive=True):
+        text = open(path).read()
+        assert "import oracle" not in text and "from oracle" not in text, path
+        assert "torch.matmul" not in text and "np.matmul" not in text, path

@@ -1,0 +1,312 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bar (elementwise): |C_gpu - C_ref| <= 4*K*2^-24*(|A||B|)_ij + 1e-6.
+Full comparison up to 1024^3-sized work; above that, a 65,536-entry
+cross-product sample (rows x columns that always include both ends and one
+index inside every edge tile).  Kernels that keep ascending-k order are also
+compared bit for bit against the float32 fused-multiply-add chain when
+alpha = 1 and beta = 0.
+"""
+import numpy as np
+import pytest
+
+from dense_fp32_matrix_sm_gb300.inputs import (WORKLOADS, make_inputs, sample_rows_cols,
+                                               workload_inputs)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+BOUND_ABS = 1e-6
+
+
+def _bound(K, S):
+    return 4.0 * K * 2.0 ** -24 * S + BOUND_ABS
+
+
+@pytest.fixture(scope="module")
+def sg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_fp32_matrix_sm_gb300 import build as b
+
+    b.build()
+    import dense_fp32_matrix_sm_gb300 as s
+
+    s.lib()
+    return s
+
+
+def _to_dev(x, ld=None, offset=0, fill=0.0):
+    """Copy a 2-D float32 array to a device buffer with row stride ld
+    (>= cols), starting `offset` floats into the allocation.  Returns
+    (buffer, view-pointer, ld)."""
+    rows, cols = x.shape
+    ld = ld or max(1, cols)
+    n = offset + (rows - 1) * ld + cols if rows > 0 else offset + 1
+    buf = torch.full((max(n, 1),), fill, dtype=torch.float32, device="cuda")
+    if rows > 0 and cols > 0:
+        host = torch.full((max(n, 1),), fill, dtype=torch.float32)
+        view = host[offset:offset + rows * ld].view(rows, ld) if rows * ld + offset <= host.numel() else None
+        if view is None:
+            for r in range(rows):
+                host[offset + r * ld: offset + r * ld + cols] = torch.from_numpy(x[r])
+        else:
+            view[:, :cols] = torch.from_numpy(x)
+        buf.copy_(host)
+    return buf, buf.data_ptr() + 4 * offset, ld
+
+
+def _from_dev(buf, rows, cols, ld, offset=0):
+    host = buf.cpu().numpy()
+    out = np.empty((rows, cols), np.float32)
+    for r in range(rows):
+        out[r] = host[offset + r * ld: offset + r * ld + cols]
+    return out
+
+
+def run_gpu(sg, A, B, C0, alpha, beta, config=None, lda=None, ldb=None, ldc=None, off_a=0, off_b=0,
+            off_c=0, c_fill=None):
+    M, K = A.shape
+    N = B.shape[1]
+    dA, pA, lda = _to_dev(A, lda, off_a)
+    dB, pB, ldb = _to_dev(B, ldb, off_b)
+    c_src = C0 if c_fill is None else np.full((M, N), c_fill, np.float32)
+    dC, pC, ldc = _to_dev(c_src, ldc, off_c)
+    plan = sg.Plan(M, N, K, lda, ldb, ldc, config=config)
+    plan.run(alpha, pA, pB, beta, pC)
+    torch.cuda.synchronize()
+    assert sg.device_status() == sg.SGEMM_OK
+    out = _from_dev(dC, M, N, ldc, off_c)
+    name = plan.config_name
+    plan.close()
+    return out, name
+
+
+def assert_parity(C, Cref, S, K, what=""):
+    C = C.astype(np.float64)
+    assert C.shape == Cref.shape
+    finite = np.isfinite(Cref)
+    assert np.array_equal(np.isfinite(C), finite), f"{what}: non-finite mismatch"
+    err = np.abs(C - Cref)[finite]
+    bnd = _bound(K, S)[finite]
+    bad = err > bnd
+    if bad.any():
+        idx = np.argmax(err / bnd)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} entries outside the bound; worst "
+                             f"err {err[idx]:.3e} vs bound {bnd[idx]:.3e}")
+
+
+def _variants(sg):
+    return sg.config_names()
+
+
+# ---- small and ragged shapes, every variant, full comparison ------------------
+
+SWEEP = [1, 2, 3, 4, 5, 7, 8, 15, 16, 17, 31, 33, 63, 65, 127, 129, 255, 257]
+
+
+def _shape_cases(n=40, seed=0):
+    rng = np.random.default_rng(seed)
+    cases = {(1, 1, 1), (257, 257, 257), (1, 257, 257), (257, 1, 257), (257, 257, 1), (128, 128, 128),
+             (129, 127, 33), (16, 300, 129)}
+    while len(cases) < n:
+        cases.add(tuple(int(x) for x in rng.choice(SWEEP, 3)))
+    return sorted(cases)
+
+
+@pytest.mark.parametrize("variant_idx", range(8))
+def test_shape_sweep_every_variant(sg, oracle_mod, variant_idx):
+    names = _variants(sg)
+    if variant_idx >= len(names):
+        pytest.skip("fewer variants in this build")
+    name = names[variant_idx]
+    for (M, N, K) in _shape_cases(36, seed=variant_idx):
+        for alpha, beta in ((1.0, 0.0), (0.5, 3.0)):
+            A, B, C0 = make_inputs(M, N, K, seed=M * 7 + N * 3 + K, dist_a=("normal", 1.0),
+                                   dist_b=("uniform", 1.0))
+            try:
+                # row strides padded to multiples of 4 so the TMA variants accept every shape
+                C, used = run_gpu(sg, A, B, C0, alpha, beta, config=name, lda=(K + 3) // 4 * 4 or 4,
+                                  ldb=(N + 3) // 4 * 4)
+            except sg.SgemmError as e:
+                if e.status == sg.SGEMM_ERR_UNSUPPORTED:
+                    break
+                raise
+            Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
+            assert_parity(C, Cref, S, K, f"{name} {M}x{N}x{K} a={alpha} b={beta}")
+            if alpha == 1.0 and beta == 0.0:
+                ii, jj = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+                chain = oracle_mod.fp32_chain_entries(A, B, ii.ravel(), jj.ravel()).reshape(M, N)
+                assert np.array_equal(C, chain), f"{name} {M}x{N}x{K}: not the ascending-k fp32 chain"
+
+
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (1000, 1100, 999), (300, 2000, 517)])
+def test_medium_full_compare(sg, oracle_mod, shape):
+    M, N, K = shape
+    A, B, C0 = make_inputs(M, N, K, seed=sum(shape), dist_a=("normal", 1.0), dist_b=("normal", 1.0))
+    Cref, S = oracle_mod.sgemm_ref(A, B, C0, 0.5, 3.0)
+    C, _ = run_gpu(sg, A, B, C0, 0.5, 3.0)
+    assert_parity(C, Cref, S, K, f"table {shape}")
+
+
+# ---- layouts: leading dimensions, misaligned pointers, guard bands ------------
+
+@pytest.mark.parametrize("lds", [(0, 0, 0), (4, 8, 12), (1, 0, 0), (0, 3, 0), (0, 0, 5), (7, 9, 11)])
+def test_leading_dimensions(sg, oracle_mod, lds):
+    M, N, K = 200, 190, 150
+    A, B, C0 = make_inputs(M, N, K, seed=3)
+    Cref, S = oracle_mod.sgemm_ref(A, B, C0, 1.5, -0.5)
+    C, used = run_gpu(sg, A, B, C0, 1.5, -0.5, lda=K + lds[0], ldb=N + lds[1], ldc=N + lds[2])
+    assert_parity(C, Cref, S, K, f"ld pads {lds} ({used})")
+    if lds[0] % 4 or lds[1] % 4:
+        assert used.startswith("generic")
+
+
+@pytest.mark.parametrize("offs", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (2, 3, 1)])
+def test_misaligned_pointers(sg, oracle_mod, offs):
+    M, N, K = 140, 260, 96
+    A, B, C0 = make_inputs(M, N, K, seed=5)
+    Cref, S = oracle_mod.sgemm_ref(A, B, C0, 1.0, 1.0)
+    for name in _variants(sg):
+        C, _ = run_gpu(sg, A, B, C0, 1.0, 1.0, config=name, off_a=offs[0], off_b=offs[1], off_c=offs[2])
+        assert_parity(C, Cref, S, K, f"{name} offsets {offs}")
+
+
+@pytest.mark.parametrize("ldc_pad", [7, 4])
+def test_guard_bands_untouched(sg, ldc_pad):
+    M, N, K = 131, 132, 76
+    A, B, C0 = make_inputs(M, N, K, seed=9)
+    sentinel = 12345.0
+    ldc = N + ldc_pad
+    off = 3 * ldc + 4
+    total = off + (M - 1) * ldc + N + 64
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    mask = np.ones(total, bool)
+    for r in range(M):
+        mask[off + r * ldc: off + r * ldc + N] = False
+    for name in _variants(sg):
+        for beta in (0.0, 1.0):
+            dC = torch.full((total,), sentinel, dtype=torch.float32, device="cuda")
+            plan = sg.Plan(M, N, K, K, N, ldc, config=name)
+            plan.run(1.0, dA, dB, beta, dC.data_ptr() + 4 * off)
+            torch.cuda.synchronize()
+            out = dC.cpu().numpy()
+            assert np.all(out[mask] == sentinel), f"{name} wrote outside C (ldc={ldc}, beta={beta})"
+            plan.close()
+
+
+# ---- degenerate cases ---------------------------------------------------------
+
+def test_beta_zero_ignores_nan_c(sg, oracle_mod):
+    M, N, K = 150, 170, 64
+    A, B, C0 = make_inputs(M, N, K, seed=1)
+    Cref, S = oracle_mod.sgemm_ref(A, B, None, 1.0, 0.0)
+    for name in _variants(sg):
+        C, _ = run_gpu(sg, A, B, C0, 1.0, 0.0, config=name, c_fill=np.nan)
+        assert_parity(C, Cref, S, K, f"{name} beta=0 over NaN")
+
+
+def test_alpha_zero_and_k_zero(sg, oracle_mod):
+    M, N = 70, 90
+    A, B, C0 = make_inputs(M, N, 33, seed=2)
+    Cref, S = oracle_mod.sgemm_ref(A, B, C0, 0.0, -2.0)
+    C, _ = run_gpu(sg, A, B, C0, 0.0, -2.0)
+    assert_parity(C, Cref, S, 33, "alpha=0")
+    A0 = np.zeros((M, 0), np.float32)
+    B0 = np.zeros((0, N), np.float32)
+    Cref, S = oracle_mod.sgemm_ref(A0, B0, C0, 1.0, 3.0)
+    C, _ = run_gpu(sg, A0, B0, C0, 1.0, 3.0)
+    assert_parity(C, Cref, S, 0, "K=0")
+    C, _ = run_gpu(sg, A0, B0, C0, 1.0, 0.0)
+    assert np.all(C == 0.0)
+
+
+def test_empty_m_or_n(sg):
+    for (M, N, K) in ((0, 5, 5), (5, 0, 5), (0, 0, 0)):
+        plan = sg.Plan(M, N, K)
+        plan.run(1.0, None, None, 0.0, None)
+        assert plan.launches == 0
+        plan.close()
+    torch.cuda.synchronize()
+
+
+def test_argument_errors_on_gpu(sg):
+    plan = sg.Plan(8, 8, 8)
+    with pytest.raises(sg.SgemmError) as e:
+        plan.run(1.0, None, None, 0.0, None)
+    assert e.value.status == sg.SGEMM_ERR_INVALID_ARG
+    plan.close()
+    with pytest.raises(sg.SgemmError) as e:
+        sg.Plan(64, 64, 64, lda=65, config="tma_128x128x32_s4_ffma2")
+    assert e.value.status == sg.SGEMM_ERR_UNSUPPORTED
+
+
+# ---- the wait limit -------------------------------------------------------------
+
+def test_wait_timeout_selftest(sg):
+    assert sg.device_status() == sg.SGEMM_OK
+    rc = sg.selftest_wait_timeout(2_000_000)          # 2 ms on a phase nobody completes
+    assert rc == sg.SGEMM_ERR_TIMEOUT
+    assert sg.device_status() == sg.SGEMM_OK           # the self-test cleared its bit
+    # the context is still usable
+    x = torch.ones(4, device="cuda")
+    assert float(x.sum()) == 4.0
+
+
+# ---- host-buffer entry point ------------------------------------------------------
+
+def test_run_host_matches_device_path(sg, oracle_mod):
+    M, N, K = 257, 300, 129
+    A, B, C0 = make_inputs(M, N, K, seed=21)
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hC = torch.from_numpy(C0.copy()).pin_memory()
+    dA = torch.empty_like(hA, device="cuda")
+    dB = torch.empty_like(hB, device="cuda")
+    dC = torch.empty_like(hC, device="cuda")
+    plan = sg.Plan(M, N, K)
+    plan.run_host(0.5, hA, hB, 3.0, hC, dA, dB, dC)
+    torch.cuda.synchronize()
+    Cdev, _ = run_gpu(sg, A, B, C0, 0.5, 3.0)
+    assert np.array_equal(hC.numpy(), Cdev)
+    Cref, S = oracle_mod.sgemm_ref(A, B, C0, 0.5, 3.0)
+    assert_parity(hC.numpy(), Cref, S, K, "run_host")
+    plan.close()
+
+
+# ---- the five workloads at full size, in the launch configuration the bench times --
+
+@pytest.mark.parametrize("wname", list(WORKLOADS))
+def test_workload_full_size(sg, oracle_mod, wname):
+    w = WORKLOADS[wname]
+    A, B, C0 = workload_inputs(w)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.from_numpy(C0).cuda()
+    plan = sg.Plan(w.M, w.N, w.K)
+    plan.run(w.alpha, dA, dB, w.beta, dC)
+    torch.cuda.synchronize()
+    assert sg.device_status() == sg.SGEMM_OK
+    info = plan.info()
+    plan.close()
+    if w.M * w.N * w.K <= 1024 ** 3:
+        C = dC.cpu().numpy()
+        Cref, S = oracle_mod.sgemm_ref(A, B, C0, w.alpha, w.beta)
+        assert_parity(C, Cref, S, w.K, wname)
+        return
+    rows, cols = sample_rows_cols(w.M, w.N, seed=w.seed)
+    r_t = torch.from_numpy(rows).cuda()
+    c_t = torch.from_numpy(cols).cuda()
+    C = dC.index_select(0, r_t).index_select(1, c_t).cpu().numpy()
+    As = np.ascontiguousarray(A[rows])
+    Bs = np.ascontiguousarray(B[:, cols])
+    Cs = np.ascontiguousarray(C0[np.ix_(rows, cols)])
+    Cref, S = oracle_mod.sgemm_ref(As, Bs, Cs, w.alpha, w.beta)
+    assert C.size >= 65536
+    assert_parity(C, Cref, S, w.K, f"{wname} ({info['variant']})")
+    if w.alpha == 1.0 and w.beta == 0.0 and info.get("k_order") == "sequential":
+        sub_r = np.arange(0, len(rows), 4)
+        ii, jj = np.meshgrid(sub_r, np.arange(len(cols)), indexing="ij")
+        chain = oracle_mod.fp32_chain_entries(As, Bs, ii.ravel(), jj.ravel())
+        assert np.array_equal(C[ii.ravel(), jj.ravel()], chain), f"{wname}: not the ascending-k chain"
