@@ -49,7 +49,9 @@ struct Variant {
 
 // Variant tables, one per kernel translation unit.
 const Variant* generic_variants(int* count);
-const Variant* tma_variants(int* count);
+const Variant* tma_variants_a(int* count);
+const Variant* tma_variants_b(int* count);
+const Variant* tma_variants_c(int* count);
 const Variant* skinny_variants(int* count);
 
 // C = beta * C (K == 0 or alpha == 0), any leading dimension.

@@ -50,8 +50,10 @@ struct Registry {
     const Variant* v = generic_variants(&n);
     first_generic = static_cast<int>(all.size());
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
-    v = tma_variants(&n);
-    for (int i = 0; i < n; ++i) all.push_back(&v[i]);
+    for (auto fn : {&tma_variants_a, &tma_variants_b, &tma_variants_c}) {
+      v = fn(&n);
+      for (int i = 0; i < n; ++i) all.push_back(&v[i]);
+    }
     v = skinny_variants(&n);
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
   }
@@ -125,8 +127,9 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   (void)num_sms;
   if (lda % 4 != 0 || ldb % 4 != 0) return "generic_64x64x16";
   if (M <= 32 && find_variant("skinny_16") >= 0 && M <= 16) return "skinny_16";
-  if (M * N <= 256 * 256) return "tma_128x64x32_s4_ffma2";
-  return "tma_128x128x32_s4_ffma2";
+  if (M * N <= 256 * 256) return "tma_128x64x32_w64x32_s3_quad_b3";
+  if (M * N >= int64_t(8192) * 8192) return "tma_128x128x32_w64x32_s4_quad_b1";
+  return "tma_128x128x32_w64x32_s3_scalar_b2";
 }
 
 sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int config_id,
@@ -201,7 +204,9 @@ sgemm_status_t encode_maps(const Variant* v, const sgemm_plan_s* p, const float*
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(&a->tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     v->tma_swizzle_a == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     v->tma_swizzle_a == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                     : v->tma_swizzle_a == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
   }
