@@ -1,13 +1,289 @@
-// kernel_skinny.cu -- small-M (decode-shaped) SGEMM variants.
+// kernel_skinny.cu -- SGEMM for few rows (M <= 16): the decode-shaped case.
+//
+// With M <= 16 every element of B is used at most 16 times, so the product
+// is bound by streaming B from HBM, not by the FMA pipe ("Writing a Fast
+// Matmul in CUDA, Step by Step", "Why decode doesn't care": a decode-step
+// matrix product multiplies each weight a handful of times, so it sits on
+// the bandwidth roof).  What matters is keeping enough bytes of B in
+// flight on every SM and spending no FMAs on padding rows.
+//
+//  * CTA tile: all 16 rows x BN columns (BN a multiple of 128), over one
+//    contiguous k-range.  Each 128-column group has GW (4 or 8) warps; warp
+//    w of a group multiplies k-quads w, w + GW, ... of every 32-deep
+//    k-slice, and
+//    lane l owns columns 4l .. 4l + 3 of its group for all 16 rows (a
+//    16 x 4 thread tile).  Wider tiles read longer contiguous runs of each
+//    B row (BN * 4 bytes) per DRAM access.  The _ef variants load B with an
+//    L2 evict-first hint: it is read exactly once, so it should not push A
+//    (read by every CTA) out of L2.  A TMA ring (A slice 16 x 32 with the 128-byte
+//    swizzle, B slice 32 x 128) feeds it exactly like the main kernel, with
+//    the same stage-release counters and bounded waits.
+//  * Split-K without scratch memory ("How a Matmul Kernel Gets Fast",
+//    section 14, and "Writing a Fast Matmul in CUDA", "What cuBLAS and
+//    CUTLASS add": split the k loop across blocks and add the pieces):
+//    the S CTAs that share a column slab form one thread-block cluster and
+//    take consecutive k-ranges.  Each CTA first adds, per column group, its GW warps'
+//    partial tiles in shared memory (warp order 0..GW-1), then the cluster
+//    synchronises and CTA r finalises 1/S of the 16 x 128 outputs by
+//    reading the S partial tiles through distributed shared memory in rank
+//    order 0..S-1.  The reduction order is fixed, so results are
+//    reproducible run to run; it is not the ascending-k chain of the
+//    single-pass kernels (the plan reports k_order=split).
+//  * Epilogue: out = alpha*sum (beta == 0, C not read) or
+//    fmaf(alpha, sum, beta*C), predicated on m < M and n < N.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace sgemm {
+namespace {
+
+constexpr int kSBM = 16;
+constexpr int kSBK = 32;
+
+struct SkinnyParams {
+  float* C;
+  int64_t ldc;
+  int M, N, K;
+  float alpha, beta;
+  unsigned int* status;
+  uint64_t timeout_ns;
+};
+
+// BN columns per CTA (a warp spans 128), GW warps per 128-column group
+// splitting each k-slice's eight quads.
+template <int BN, int GW, int STAGES>
+struct SkinnyShape {
+  static_assert(GW == 4 || GW == 8, "each warp takes 8 / GW quads of a 32-deep slice");
+  static constexpr int kQuadsPerWarp = (kSBK / 4) / GW;
+  static_assert(BN % 128 == 0 && BN <= 256, "a warp spans 128 columns (32 lanes x 4); one TMA box spans <= 256");
+  static constexpr int kGroups = BN / 128;
+  static constexpr int kWarps = GW * kGroups;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kStageA = kSBM * kSBK * 4;  // 2 KB
+  static constexpr int kStageB = kSBK * BN * 4;    // 16 KB
+  static constexpr int kStageBytes = kStageA + kStageB;
+  static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0, "stages keep 1024-byte alignment");
+  static constexpr int kRingBytes = STAGES * kStageBytes;
+  static constexpr int kRedBytes = GW * kSBM * BN * 4;  // warp partials, reuses the ring
+  static_assert(kRingBytes >= kRedBytes, "the ring must hold the warps' partial tiles");
+  static constexpr int kPartialBytes = kSBM * BN * 4;
+  static constexpr int kSmemBytes = kRingBytes + kPartialBytes + STAGES * 16 + 1024;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of all CTAs of the cluster; orders shared-memory writes
+// before the peers' reads.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(ptx::smem_addr(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST>
+__global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
+    sgemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const SkinnyParams p) {
+  using S = SkinnyShape<BN, GW, STAGES>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw_base = ptx::smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+  const uint32_t smem_base = ptx::smem_addr(smem);
+  float* partial = reinterpret_cast<float*>(smem + S::kRingBytes);  // [16][BN], read by cluster peers
+  const uint32_t bar_full = smem_base + S::kRingBytes + S::kPartialBytes;
+  unsigned int* released = reinterpret_cast<unsigned int*>(smem + S::kRingBytes + S::kPartialBytes + STAGES * 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int group = warp / GW;  // columns 128*group .. +127 of the tile
+  const int gw = warp % GW;     // k-quads gw, gw + GW, ... of each slice
+  const uint32_t rank = cluster_rank();
+  const uint32_t nsplit = cluster_size();
+  const int slab = static_cast<int>(blockIdx.x / nsplit);
+  const int n0 = slab * BN;
+  const int KT = (p.K + kSBK - 1) / kSBK;
+  const int kt_begin = static_cast<int>((static_cast<int64_t>(KT) * rank) / nsplit);
+  const int kt_end = static_cast<int>((static_cast<int64_t>(KT) * (rank + 1)) / nsplit);
+  const uint32_t nkt = static_cast<uint32_t>(kt_end - kt_begin);
+
+  auto issue = [&](uint32_t j) {
+    const uint32_t s = j % STAGES;
+    const int kt = kt_begin + static_cast<int>(j);
+    const uint32_t dst = smem_base + s * S::kStageBytes;
+    ptx::mbar_arrive_expect_tx(bar_full + 8 * s, S::kStageBytes);
+    ptx::tma_load_2d(dst, &tmA, kt * kSBK, 0, bar_full + 8 * s);
+    if constexpr (EVICT_FIRST) {
+      ptx::tma_load_2d_hint(dst + S::kStageA, &tmB, n0, kt * kSBK, bar_full + 8 * s, ptx::l2_policy_evict_first());
+    } else {
+      ptx::tma_load_2d(dst + S::kStageA, &tmB, n0, kt * kSBK, bar_full + 8 * s);
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(bar_full + 8 * s, 1);
+      released[s] = 0u;
+    }
+    ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB);
+    for (uint32_t j = 0; j < STAGES && j < nkt; ++j) issue(j);
+  }
+  __syncthreads();
+
+  // acc[m][0] = columns 4l, 4l+1 of row m; acc[m][1] = columns 4l+2, 4l+3
+  float2 acc[kSBM][2];
+#pragma unroll
+  for (int m = 0; m < kSBM; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
+
+  bool ready = false;
+  for (uint32_t it = 0; it < nkt; ++it) {
+    const uint32_t s = it % STAGES;
+    if (!ready && !ptx::mbar_wait(bar_full + 8 * s, (it / STAGES) & 1u, p.timeout_ns)) {
+      atomicOr(p.status, kStatusTimeoutFull);
+      break;  // stay in step with the CTA and cluster barriers below
+    }
+    if (it + 1 < nkt) ready = ptx::mbar_test_wait(bar_full + 8 * ((it + 1) % STAGES), ((it + 1) / STAGES) & 1u);
+    const float* As = reinterpret_cast<const float*>(smem + s * S::kStageBytes);
+    const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + group * 32 + lane;
+#pragma unroll
+    for (int qq = 0; qq < S::kQuadsPerWarp; ++qq) {
+      const int q = gw + GW * qq;
+      float4 a4[kSBM];
+#pragma unroll
+      for (int m = 0; m < kSBM; ++m)
+        a4[m] = *reinterpret_cast<const float4*>(As + m * kSBK + ((q ^ (m & 7)) << 2));
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 b = Bs4[(4 * q + kk) * (BN / 4)];
+        const float2 b01 = make_float2(b.x, b.y);
+        const float2 b23 = make_float2(b.z, b.w);
+#pragma unroll
+        for (int m = 0; m < kSBM; ++m) {
+          const float a = kk == 0 ? a4[m].x : kk == 1 ? a4[m].y : kk == 2 ? a4[m].z : a4[m].w;
+          const float2 aa = make_float2(a, a);
+          acc[m][0] = __ffma2_rn(aa, b01, acc[m][0]);
+          acc[m][1] = __ffma2_rn(aa, b23, acc[m][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const unsigned int before = ptx::atom_add_acq_rel_cta(&released[s], 1u);
+      if ((before + 1u) % S::kWarps == 0u && it + STAGES < nkt) {
+        ptx::fence_proxy_async_smem();
+        issue(it + STAGES);
+      }
+    }
+  }
+
+  // ---- reduce each column group's GW warp partials (fixed order) ----
+  __syncthreads();  // every stage consumed: the ring is free
+  float4* red4 = reinterpret_cast<float4*>(smem);  // [gw][16][BN/4]
+#pragma unroll
+  for (int m = 0; m < kSBM; ++m)
+    red4[(gw * kSBM + m) * (BN / 4) + group * 32 + lane] =
+        make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
+  __syncthreads();
+  const float* red = reinterpret_cast<const float*>(smem);
+  constexpr int kTile = kSBM * BN;
+  for (int idx = threadIdx.x; idx < kTile; idx += S::kThreads) {
+    float sum = red[idx];
+#pragma unroll
+    for (int w = 1; w < GW; ++w) sum += red[idx + w * kTile];
+    partial[idx] = sum;
+  }
+
+  // ---- reduce the cluster's partial tiles (rank order) and write C ----
+  cluster_sync();
+  const int begin = static_cast<int>((static_cast<int64_t>(kTile) * rank) / nsplit);
+  const int end = static_cast<int>((static_cast<int64_t>(kTile) * (rank + 1)) / nsplit);
+  for (int idx = begin + static_cast<int>(threadIdx.x); idx < end; idx += S::kThreads) {
+    const int m = idx / BN;
+    const int n = n0 + idx % BN;
+    float sum = 0.f;
+    for (uint32_t r = 0; r < nsplit; ++r) sum += ld_peer(partial + idx, r);
+    if (m < p.M && n < p.N) {
+      float* d = p.C + static_cast<int64_t>(m) * p.ldc + n;
+      *d = p.beta == 0.f ? p.alpha * sum : fmaf(p.alpha, sum, p.beta * *d);
+    }
+  }
+  cluster_sync();  // peers may still be reading this CTA's partial tile
+}
+
+template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST>
+struct SkinnyVariant {
+  using S = SkinnyShape<BN, GW, STAGES>;
+  static constexpr auto kernel = sgemm_skinny_kernel<BN, GW, STAGES, MINB, EVICT_FIRST>;
+  static cudaError_t prepare() {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  }
+  static cudaError_t occupancy(int* ctas) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kernel, S::kThreads, S::kSmemBytes);
+  }
+  static cudaError_t launch(const LaunchArgs& a, cudaStream_t stream) {
+    SkinnyParams p;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.grid), 1, 1);
+    cfg.blockDim = dim3(S::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = S::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(a.split_k);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a.tmA, a.tmB, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  static Variant describe(const char* name) {
+    return Variant{name, kKindSkinny, kSBM, BN, kSBK, STAGES, 1, S::kThreads, S::kSmemBytes, 128, &prepare, &occupancy,
+                   &launch};
+  }
+};
+
+const Variant kSkinnyVariants[] = {
+    SkinnyVariant<128, 4, 3, 3, false>::describe("skinny_16x128x32_w4_s3_b3"),
+    SkinnyVariant<128, 4, 3, 3, true>::describe("skinny_16x128x32_w4_s3_b3_ef"),
+    SkinnyVariant<128, 4, 4, 2, true>::describe("skinny_16x128x32_w4_s4_b2_ef"),
+};
+
+}  // namespace
 
 const Variant* skinny_variants(int* count) {
-  *count = 0;
-  return nullptr;
+  *count = static_cast<int>(sizeof(kSkinnyVariants) / sizeof(kSkinnyVariants[0]));
+  return kSkinnyVariants;
 }
 
 }  // namespace sgemm

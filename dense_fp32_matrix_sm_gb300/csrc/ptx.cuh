@@ -58,6 +58,19 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Shared-memory fetch-and-add with acquire-release semantics at CTA scope:
+// this thread's earlier accesses are ordered before the add, and the adds
+// of other threads that precede it in the counter's order are visible
+// after it.
+__device__ __forceinline__ unsigned int atom_add_acq_rel_cta(unsigned int* addr, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(smem_addr(addr)), "r"(v)
+               : "memory");
+  return old;
+}
+
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -94,6 +107,31 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// As tma_load_2d, with an L2 eviction-priority hint (a policy made by
+// l2_policy_evict_first / l2_policy_evict_last).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// L2 policy: data read once (stream it through, evict first).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// L2 policy: data reused by many CTAs (keep it).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

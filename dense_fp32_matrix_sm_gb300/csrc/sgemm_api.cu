@@ -26,6 +26,7 @@ struct sgemm_plan_s {
   int generic_id;   // scalar-load variant used when A or B is not 16-byte aligned
   int ctas_per_sm;
   int grid;
+  int split;        // CTAs per cluster along K (skinny variants), else 1
   int64_t tiles;
 };
 
@@ -126,7 +127,7 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   (void)K;
   (void)num_sms;
   if (lda % 4 != 0 || ldb % 4 != 0) return "generic_64x64x16";
-  if (M <= 32 && find_variant("skinny_16") >= 0 && M <= 16) return "skinny_16";
+  if (M <= 16) return "skinny_16x128x32_w4_s3_b3_ef";
   if (M * N <= 256 * 256) return "tma_128x64x32_w64x32_s3_quad_b3";
   if (M * N >= int64_t(8192) * 8192) return "tma_128x128x32_w64x32_s4_quad_b1";
   return "tma_128x128x32_w64x32_s3_scalar_b2";
@@ -184,9 +185,29 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->ctas_per_sm = ctas;
   p->tiles = ((M + v->bm - 1) / v->bm) * ((N + v->bn - 1) / v->bn);
   int64_t grid = p->tiles;
+  p->split = 1;
   if (v->kind == kKindTma) {
     const int64_t slots = static_cast<int64_t>(sms) * ctas;
     if (grid > slots) grid = slots;
+  } else if (v->kind == kKindSkinny) {
+    // Split K over a cluster of S CTAs per column slab (S <= 8, the portable
+    // cluster size).  Pick S so the CTAs spread evenly over the SMs: score =
+    // (CTAs per SM) / ceil(CTAs per SM), times the fraction of CTA slots
+    // filled; ties go to the larger S.
+    const int64_t KT = (K + v->bk - 1) / v->bk;
+    double best = -1.0;
+    for (int s = 1; s <= 8 && s <= KT; ++s) {
+      const double total = static_cast<double>(p->tiles) * s;
+      const double per_sm = total / sms;
+      const double balance = per_sm / static_cast<double>(static_cast<int64_t>(per_sm + 0.999999));
+      const double fill = total >= static_cast<double>(sms) * ctas ? 1.0 : total / (static_cast<double>(sms) * ctas);
+      const double score = balance * fill;
+      if (score >= best - 1e-9) {
+        best = score;
+        p->split = s;
+      }
+    }
+    grid = p->tiles * p->split;
   }
   p->grid = static_cast<int>(grid > 0x7fffffff ? 0x7fffffff : grid);
   *out = p;
@@ -280,7 +301,7 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   a.alpha = alpha;
   a.beta = beta;
   a.grid = grid;
-  a.split_k = 1;
+  a.split_k = v->kind == kKindSkinny ? p->split : 1;
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   sgemm_status_t st = status_addr(device, &a.status);
   if (st != SGEMM_OK) return st;
@@ -332,10 +353,11 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
   const Variant* v = registry().all[plan->config_id];
   snprintf(buf, n,
            "variant=%s kind=%s tile=%dx%dx%d stages=%d ffma2=%d threads=%d smem=%d grid=%d ctas_per_sm=%d "
-           "tiles=%lld sms=%d k_order=sequential M=%lld N=%lld K=%lld",
+           "tiles=%lld sms=%d split=%d k_order=%s M=%lld N=%lld K=%lld",
            v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : "skinny", v->bm, v->bn,
            v->bk, v->stages, v->ffma2, v->threads, v->smem_bytes, plan->grid, plan->ctas_per_sm,
-           static_cast<long long>(plan->tiles), plan->num_sms, static_cast<long long>(plan->M),
+           static_cast<long long>(plan->tiles), plan->num_sms, plan->split, (plan->split > 1 || v->kind == kKindSkinny) ? "split" : "sequential",
+           static_cast<long long>(plan->M),
            static_cast<long long>(plan->N), static_cast<long long>(plan->K));
   return SGEMM_OK;
 }

@@ -278,10 +278,8 @@ __global__ void __launch_bounds__(Shape<BM, BN, BK, WM, WN, STAGES>::kThreads, M
       // it at once with the slice STAGES ahead (no warp waits for another).
       __syncwarp();
       if (lane == 0) {
-        __threadfence_block();
-        const unsigned int before = atomicAdd(&released[s], 1u);
+        const unsigned int before = ptx::atom_add_acq_rel_cta(&released[s], 1u);
         if ((before + 1u) % S::kWarps == 0u && it + STAGES < total_it) {
-          __threadfence_block();
           ptx::fence_proxy_async_smem();
           issue(it + STAGES);
         }

@@ -78,6 +78,7 @@ def run_gpu(sg, A, B, C0, alpha, beta, config=None, lda=None, ldb=None, ldc=None
     assert sg.device_status() == sg.SGEMM_OK
     out = _from_dev(dC, M, N, ldc, off_c)
     name = plan.config_name
+    run_gpu.last_info = plan.info()
     plan.close()
     return out, name
 
@@ -96,8 +97,12 @@ def assert_parity(C, Cref, S, K, what=""):
                              f"err {err[idx]:.3e} vs bound {bnd[idx]:.3e}")
 
 
-def _variants(sg):
-    return sg.config_names()
+def _variants(sg, M=None):
+    """Variant names, without the few-row kernels when M is above their limit."""
+    names = sg.config_names()
+    if M is not None and M > 16:
+        names = [n for n in names if not n.startswith("skinny")]
+    return names
 
 
 # ---- small and ragged shapes, every variant, full comparison ------------------
@@ -134,7 +139,7 @@ def test_shape_sweep_every_variant(sg, oracle_mod, variant_idx):
                 raise
             Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
             assert_parity(C, Cref, S, K, f"{name} {M}x{N}x{K} a={alpha} b={beta}")
-            if alpha == 1.0 and beta == 0.0:
+            if alpha == 1.0 and beta == 0.0 and run_gpu.last_info.get("k_order") == "sequential":
                 ii, jj = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
                 chain = oracle_mod.fp32_chain_entries(A, B, ii.ravel(), jj.ravel()).reshape(M, N)
                 assert np.array_equal(C, chain), f"{name} {M}x{N}x{K}: not the ascending-k fp32 chain"
@@ -147,6 +152,36 @@ def test_medium_full_compare(sg, oracle_mod, shape):
     Cref, S = oracle_mod.sgemm_ref(A, B, C0, 0.5, 3.0)
     C, _ = run_gpu(sg, A, B, C0, 0.5, 3.0)
     assert_parity(C, Cref, S, K, f"table {shape}")
+
+
+# ---- few rows: the cluster split-K kernel ---------------------------------------
+
+SKINNY_CASES = [(16, 16384 // 8, 8192 // 4), (1, 300, 1000), (7, 129, 33), (16, 128, 32), (13, 1000, 4097),
+                (16, 2048, 96), (3, 5000, 8), (16, 77, 1), (9, 4096, 2000)]
+
+
+@pytest.mark.parametrize("shape", SKINNY_CASES)
+def test_skinny_variants(sg, oracle_mod, shape):
+    M, N, K = shape
+    A, B, C0 = make_inputs(M, N, K, seed=M + N + K, dist_a=("normal", 1.0), dist_b=("normal", 0.02))
+    lda, ldb = (K + 3) // 4 * 4, (N + 3) // 4 * 4
+    for name in [n for n in sg.config_names() if n.startswith("skinny")] + [None]:
+        for alpha, beta in ((1.0, 0.0), (1.0, 1.0), (-0.75, 2.0)):
+            C, used = run_gpu(sg, A, B, C0, alpha, beta, config=name, lda=lda, ldb=ldb)
+            info = run_gpu.last_info
+            assert name is not None or used.startswith("skinny"), used
+            Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
+            assert_parity(C, Cref, S, K, f"{used} {shape} split={info['split']} a={alpha} b={beta}")
+            # a fixed reduction order: the same inputs give the same bits again
+            C2, _ = run_gpu(sg, A, B, C0, alpha, beta, config=name, lda=lda, ldb=ldb)
+            assert np.array_equal(C, C2)
+
+
+def test_skinny_rejects_tall_m(sg):
+    name = next(n for n in sg.config_names() if n.startswith("skinny"))
+    with pytest.raises(sg.SgemmError) as e:
+        sg.Plan(17, 256, 256, config=name)
+    assert e.value.status == sg.SGEMM_ERR_UNSUPPORTED
 
 
 # ---- layouts: leading dimensions, misaligned pointers, guard bands ------------
@@ -167,7 +202,7 @@ def test_misaligned_pointers(sg, oracle_mod, offs):
     M, N, K = 140, 260, 96
     A, B, C0 = make_inputs(M, N, K, seed=5)
     Cref, S = oracle_mod.sgemm_ref(A, B, C0, 1.0, 1.0)
-    for name in _variants(sg):
+    for name in _variants(sg, M):
         C, _ = run_gpu(sg, A, B, C0, 1.0, 1.0, config=name, off_a=offs[0], off_b=offs[1], off_c=offs[2])
         assert_parity(C, Cref, S, K, f"{name} offsets {offs}")
 
@@ -185,7 +220,7 @@ def test_guard_bands_untouched(sg, ldc_pad):
     mask = np.ones(total, bool)
     for r in range(M):
         mask[off + r * ldc: off + r * ldc + N] = False
-    for name in _variants(sg):
+    for name in _variants(sg, M):
         for beta in (0.0, 1.0):
             dC = torch.full((total,), sentinel, dtype=torch.float32, device="cuda")
             plan = sg.Plan(M, N, K, K, N, ldc, config=name)
@@ -202,7 +237,7 @@ def test_beta_zero_ignores_nan_c(sg, oracle_mod):
     M, N, K = 150, 172, 64
     A, B, C0 = make_inputs(M, N, K, seed=1)
     Cref, S = oracle_mod.sgemm_ref(A, B, None, 1.0, 0.0)
-    for name in _variants(sg):
+    for name in _variants(sg, M):
         C, _ = run_gpu(sg, A, B, C0, 1.0, 0.0, config=name, c_fill=np.nan)
         assert_parity(C, Cref, S, K, f"{name} beta=0 over NaN")
 
@@ -310,3 +345,16 @@ def test_workload_full_size(sg, oracle_mod, wname):
         ii, jj = np.meshgrid(sub_r, np.arange(len(cols)), indexing="ij")
         chain = oracle_mod.fp32_chain_entries(As, Bs, ii.ravel(), jj.ravel())
         assert np.array_equal(C[ii.ravel(), jj.ravel()], chain), f"{wname}: not the ascending-k chain"
+
+
+def test_misaligned_and_guarded_few_rows(sg, oracle_mod):
+    """The few-row kernels under a misaligned A (scalar-load fallback), a
+    padded ldc and NaN in C with beta = 0."""
+    M, N, K = 11, 700, 300
+    A, B, C0 = make_inputs(M, N, K, seed=77)
+    Cref, S = oracle_mod.sgemm_ref(A, B, None, 1.0, 0.0)
+    for name in [n for n in sg.config_names() if n.startswith("skinny")]:
+        C, _ = run_gpu(sg, A, B, C0, 1.0, 0.0, config=name, ldc=N + 5, c_fill=np.nan)
+        assert_parity(C, Cref, S, K, f"{name} nan C")
+        C, used = run_gpu(sg, A, B, C0, 1.0, 0.0, config=name, off_a=1)
+        assert_parity(C, Cref, S, K, f"{name} misaligned A -> {used}")
