@@ -42,7 +42,7 @@ METRIC = "FP32 SGEMM GFLOP/s at 4096^3 on 1 GB300; % of FP32 FFMA peak"
 FMA_LANES_PER_SM = 128          # FP32 lanes per SM (4 sub-partitions x 32)
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ["tma_kernel.cuh", "kernel_skinny.cu", "kernel_generic.cu", "ptx.cuh", "kernels.h"]
+KERNEL_SOURCES = ["tma_kernel.cuh", "cpa_kernel.cuh", "tmat_kernel.cuh", "tile_order.cuh", "kernel_skinny.cu", "kernel_generic.cu", "ptx.cuh", "kernels.h"]
 
 
 def kernel_source_hash() -> str:

@@ -12,6 +12,7 @@ enum VariantKind : int {
   kKindGeneric = 0,  // scalar predicated loads, any alignment / leading dimension
   kKindTma = 1,      // TMA-fed multi-stage pipeline, needs 16-byte aligned A/B rows
   kKindSkinny = 2,   // small-M streaming kernel, needs 16-byte aligned A/B rows
+  kKindCpa = 3,      // A by cp.async (transposed, any alignment), B by TMA (16-byte aligned rows)
 };
 
 // Everything one launch needs.  Tensor maps are encoded by the caller per
@@ -53,6 +54,8 @@ const Variant* tma_variants_a(int* count);
 const Variant* tma_variants_b(int* count);
 const Variant* tma_variants_c(int* count);
 const Variant* skinny_variants(int* count);
+const Variant* cpa_variants(int* count);
+const Variant* tmat_variants(int* count);
 
 // C = beta * C (K == 0 or alpha == 0), any leading dimension.
 cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaStream_t stream);

@@ -57,6 +57,10 @@ struct Registry {
     }
     v = skinny_variants(&n);
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
+    v = cpa_variants(&n);
+    for (int i = 0; i < n; ++i) all.push_back(&v[i]);
+    v = tmat_variants(&n);
+    for (int i = 0; i < n; ++i) all.push_back(&v[i]);
   }
 };
 
@@ -116,7 +120,9 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
   (void)N;
   (void)K;
   if (v->kind == kKindGeneric) return true;
-  if (lda % 4 != 0 || ldb % 4 != 0) return false;  // TMA row strides must be multiples of 16 bytes
+  if (ldb % 4 != 0) return false;  // TMA row strides must be multiples of 16 bytes
+  if (v->kind == kKindCpa) return true;  // A is copied 4 bytes at a time: any lda
+  if (lda % 4 != 0) return false;
   if (v->kind == kKindSkinny) return M <= v->bm;
   return true;
 }
@@ -125,12 +131,13 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
 // names.  The entries come from the measured sweeps on GB300.
 const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms) {
   (void)K;
+  (void)lda;
   (void)num_sms;
-  if (lda % 4 != 0 || ldb % 4 != 0) return "generic_64x64x16";
-  if (M <= 16) return "skinny_16x128x32_w4_s3_b3_ef";
+  if (ldb % 4 != 0) return "generic_64x64x16";
+  if (M <= 16 && lda % 4 == 0) return "skinny_16x128x32_w4_s3_b3_ef";
+  if (lda % 4 != 0) return "cpa_128x128x32_s3_k8_b2";  // A copied 4 bytes at a time: any lda
   if (M * N <= 256 * 256) return "tma_128x64x32_w64x32_s3_quad_b3";
-  if (M * N >= int64_t(8192) * 8192) return "tma_128x128x32_w64x32_s4_quad_b1";
-  return "tma_128x128x32_w64x32_s3_scalar_b2";
+  return "tmat_128x128x32_s4_b1";
 }
 
 sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int config_id,
@@ -186,7 +193,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->tiles = ((M + v->bm - 1) / v->bm) * ((N + v->bn - 1) / v->bn);
   int64_t grid = p->tiles;
   p->split = 1;
-  if (v->kind == kKindTma) {
+  if (v->kind == kKindTma || v->kind == kKindCpa) {
     const int64_t slots = static_cast<int64_t>(sms) * ctas;
     if (grid > slots) grid = slots;
   } else if (v->kind == kKindSkinny) {
@@ -218,7 +225,7 @@ sgemm_status_t encode_maps(const Variant* v, const sgemm_plan_s* p, const float*
                            LaunchArgs* a) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return SGEMM_ERR_CUDA;
-  {
+  if (v->kind != kKindCpa) {  // the transposed-A kernels copy A themselves
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->lda) * 4};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(v->bk), static_cast<cuuint32_t>(v->bm)};
@@ -281,8 +288,9 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   const Registry& reg = registry();
   const Variant* v = reg.all[p->config_id];
   int grid = p->grid;
+  const bool a_needs_16 = v->kind == kKindTma || v->kind == kKindSkinny;
   if (v->kind != kKindGeneric &&
-      ((reinterpret_cast<uintptr_t>(A) & 15) != 0 || (reinterpret_cast<uintptr_t>(B) & 15) != 0)) {
+      ((a_needs_16 && (reinterpret_cast<uintptr_t>(A) & 15) != 0) || (reinterpret_cast<uintptr_t>(B) & 15) != 0)) {
     v = reg.all[p->generic_id];
     grid = 0;
   }
@@ -354,7 +362,7 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
   snprintf(buf, n,
            "variant=%s kind=%s tile=%dx%dx%d stages=%d ffma2=%d threads=%d smem=%d grid=%d ctas_per_sm=%d "
            "tiles=%lld sms=%d split=%d k_order=%s M=%lld N=%lld K=%lld",
-           v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : "skinny", v->bm, v->bn,
+           v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : "skinny", v->bm, v->bn,
            v->bk, v->stages, v->ffma2, v->threads, v->smem_bytes, plan->grid, plan->ctas_per_sm,
            static_cast<long long>(plan->tiles), plan->num_sms, plan->split, (plan->split > 1 || v->kind == kKindSkinny) ? "split" : "sequential",
            static_cast<long long>(plan->M),

@@ -61,6 +61,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tile_order.cuh"
 
 namespace sgemm {
 namespace tma {
@@ -99,17 +100,6 @@ struct Shape {
   // 1024 bytes of slack to align the ring for the swizzle pattern
   static constexpr int kSmemBytes = STAGES * kStageBytes + kBarrierBytes + 1024;
 };
-
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m, int& tm,
-                                            int& tn) {
-  const int per_group = group_m * tiles_n;
-  const int group = tile / per_group;
-  const int first_m = group * group_m;
-  const int rows = min(tiles_m - first_m, group_m);
-  const int in_group = tile - group * per_group;
-  tm = first_m + in_group % rows;
-  tn = in_group / rows;
-}
 
 // The TMA swizzle of a [BM][BK] A tile moves 16-byte chunk q of row r to
 // chunk q ^ x(r), with x(r) = r & 7 for 128-byte rows (BK 32) and

@@ -1,0 +1,277 @@
+// tmat_kernel.cuh -- FP32 SGEMM with both operands fed by TMA and A
+// transposed inside shared memory (template; instantiated by
+// tmat_variants.cu).
+//
+// C = alpha*A*B + beta*C, row-major float32, single-rounding fp32 FMAs in
+// ascending k for every output (bit-identical to the float32 fma chain).
+//
+// The inner loop is the fast paired-FMA form: each FFMA2 multiplies a
+// register PAIR holding two rows of A at one k, (A[m][k], A[m+1][k]), by
+// one BROADCAST element of B; on GB300 this keeps the FP32 pipe ~87% busy
+// against ~81% for the mirrored form (pair of B columns, broadcast A).  It
+// needs A k-major in shared memory (At[k][m]).  TMA cannot transpose
+// 4-byte elements, so:
+//
+//  * TMA copies the A slice [BM][BK] (128-byte swizzle) and the B slice
+//    [BK][BN] into a STAGES-deep ring signalled by mbarriers, as in
+//    tma_kernel.cuh.
+//  * One slice ahead of the math, all threads transpose the A slice into a
+//    double-buffered At[BK][BM]: thread t reads row t/2, k-half t%2 (four
+//    128-bit loads) and writes 16 words At[k][m ^ 16*((k >> 4) & 1)].  The
+//    XOR puts the two k-halves of a warp's 16 rows in opposite bank halves
+//    (conflict-free writes) and keeps pairs (m, m+1) adjacent.
+//    ("Learn: Optimizing GEMM", section 7, and "Writing a Fast Matmul in
+//    CUDA", Step 5: A stored transposed so the inner loop reads contiguous
+//    m -- here the transpose runs on the on-chip copy instead of on the
+//    global loads.)
+//  * One CTA barrier per slice: after it the next transposed slice is
+//    complete and the current ring stage is free; thread 0 then refills
+//    that stage with the slice STAGES ahead.
+//  * Warps own 64 x 32 tiles; lane (g, c) owns rows 16i + 2g + e and
+//    columns 4c + 16h + j; per k: four 64-bit A-pair loads, two 128-bit B
+//    loads, 32 FFMA2.
+//  * Persistent CTAs in grouped tile order, bounded waits with a status
+//    word, epilogue out = alpha*acc (beta == 0, C not read) or
+//    fmaf(alpha, acc, beta*C).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tile_order.cuh"
+
+namespace sgemm {
+namespace tmat {
+
+struct Params {
+  float* C;
+  int64_t ldc;
+  int M, N, K;
+  float alpha, beta;
+  int vec_c;
+  int group_m;
+  unsigned int* status;
+  uint64_t timeout_ns;
+};
+
+template <int BN, int STAGES>
+struct Shape {
+  static constexpr int BM = 128;
+  static constexpr int BK = 32;
+  static constexpr int kWarpsM = BM / 64;
+  static constexpr int kWarpsN = BN / 32;
+  static constexpr int kWarps = kWarpsM * kWarpsN;
+  static constexpr int kThreads = kWarps * 32;
+  static_assert(kThreads == 2 * BM, "transpose mapping: two threads per A row");
+  static constexpr int kStageA = BM * BK * 4;
+  static constexpr int kStageB = BK * BN * 4;
+  static constexpr int kStageBytes = kStageA + kStageB;
+  static constexpr int kAtBytes = BK * BM * 4;
+  static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0, "stages keep 1024-byte alignment");
+  static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * kAtBytes + STAGES * 8 + 1024;
+};
+
+template <int BN, int STAGES, int MINB>
+__global__ void __launch_bounds__(Shape<BN, STAGES>::kThreads, MINB)
+    sgemm_tmat_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const Params p) {
+  using S = Shape<BN, STAGES>;
+  constexpr int BM = S::BM;
+  constexpr int BK = S::BK;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw_base = ptx::smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+  const uint32_t smem_base = ptx::smem_addr(smem);
+  float* at_buf = reinterpret_cast<float*>(smem + STAGES * S::kStageBytes);  // [2][BK][BM]
+  const uint32_t bar_full = smem_base + STAGES * S::kStageBytes + 2 * S::kAtBytes;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tiles_m = (p.M + BM - 1) / BM;
+  const int tiles_n = (p.N + BN - 1) / BN;
+  const int num_tiles = tiles_m * tiles_n;
+  const int KT = (p.K + BK - 1) / BK;
+  const int my_tiles = static_cast<int>(blockIdx.x) < num_tiles
+                           ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                           : 0;
+  const uint32_t total_it = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(KT);
+
+  // producer cursor (thread 0): slices are issued in order
+  int c_lt = 0, c_kt = 0, c_tm = 0, c_tn = 0;
+  auto issue = [&](uint32_t j) {
+    const uint32_t s = j % STAGES;
+    if (c_kt == 0) tile_coords(blockIdx.x + c_lt * gridDim.x, tiles_m, tiles_n, p.group_m, c_tm, c_tn);
+    const uint32_t dst = smem_base + s * S::kStageBytes;
+    ptx::mbar_arrive_expect_tx(bar_full + 8 * s, S::kStageBytes);
+    ptx::tma_load_2d(dst, &tmA, c_kt * BK, c_tm * BM, bar_full + 8 * s);
+    ptx::tma_load_2d(dst + S::kStageA, &tmB, c_tn * BN, c_kt * BK, bar_full + 8 * s);
+    if (++c_kt == KT) {
+      c_kt = 0;
+      ++c_lt;
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) ptx::mbar_init(bar_full + 8 * s, 1);
+    ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB);
+    for (uint32_t j = 0; j < STAGES && j < total_it; ++j) issue(j);
+  }
+  __syncthreads();
+
+  // transpose mapping: row tr = t / 2, k-half th = t % 2 (16 k)
+  const int tr = threadIdx.x >> 1;
+  const int th = threadIdx.x & 1;
+  bool failed;
+  // Transpose A of slice j (ring stage j % STAGES) into at_buf[j & 1].
+  auto transpose = [&](uint32_t j) -> bool {
+    const uint32_t s = j % STAGES;
+    if (!ptx::mbar_wait(bar_full + 8 * s, (j / STAGES) & 1u, p.timeout_ns)) {
+      atomicOr(p.status, kStatusTimeoutFull);
+      return false;
+    }
+    const float* As = reinterpret_cast<const float*>(smem + s * S::kStageBytes) + tr * BK;
+    float* At = at_buf + (j & 1) * (BK * BM);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int chunk = 4 * th + q;  // k = 4*chunk .. +3
+      const float4 v = *reinterpret_cast<const float4*>(As + ((chunk ^ (tr & 7)) << 2));
+      const float e4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = 4 * chunk + u;
+        At[k * BM + (tr ^ (16 * th))] = e4[u];  // (k >> 4) & 1 == th
+      }
+    }
+    return true;
+  };
+
+  const int wm = warp / S::kWarpsN;
+  const int wn = warp % S::kWarpsN;
+  const int g = lane >> 2;
+  const int c = lane & 3;
+
+  // failures are made CTA-uniform through the barrier, so every thread
+  // leaves the loop at the same slice and no barrier is left waiting
+  failed = __syncthreads_or(total_it > 0 && !transpose(0)) != 0;
+
+  uint32_t it = 0;
+  for (int tile = blockIdx.x; tile < num_tiles && !failed; tile += gridDim.x) {
+    int tm, tn;
+    tile_coords(tile, tiles_m, tiles_n, p.group_m, tm, tn);
+
+    // acc[i][j] = {C[row 16i+2g][col j], C[row 16i+2g+1][col j]}, col j = 4c + 16(j/4) + j%4
+    float2 acc[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = make_float2(0.f, 0.f);
+
+    for (int kt = 0; kt < KT; ++kt, ++it) {
+      // the next slice's A, transposed ahead (its buffer was last read one slice ago)
+      const bool bad = it + 1 < total_it && !transpose(it + 1);
+      const uint32_t s = it % STAGES;
+      const float* At = at_buf + (it & 1) * (BK * BM) + wm * 64 + 2 * g;
+      const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + (wn * 32 + 4 * c) / 4;
+#pragma unroll
+      for (int k = 0; k < BK; ++k) {
+        float2 ap[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          ap[i] = *reinterpret_cast<const float2*>(At + k * BM + 16 * (i ^ ((k >> 4) & 1)));
+        const float4 b0 = Bs4[k * (BN / 4)];
+        const float4 b1 = Bs4[k * (BN / 4) + 4];
+        const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = __ffma2_rn(ap[i], make_float2(bb[j], bb[j]), acc[i][j]);
+      }
+      // every warp is done with stage s and At[it & 1]; At[(it+1) & 1] is complete
+      failed = __syncthreads_or(bad) != 0;
+      if (failed) break;
+      if (threadIdx.x == 0 && it + STAGES < total_it) {
+        ptx::fence_proxy_async_smem();
+        issue(it + STAGES);
+      }
+    }
+    if (failed) break;
+
+    // ---------------- epilogue ----------------
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int row = tm * BM + wm * 64 + 16 * i + 2 * g + e;
+        if (row >= p.M) continue;
+        float* crow = p.C + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int col = tn * BN + wn * 32 + 4 * c + 16 * h;
+          float v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[q] = e ? acc[i][4 * h + q].y : acc[i][4 * h + q].x;
+          if (p.vec_c && col + 3 < p.N) {
+            float4* dst = reinterpret_cast<float4*>(crow + col);
+            float4 o;
+            if (p.beta == 0.f) {
+              o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
+            } else {
+              const float4 old = *dst;
+              o = make_float4(fmaf(p.alpha, v[0], p.beta * old.x), fmaf(p.alpha, v[1], p.beta * old.y),
+                              fmaf(p.alpha, v[2], p.beta * old.z), fmaf(p.alpha, v[3], p.beta * old.w));
+            }
+            *dst = o;
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (col + q < p.N) {
+                float* d = crow + col + q;
+                *d = p.beta == 0.f ? p.alpha * v[q] : fmaf(p.alpha, v[q], p.beta * *d);
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int BN, int STAGES, int MINB>
+struct Variant_ {
+  using S = Shape<BN, STAGES>;
+  static constexpr auto kernel = sgemm_tmat_kernel<BN, STAGES, MINB>;
+  static cudaError_t prepare() {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  }
+  static cudaError_t occupancy(int* ctas) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kernel, S::kThreads, S::kSmemBytes);
+  }
+  static cudaError_t launch(const LaunchArgs& a, cudaStream_t stream) {
+    Params p;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    p.vec_c = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && (a.ldc % 4 == 0);
+    p.group_m = 8;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    kernel<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    return cudaGetLastError();
+  }
+  static Variant describe(const char* name) {
+    return Variant{name, kKindTma, S::BM, BN, S::BK, STAGES, 1, S::kThreads, S::kSmemBytes, 128,
+                   &prepare, &occupancy, &launch};
+  }
+};
+
+}  // namespace tmat
+}  // namespace sgemm

@@ -119,7 +119,7 @@ def _shape_cases(n=40, seed=0):
     return sorted(cases)
 
 
-@pytest.mark.parametrize("variant_idx", range(16))
+@pytest.mark.parametrize("variant_idx", range(24))
 def test_shape_sweep_every_variant(sg, oracle_mod, variant_idx):
     names = _variants(sg)
     if variant_idx >= len(names):
@@ -358,3 +358,16 @@ def test_misaligned_and_guarded_few_rows(sg, oracle_mod):
         assert_parity(C, Cref, S, K, f"{name} nan C")
         C, used = run_gpu(sg, A, B, C0, 1.0, 0.0, config=name, off_a=1)
         assert_parity(C, Cref, S, K, f"{name} misaligned A -> {used}")
+
+
+def test_transposed_a_variants_take_any_lda(sg, oracle_mod):
+    """The kernels that copy A themselves accept any lda and any A alignment
+    and stay on their own path (no scalar-load fallback)."""
+    M, N, K = 190, 260, 133
+    A, B, C0 = make_inputs(M, N, K, seed=31, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
+    Cref, S = oracle_mod.sgemm_ref(A, B, C0, 0.5, 3.0)
+    for name in [n for n in sg.config_names() if n.startswith("cpa")]:
+        for lda, off_a in ((K, 0), (K + 1, 0), (K + 3, 1)):
+            C, used = run_gpu(sg, A, B, C0, 0.5, 3.0, config=name, lda=lda, off_a=off_a)
+            assert used == name
+            assert_parity(C, Cref, S, K, f"{name} lda={lda} off_a={off_a}")
