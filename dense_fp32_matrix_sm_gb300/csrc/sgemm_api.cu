@@ -131,12 +131,14 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
 // names.  The entries come from the measured sweeps on GB300.
 const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms) {
   (void)K;
-  (void)lda;
-  (void)num_sms;
   if (ldb % 4 != 0) return "generic_64x64x16";
   if (M <= 16 && lda % 4 == 0) return "skinny_16x128x32_w4_s3_b3_ef";
   if (lda % 4 != 0) return "cpa_128x128x32_s3_k8_b2";  // A copied 4 bytes at a time: any lda
   if (M * N <= 256 * 256) return "tma_128x64x32_w64x32_s3_quad_b3";
+  // 128 x 256 tiles when there are enough of them to fill every SM about
+  // ten times over (tile-count rounding then costs little); else 128 x 128
+  const int64_t wide_tiles = ((M + 127) / 128) * ((N + 255) / 256);
+  if (wide_tiles >= 10 * static_cast<int64_t>(num_sms)) return "tmat_128x256x32_s3_b1";
   return "tmat_128x128x32_s4_b1";
 }
 

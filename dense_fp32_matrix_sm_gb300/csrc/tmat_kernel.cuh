@@ -16,10 +16,11 @@
 //    [BK][BN] into a STAGES-deep ring signalled by mbarriers, as in
 //    tma_kernel.cuh.
 //  * One slice ahead of the math, all threads transpose the A slice into a
-//    double-buffered At[BK][BM]: thread t reads row t/2, k-half t%2 (four
-//    128-bit loads) and writes 16 words At[k][m ^ 16*((k >> 4) & 1)].  The
-//    XOR puts the two k-halves of a warp's 16 rows in opposite bank halves
-//    (conflict-free writes) and keeps pairs (m, m+1) adjacent.
+//    double-buffered At[BK][BM]: with T = threads/BM (1, 2 or 4) threads per
+//    row, thread t reads row t/T, k-part t%T (BK/T k, 128-bit loads) and
+//    writes At[k][m ^ (32/T)*(k / (BK/T))].  The XOR puts the T k-parts of
+//    a warp's 32/T rows in different bank groups (conflict-free writes) and
+//    keeps pairs (m, m+1) adjacent.
 //    ("Learn: Optimizing GEMM", section 7, and "Writing a Fast Matmul in
 //    CUDA", Step 5: A stored transposed so the inner loop reads contiguous
 //    m -- here the transpose runs on the on-chip copy instead of on the
@@ -57,15 +58,19 @@ struct Params {
   uint64_t timeout_ns;
 };
 
-template <int BN, int STAGES>
+template <int BM_, int BN, int STAGES>
 struct Shape {
-  static constexpr int BM = 128;
+  static constexpr int BM = BM_;
   static constexpr int BK = 32;
   static constexpr int kWarpsM = BM / 64;
   static constexpr int kWarpsN = BN / 32;
   static constexpr int kWarps = kWarpsM * kWarpsN;
   static constexpr int kThreads = kWarps * 32;
-  static_assert(kThreads == 2 * BM, "transpose mapping: two threads per A row");
+  // transpose mapping: kTPR threads per A row, each taking BK/kTPR k
+  static constexpr int kTPR = kThreads / BM;
+  static_assert(kThreads % BM == 0 && (kTPR == 1 || kTPR == 2 || kTPR == 4), "1, 2 or 4 threads per A row");
+  static constexpr int kKPart = BK / kTPR;       // k per thread
+  static constexpr int kSwz = 32 / kTPR;         // At[k][m ^ kSwz*(k / kKPart)]
   static constexpr int kStageA = BM * BK * 4;
   static constexpr int kStageB = BK * BN * 4;
   static constexpr int kStageBytes = kStageA + kStageB;
@@ -74,11 +79,11 @@ struct Shape {
   static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * kAtBytes + STAGES * 8 + 1024;
 };
 
-template <int BN, int STAGES, int MINB>
-__global__ void __launch_bounds__(Shape<BN, STAGES>::kThreads, MINB)
+template <int BM_, int BN, int STAGES, int MINB>
+__global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
     sgemm_tmat_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const Params p) {
-  using S = Shape<BN, STAGES>;
+  using S = Shape<BM_, BN, STAGES>;
   constexpr int BM = S::BM;
   constexpr int BK = S::BK;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -123,9 +128,10 @@ __global__ void __launch_bounds__(Shape<BN, STAGES>::kThreads, MINB)
   }
   __syncthreads();
 
-  // transpose mapping: row tr = t / 2, k-half th = t % 2 (16 k)
-  const int tr = threadIdx.x >> 1;
-  const int th = threadIdx.x & 1;
+  // transpose mapping: row tr = t / kTPR, k-part th = t % kTPR (kKPart k)
+  const int tr = threadIdx.x / S::kTPR;
+  const int th = threadIdx.x % S::kTPR;
+  const int at_col = tr ^ (S::kSwz * th);  // k / kKPart == th for every k this thread writes
   bool failed;
   // Transpose A of slice j (ring stage j % STAGES) into at_buf[j & 1].
   auto transpose = [&](uint32_t j) -> bool {
@@ -137,15 +143,12 @@ __global__ void __launch_bounds__(Shape<BN, STAGES>::kThreads, MINB)
     const float* As = reinterpret_cast<const float*>(smem + s * S::kStageBytes) + tr * BK;
     float* At = at_buf + (j & 1) * (BK * BM);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int chunk = 4 * th + q;  // k = 4*chunk .. +3
+    for (int q = 0; q < S::kKPart / 4; ++q) {
+      const int chunk = (S::kKPart / 4) * th + q;  // k = 4*chunk .. +3
       const float4 v = *reinterpret_cast<const float4*>(As + ((chunk ^ (tr & 7)) << 2));
       const float e4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int k = 4 * chunk + u;
-        At[k * BM + (tr ^ (16 * th))] = e4[u];  // (k >> 4) & 1 == th
-      }
+      for (int u = 0; u < 4; ++u) At[(4 * chunk + u) * BM + at_col] = e4[u];
     }
     return true;
   };
@@ -154,6 +157,11 @@ __global__ void __launch_bounds__(Shape<BN, STAGES>::kThreads, MINB)
   const int wn = warp % S::kWarpsN;
   const int g = lane >> 2;
   const int c = lane & 3;
+  // A pair i of this lane starts at m = wm*64 + 16i + 2g and is stored at
+  // m ^ f(k), f(k) = kSwz * (k / kKPart) < 32:
+  // (16i + 2g) ^ f = 16*(i ^ (f >> 4)) + (2g ^ (f & 15)); f & 15 is 0 or 8.
+  const int a_lo0 = wm * 64 + (2 * g);
+  const int a_lo8 = wm * 64 + ((2 * g) ^ 8);
 
   // failures are made CTA-uniform through the barrier, so every thread
   // leaves the loop at the same slice and no barrier is left waiting
@@ -175,14 +183,16 @@ __global__ void __launch_bounds__(Shape<BN, STAGES>::kThreads, MINB)
       // the next slice's A, transposed ahead (its buffer was last read one slice ago)
       const bool bad = it + 1 < total_it && !transpose(it + 1);
       const uint32_t s = it % STAGES;
-      const float* At = at_buf + (it & 1) * (BK * BM) + wm * 64 + 2 * g;
+      const float* At = at_buf + (it & 1) * (BK * BM);
       const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + (wn * 32 + 4 * c) / 4;
 #pragma unroll
       for (int k = 0; k < BK; ++k) {
         float2 ap[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          ap[i] = *reinterpret_cast<const float2*>(At + k * BM + 16 * (i ^ ((k >> 4) & 1)));
+        for (int i = 0; i < 4; ++i) {
+          const int f = S::kSwz * (k / S::kKPart);
+          ap[i] = *reinterpret_cast<const float2*>(At + k * BM + ((f & 15) ? a_lo8 : a_lo0) + 16 * (i ^ (f >> 4)));
+        }
         const float4 b0 = Bs4[k * (BN / 4)];
         const float4 b1 = Bs4[k * (BN / 4) + 4];
         const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
@@ -241,10 +251,10 @@ __global__ void __launch_bounds__(Shape<BN, STAGES>::kThreads, MINB)
   }
 }
 
-template <int BN, int STAGES, int MINB>
+template <int BM_, int BN, int STAGES, int MINB>
 struct Variant_ {
-  using S = Shape<BN, STAGES>;
-  static constexpr auto kernel = sgemm_tmat_kernel<BN, STAGES, MINB>;
+  using S = Shape<BM_, BN, STAGES>;
+  static constexpr auto kernel = sgemm_tmat_kernel<BM_, BN, STAGES, MINB>;
   static cudaError_t prepare() {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   }

@@ -1,12 +1,16 @@
 // tmat_variants.cu -- instantiations of the TMA + in-shared-memory transposed-A
-// kernel (see tmat_kernel.cuh).  Name: tmat_128x<BN>x32_s<STAGES>_b<CTAs per SM>.
+// kernel (see tmat_kernel.cuh).  Name: tmat_<BM>x<BN>x32_s<STAGES>_b<CTAs per SM>.
 #include "tmat_kernel.cuh"
 
 namespace sgemm {
 namespace {
 const Variant kVariants[] = {
-    tmat::Variant_<128, 4, 1>::describe("tmat_128x128x32_s4_b1"),
-    tmat::Variant_<128, 3, 1>::describe("tmat_128x128x32_s3_b1"),
+    tmat::Variant_<128, 128, 4, 1>::describe("tmat_128x128x32_s4_b1"),
+    tmat::Variant_<128, 128, 5, 1>::describe("tmat_128x128x32_s5_b1"),
+    tmat::Variant_<128, 128, 6, 1>::describe("tmat_128x128x32_s6_b1"),
+    tmat::Variant_<128, 64, 3, 2>::describe("tmat_128x64x32_s3_b2"),
+    tmat::Variant_<256, 128, 3, 1>::describe("tmat_256x128x32_s3_b1"),
+    tmat::Variant_<128, 256, 3, 1>::describe("tmat_128x256x32_s3_b1"),
 };
 }  // namespace
 
