@@ -18,17 +18,26 @@
 //    (read by every CTA) out of L2.  A TMA ring (A slice 16 x 32 with the 128-byte
 //    swizzle, B slice 32 x 128) feeds it exactly like the main kernel, with
 //    the same stage-release counters and bounded waits.
+//  * Cluster c walks column slabs c, c + #clusters, ...  With one slab per
+//    cluster (the default grid) clusters come and go independently; the
+//    _persist variant launches only as many clusters as fit on the GPU at
+//    once and keeps each TMA ring running across slab boundaries (measured
+//    slower on the 16 x 16384 x 8192 decode shape: lock-stepped clusters).
 //  * Split-K without scratch memory ("How a Matmul Kernel Gets Fast",
 //    section 14, and "Writing a Fast Matmul in CUDA", "What cuBLAS and
 //    CUTLASS add": split the k loop across blocks and add the pieces):
 //    the S CTAs that share a column slab form one thread-block cluster and
 //    take consecutive k-ranges.  Each CTA first adds, per column group, its GW warps'
-//    partial tiles in shared memory (warp order 0..GW-1), then the cluster
+//    partial tiles into one shared tile (warp order 0..GW-1), then the cluster
 //    synchronises and CTA r finalises 1/S of the 16 x 128 outputs by
 //    reading the S partial tiles through distributed shared memory in rank
 //    order 0..S-1.  The reduction order is fixed, so results are
 //    reproducible run to run; it is not the ascending-k chain of the
 //    single-pass kernels (the plan reports k_order=split).
+//  * _pa variants multiply in the paired form the main kernels found
+//    fastest on GB300: each warp transposes its own 16 x 4 k-quad of A into
+//    a small per-warp buffer (no CTA barrier), then each FFMA2 multiplies a
+//    register pair of two A rows by one broadcast element of B.
 //  * Epilogue: out = alpha*sum (beta == 0, C not read) or
 //    fmaf(alpha, sum, beta*C), predicated on m < M and n < N.
 #include <cuda.h>
@@ -57,6 +66,7 @@ struct SkinnyParams {
 // splitting each k-slice's eight quads.
 template <int BN, int GW, int STAGES>
 struct SkinnyShape {
+  static constexpr int kAtwBytes = 4 * 32 * 4;  // per warp: one transposed k-quad, rows padded to 32
   static_assert(GW == 4 || GW == 8, "each warp takes 8 / GW quads of a 32-deep slice");
   static constexpr int kQuadsPerWarp = (kSBK / 4) / GW;
   static_assert(BN % 128 == 0 && BN <= 256, "a warp spans 128 columns (32 lanes x 4); one TMA box spans <= 256");
@@ -68,10 +78,8 @@ struct SkinnyShape {
   static constexpr int kStageBytes = kStageA + kStageB;
   static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0, "stages keep 1024-byte alignment");
   static constexpr int kRingBytes = STAGES * kStageBytes;
-  static constexpr int kRedBytes = GW * kSBM * BN * 4;  // warp partials, reuses the ring
-  static_assert(kRingBytes >= kRedBytes, "the ring must hold the warps' partial tiles");
   static constexpr int kPartialBytes = kSBM * BN * 4;
-  static constexpr int kSmemBytes = kRingBytes + kPartialBytes + STAGES * 16 + 1024;
+  static constexpr int kSmemBytes = kRingBytes + kPartialBytes + kWarps * kAtwBytes + STAGES * 16 + 1024;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -100,18 +108,21 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
   return v;
 }
 
-template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST>
+template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST, bool PAIRA>
 __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     sgemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const SkinnyParams p) {
   using S = SkinnyShape<BN, GW, STAGES>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ int s_failed;  // set when any wait of this CTA ran out; later waits are skipped
   const uint32_t raw_base = ptx::smem_addr(smem_raw);
   unsigned char* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
   const uint32_t smem_base = ptx::smem_addr(smem);
   float* partial = reinterpret_cast<float*>(smem + S::kRingBytes);  // [16][BN], read by cluster peers
-  const uint32_t bar_full = smem_base + S::kRingBytes + S::kPartialBytes;
-  unsigned int* released = reinterpret_cast<unsigned int*>(smem + S::kRingBytes + S::kPartialBytes + STAGES * 8);
+  constexpr int kBarOff = S::kRingBytes + S::kPartialBytes + S::kWarps * S::kAtwBytes;
+  float* atw = reinterpret_cast<float*>(smem + S::kRingBytes + S::kPartialBytes) + (threadIdx.x >> 5) * (S::kAtwBytes / 4);
+  const uint32_t bar_full = smem_base + kBarOff;
+  unsigned int* released = reinterpret_cast<unsigned int*>(smem + kBarOff + STAGES * 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -119,16 +130,23 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
   const int gw = warp % GW;     // k-quads gw, gw + GW, ... of each slice
   const uint32_t rank = cluster_rank();
   const uint32_t nsplit = cluster_size();
-  const int slab = static_cast<int>(blockIdx.x / nsplit);
-  const int n0 = slab * BN;
+  // Persistent clusters: cluster cid walks column slabs cid, cid + ncl, ...;
+  // its S CTAs take the same consecutive k-ranges of every slab.
+  const int cid = static_cast<int>(blockIdx.x / nsplit);
+  const int ncl = static_cast<int>(gridDim.x / nsplit);
+  const int nslabs = (p.N + BN - 1) / BN;
+  const int my_slabs = cid < nslabs ? (nslabs - 1 - cid) / ncl + 1 : 0;
   const int KT = (p.K + kSBK - 1) / kSBK;
   const int kt_begin = static_cast<int>((static_cast<int64_t>(KT) * rank) / nsplit);
   const int kt_end = static_cast<int>((static_cast<int64_t>(KT) * (rank + 1)) / nsplit);
   const uint32_t nkt = static_cast<uint32_t>(kt_end - kt_begin);
+  const uint32_t total_it = static_cast<uint32_t>(my_slabs) * nkt;
 
+  // slices are numbered j = local_slab * nkt + (kt - kt_begin) over all of this CTA's slabs
   auto issue = [&](uint32_t j) {
     const uint32_t s = j % STAGES;
-    const int kt = kt_begin + static_cast<int>(j);
+    const int kt = kt_begin + static_cast<int>(j % nkt);
+    const int n0 = (cid + static_cast<int>(j / nkt) * ncl) * BN;
     const uint32_t dst = smem_base + s * S::kStageBytes;
     ptx::mbar_arrive_expect_tx(bar_full + 8 * s, S::kStageBytes);
     ptx::tma_load_2d(dst, &tmA, kt * kSBK, 0, bar_full + 8 * s);
@@ -140,6 +158,7 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
   };
 
   if (threadIdx.x == 0) {
+    s_failed = 0;
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(bar_full + 8 * s, 1);
       released[s] = 0u;
@@ -147,94 +166,146 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tmA);
     ptx::prefetch_tensormap(&tmB);
-    for (uint32_t j = 0; j < STAGES && j < nkt; ++j) issue(j);
+    for (uint32_t j = 0; j < STAGES && j < total_it; ++j) issue(j);
   }
   __syncthreads();
 
-  // acc[m][0] = columns 4l, 4l+1 of row m; acc[m][1] = columns 4l+2, 4l+3
-  float2 acc[kSBM][2];
-#pragma unroll
-  for (int m = 0; m < kSBM; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
-
+  uint32_t it = 0;
   bool ready = false;
-  for (uint32_t it = 0; it < nkt; ++it) {
-    const uint32_t s = it % STAGES;
-    if (!ready && !ptx::mbar_wait(bar_full + 8 * s, (it / STAGES) & 1u, p.timeout_ns)) {
-      atomicOr(p.status, kStatusTimeoutFull);
-      break;  // stay in step with the CTA and cluster barriers below
-    }
-    if (it + 1 < nkt) ready = ptx::mbar_test_wait(bar_full + 8 * ((it + 1) % STAGES), ((it + 1) / STAGES) & 1u);
-    const float* As = reinterpret_cast<const float*>(smem + s * S::kStageBytes);
-    const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + group * 32 + lane;
+  for (int ls = 0; ls < my_slabs; ++ls) {
+    const int n0 = (cid + ls * ncl) * BN;
+    // row-major form: acc[m][0] = columns 4l, 4l+1 of row m; acc[m][1] = columns 4l+2, 4l+3.
+    // pair form (PAIRA): accp[p][j] = {C[2p][4l + j], C[2p+1][4l + j]}.
+    float2 acc[kSBM][2];
+    float2 accp[kSBM / 2][4];
 #pragma unroll
-    for (int qq = 0; qq < S::kQuadsPerWarp; ++qq) {
-      const int q = gw + GW * qq;
-      float4 a4[kSBM];
+    for (int m = 0; m < kSBM; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int m = 0; m < kSBM; ++m)
-        a4[m] = *reinterpret_cast<const float4*>(As + m * kSBK + ((q ^ (m & 7)) << 2));
+    for (int q = 0; q < kSBM / 2; ++q)
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const float4 b = Bs4[(4 * q + kk) * (BN / 4)];
-        const float2 b01 = make_float2(b.x, b.y);
-        const float2 b23 = make_float2(b.z, b.w);
+      for (int j = 0; j < 4; ++j) accp[q][j] = make_float2(0.f, 0.f);
+
+    for (uint32_t kk_it = 0; kk_it < nkt; ++kk_it, ++it) {
+      if (*reinterpret_cast<volatile int*>(&s_failed)) continue;
+      const uint32_t s = it % STAGES;
+      if (!ready && !ptx::mbar_wait(bar_full + 8 * s, (it / STAGES) & 1u, p.timeout_ns)) {
+        atomicOr(p.status, kStatusTimeoutFull);
+        *reinterpret_cast<volatile int*>(&s_failed) = 1;
+        continue;  // keep step with the CTA and cluster barriers below
+      }
+      ready = it + 1 < total_it &&
+              ptx::mbar_test_wait(bar_full + 8 * ((it + 1) % STAGES), ((it + 1) / STAGES) & 1u);
+      const float* As = reinterpret_cast<const float*>(smem + s * S::kStageBytes);
+      const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + group * 32 + lane;
 #pragma unroll
-        for (int m = 0; m < kSBM; ++m) {
-          const float a = kk == 0 ? a4[m].x : kk == 1 ? a4[m].y : kk == 2 ? a4[m].z : a4[m].w;
-          const float2 aa = make_float2(a, a);
-          acc[m][0] = __ffma2_rn(aa, b01, acc[m][0]);
-          acc[m][1] = __ffma2_rn(aa, b23, acc[m][1]);
+      for (int qq = 0; qq < S::kQuadsPerWarp && PAIRA; ++qq) {
+        // Transpose this warp's k-quad of A (16 rows x 4 k) into atw[k][m]:
+        // lane takes row l/2, k pair 2*(l%2); rows are 32 floats apart and
+        // k = 2, 3 sit 16 floats further in, so the 32 writes hit 32 banks.
+        const int q = gw + GW * qq;
+        {
+          const int m = lane >> 1, h = lane & 1;
+          const float2 v = *reinterpret_cast<const float2*>(As + m * kSBK + ((q ^ (m & 7)) << 2) + 2 * h);
+          atw[(2 * h) * 32 + 16 * h + m] = v.x;
+          atw[(2 * h + 1) * 32 + 16 * h + m] = v.y;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float4 b = Bs4[(4 * q + kk) * (BN / 4)];
+          const float bb[4] = {b.x, b.y, b.z, b.w};
+          const float* ak = atw + kk * 32 + 16 * ((kk >> 1) & 1);
+#pragma unroll
+          for (int pp = 0; pp < kSBM / 2; ++pp) {
+            const float2 ap = *reinterpret_cast<const float2*>(ak + 2 * pp);  // rows 2pp, 2pp+1
+#pragma unroll
+            for (int j = 0; j < 4; ++j) accp[pp][j] = __ffma2_rn(ap, make_float2(bb[j], bb[j]), accp[pp][j]);
+          }
+        }
+        __syncwarp();  // the next quad overwrites atw
+      }
+#pragma unroll
+      for (int qq = 0; qq < S::kQuadsPerWarp && !PAIRA; ++qq) {
+        const int q = gw + GW * qq;
+        float4 a4[kSBM];
+#pragma unroll
+        for (int m = 0; m < kSBM; ++m)
+          a4[m] = *reinterpret_cast<const float4*>(As + m * kSBK + ((q ^ (m & 7)) << 2));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float4 b = Bs4[(4 * q + kk) * (BN / 4)];
+          const float2 b01 = make_float2(b.x, b.y);
+          const float2 b23 = make_float2(b.z, b.w);
+#pragma unroll
+          for (int m = 0; m < kSBM; ++m) {
+            const float a = kk == 0 ? a4[m].x : kk == 1 ? a4[m].y : kk == 2 ? a4[m].z : a4[m].w;
+            const float2 aa = make_float2(a, a);
+            acc[m][0] = __ffma2_rn(aa, b01, acc[m][0]);
+            acc[m][1] = __ffma2_rn(aa, b23, acc[m][1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const unsigned int before = ptx::atom_add_acq_rel_cta(&released[s], 1u);
+        if ((before + 1u) % S::kWarps == 0u && it + STAGES < total_it) {
+          ptx::fence_proxy_async_smem();
+          issue(it + STAGES);
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) {
-      const unsigned int before = ptx::atom_add_acq_rel_cta(&released[s], 1u);
-      if ((before + 1u) % S::kWarps == 0u && it + STAGES < nkt) {
-        ptx::fence_proxy_async_smem();
-        issue(it + STAGES);
+
+    // ---- this slab: add each column group's GW warp partials into `partial` (warp order) ----
+    // The ring keeps streaming the next slab meanwhile.
+#pragma unroll 1
+    for (int w = 0; w < GW; ++w) {
+      if (gw == w) {
+        float4* part4 = reinterpret_cast<float4*>(partial);
+#pragma unroll
+        for (int m = 0; m < kSBM; ++m) {
+          float4 v;
+          if constexpr (PAIRA) {
+            const int pp = m >> 1;
+            v = (m & 1) ? make_float4(accp[pp][0].y, accp[pp][1].y, accp[pp][2].y, accp[pp][3].y)
+                        : make_float4(accp[pp][0].x, accp[pp][1].x, accp[pp][2].x, accp[pp][3].x);
+          } else {
+            v = make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
+          }
+          float4* d = part4 + m * (BN / 4) + group * 32 + lane;
+          if (w == 0) {
+            *d = v;
+          } else {
+            const float4 o = *d;
+            *d = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+          }
+        }
+      }
+      __syncthreads();
+    }
+
+    // ---- reduce the cluster's partial tiles (rank order) and write C ----
+    cluster_sync();
+    constexpr int kTile = kSBM * BN;
+    const int begin = static_cast<int>((static_cast<int64_t>(kTile) * rank) / nsplit);
+    const int end = static_cast<int>((static_cast<int64_t>(kTile) * (rank + 1)) / nsplit);
+    for (int idx = begin + static_cast<int>(threadIdx.x); idx < end; idx += S::kThreads) {
+      const int m = idx / BN;
+      const int n = n0 + idx % BN;
+      float sum = 0.f;
+      for (uint32_t r = 0; r < nsplit; ++r) sum += ld_peer(partial + idx, r);
+      if (m < p.M && n < p.N) {
+        float* d = p.C + static_cast<int64_t>(m) * p.ldc + n;
+        *d = p.beta == 0.f ? p.alpha * sum : fmaf(p.alpha, sum, p.beta * *d);
       }
     }
+    cluster_sync();  // peers may still be reading this CTA's partial tile
   }
-
-  // ---- reduce each column group's GW warp partials (fixed order) ----
-  __syncthreads();  // every stage consumed: the ring is free
-  float4* red4 = reinterpret_cast<float4*>(smem);  // [gw][16][BN/4]
-#pragma unroll
-  for (int m = 0; m < kSBM; ++m)
-    red4[(gw * kSBM + m) * (BN / 4) + group * 32 + lane] =
-        make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
-  __syncthreads();
-  const float* red = reinterpret_cast<const float*>(smem);
-  constexpr int kTile = kSBM * BN;
-  for (int idx = threadIdx.x; idx < kTile; idx += S::kThreads) {
-    float sum = red[idx];
-#pragma unroll
-    for (int w = 1; w < GW; ++w) sum += red[idx + w * kTile];
-    partial[idx] = sum;
-  }
-
-  // ---- reduce the cluster's partial tiles (rank order) and write C ----
-  cluster_sync();
-  const int begin = static_cast<int>((static_cast<int64_t>(kTile) * rank) / nsplit);
-  const int end = static_cast<int>((static_cast<int64_t>(kTile) * (rank + 1)) / nsplit);
-  for (int idx = begin + static_cast<int>(threadIdx.x); idx < end; idx += S::kThreads) {
-    const int m = idx / BN;
-    const int n = n0 + idx % BN;
-    float sum = 0.f;
-    for (uint32_t r = 0; r < nsplit; ++r) sum += ld_peer(partial + idx, r);
-    if (m < p.M && n < p.N) {
-      float* d = p.C + static_cast<int64_t>(m) * p.ldc + n;
-      *d = p.beta == 0.f ? p.alpha * sum : fmaf(p.alpha, sum, p.beta * *d);
-    }
-  }
-  cluster_sync();  // peers may still be reading this CTA's partial tile
 }
 
-template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST>
+template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST, bool PAIRA = false, int PERSIST = 0>
 struct SkinnyVariant {
   using S = SkinnyShape<BN, GW, STAGES>;
-  static constexpr auto kernel = sgemm_skinny_kernel<BN, GW, STAGES, MINB, EVICT_FIRST>;
+  static constexpr auto kernel = sgemm_skinny_kernel<BN, GW, STAGES, MINB, EVICT_FIRST, PAIRA>;
   static cudaError_t prepare() {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   }
@@ -269,14 +340,15 @@ struct SkinnyVariant {
   }
   static Variant describe(const char* name) {
     return Variant{name, kKindSkinny, kSBM, BN, kSBK, STAGES, 1, S::kThreads, S::kSmemBytes, 128, &prepare, &occupancy,
-                   &launch};
+                   &launch, PERSIST};
   }
 };
 
 const Variant kSkinnyVariants[] = {
-    SkinnyVariant<128, 4, 3, 3, false>::describe("skinny_16x128x32_w4_s3_b3"),
-    SkinnyVariant<128, 4, 3, 3, true>::describe("skinny_16x128x32_w4_s3_b3_ef"),
-    SkinnyVariant<128, 4, 4, 2, true>::describe("skinny_16x128x32_w4_s4_b2_ef"),
+    SkinnyVariant<128, 4, 3, 3, true, true>::describe("skinny_16x128x32_w4_s3_b3_ef_pa"),
+    SkinnyVariant<128, 4, 3, 3, true, false>::describe("skinny_16x128x32_w4_s3_b3_ef"),
+    SkinnyVariant<128, 4, 3, 3, true, true, 1>::describe("skinny_16x128x32_w4_s3_b3_ef_pa_persist"),
+    SkinnyVariant<128, 4, 3, 3, false, true>::describe("skinny_16x128x32_w4_s3_b3_pa"),
 };
 
 }  // namespace

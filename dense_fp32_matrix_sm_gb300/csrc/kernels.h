@@ -40,12 +40,13 @@ struct Variant {
   int ffma2;             // 1: inner product issued as paired fp32 FMAs
   int threads;           // threads per CTA
   int smem_bytes;        // dynamic shared memory per CTA
-  int tma_swizzle_a;     // 0 none, 128: A tile uses the 128-byte swizzle
+  int tma_swizzle_a;     // 0 none, 64/128: A tile swizzle; -1: the variant takes no tensor maps
   // set kernel attributes for the current device (idempotent)
   cudaError_t (*prepare)();
   // resident CTAs per SM for this variant on the current device
   cudaError_t (*occupancy)(int* ctas_per_sm);
   cudaError_t (*launch)(const LaunchArgs& args, cudaStream_t stream);
+  int persistent;        // few-row kernels: 1 = clusters walk several column slabs
 };
 
 // Variant tables, one per kernel translation unit.

@@ -8,6 +8,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <new>
@@ -117,13 +118,15 @@ sgemm_status_t check_dims(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
 }
 
 bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb) {
-  (void)N;
   (void)K;
   if (v->kind == kKindGeneric) return true;
   if (ldb % 4 != 0) return false;  // TMA row strides must be multiples of 16 bytes
   if (v->kind == kKindCpa) return true;  // A is copied 4 bytes at a time: any lda
   if (lda % 4 != 0) return false;
-  if (v->kind == kKindSkinny) return M <= v->bm;
+  if (v->kind == kKindSkinny) {
+    // the register-streaming form reads whole float4s of B: N must be a multiple of 4
+    return M <= v->bm && (v->tma_swizzle_a >= 0 || N % 4 == 0);
+  }
   return true;
 }
 
@@ -132,7 +135,7 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
 const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms) {
   (void)K;
   if (ldb % 4 != 0) return "generic_64x64x16";
-  if (M <= 16 && lda % 4 == 0) return "skinny_16x128x32_w4_s3_b3_ef";
+  if (M <= 16 && lda % 4 == 0) return "skinny_16x128x32_w4_s3_b3_ef_pa";
   if (lda % 4 != 0) return "cpa_128x128x32_s3_k8_b2";  // A copied 4 bytes at a time: any lda
   if (M * N <= 256 * 256) return "tma_128x64x32_w64x32_s3_quad_b3";
   // 128 x 256 tiles when there are enough of them to fill every SM about
@@ -167,7 +170,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   }
   const Variant* v = reg.all[config_id];
   if (!variant_supports(v, M, N, K, lda, ldb)) return SGEMM_ERR_UNSUPPORTED;
-  if (v->kind != kKindGeneric && !encode_fn()) return SGEMM_ERR_CUDA;
+  if (v->kind != kKindGeneric && v->tma_swizzle_a >= 0 && !encode_fn()) return SGEMM_ERR_CUDA;
 
   unsigned int* status = nullptr;
   st = status_addr(device, &status);
@@ -199,25 +202,39 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     const int64_t slots = static_cast<int64_t>(sms) * ctas;
     if (grid > slots) grid = slots;
   } else if (v->kind == kKindSkinny) {
-    // Split K over a cluster of S CTAs per column slab (S <= 8, the portable
-    // cluster size).  Pick S so the CTAs spread evenly over the SMs: score =
-    // (CTAs per SM) / ceil(CTAs per SM), times the fraction of CTA slots
-    // filled; ties go to the larger S.
+    // Persistent clusters of S CTAs (S <= 8, the portable cluster size)
+    // split K; each cluster walks column slabs.  Pick S and the cluster
+    // count so the slabs divide evenly over clusters that all fit on the
+    // GPU at once: efficiency = slabs / (clusters * rounds) * (resident
+    // CTAs used / CTA slots); ties go to the larger S.
     const int64_t KT = (K + v->bk - 1) / v->bk;
+    const int64_t slots = static_cast<int64_t>(sms) * ctas;
     double best = -1.0;
+    int64_t best_ncl = 1;
     for (int s = 1; s <= 8 && s <= KT; ++s) {
-      const double total = static_cast<double>(p->tiles) * s;
-      const double per_sm = total / sms;
-      const double balance = per_sm / static_cast<double>(static_cast<int64_t>(per_sm + 0.999999));
-      const double fill = total >= static_cast<double>(sms) * ctas ? 1.0 : total / (static_cast<double>(sms) * ctas);
-      const double score = balance * fill;
-      if (score >= best - 1e-9) {
-        best = score;
+      // one slab per cluster unless the variant keeps clusters resident
+      const int64_t ncl = v->persistent ? std::min<int64_t>(p->tiles, std::max<int64_t>(1, slots / s)) : p->tiles;
+      double eff;
+      if (v->persistent) {
+        const int64_t rounds = (p->tiles + ncl - 1) / ncl;
+        eff = static_cast<double>(p->tiles) / static_cast<double>(ncl * rounds) *
+              std::min(1.0, static_cast<double>(ncl * s) / static_cast<double>(slots));
+      } else {
+        // CTAs spread over SMs: (CTAs per SM) / ceil(CTAs per SM), times the filled fraction of slots
+        const double total = static_cast<double>(ncl) * s;
+        const double per_sm = total / sms;
+        eff = per_sm / static_cast<double>(static_cast<int64_t>(per_sm + 0.999999)) *
+              std::min(1.0, total / static_cast<double>(slots));
+      }
+      if (eff >= best - 1e-9) {
+        best = eff;
         p->split = s;
+        best_ncl = ncl;
       }
     }
-    grid = p->tiles * p->split;
+    grid = best_ncl * p->split;
   }
+
   p->grid = static_cast<int>(grid > 0x7fffffff ? 0x7fffffff : grid);
   *out = p;
   return SGEMM_OK;
@@ -315,7 +332,7 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   sgemm_status_t st = status_addr(device, &a.status);
   if (st != SGEMM_OK) return st;
-  if (v->kind != kKindGeneric) {
+  if (v->kind != kKindGeneric && v->tma_swizzle_a >= 0) {
     st = encode_maps(v, p, A, B, &a);
     if (st != SGEMM_OK) return st;
   }

@@ -167,7 +167,12 @@ def test_skinny_variants(sg, oracle_mod, shape):
     lda, ldb = (K + 3) // 4 * 4, (N + 3) // 4 * 4
     for name in [n for n in sg.config_names() if n.startswith("skinny")] + [None]:
         for alpha, beta in ((1.0, 0.0), (1.0, 1.0), (-0.75, 2.0)):
-            C, used = run_gpu(sg, A, B, C0, alpha, beta, config=name, lda=lda, ldb=ldb)
+            try:
+                C, used = run_gpu(sg, A, B, C0, alpha, beta, config=name, lda=lda, ldb=ldb)
+            except sg.SgemmError as e:
+                if e.status == sg.SGEMM_ERR_UNSUPPORTED and name is not None:
+                    break  # this few-row variant does not take this shape
+                raise
             info = run_gpu.last_info
             assert name is not None or used.startswith("skinny"), used
             Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
