@@ -28,6 +28,12 @@ struct LaunchArgs {
   CUtensorMap tmB;
   int grid;              // CTAs to launch (persistent variants: <= tiles)
   int split_k;           // skinny variant: CTAs per cluster along K
+  // stream-K tail (variants with streamk = 1; sk_iters == 0 disables it)
+  int dp_waves;
+  int64_t sk_iters;
+  float* ws;
+  unsigned int* flags;
+  unsigned int epoch;
   unsigned int* status;  // per-device status word (error bits)
   uint64_t timeout_ns;   // limit for every in-kernel wait
 };
@@ -47,6 +53,7 @@ struct Variant {
   cudaError_t (*occupancy)(int* ctas_per_sm);
   cudaError_t (*launch)(const LaunchArgs& args, cudaStream_t stream);
   int persistent;        // few-row kernels: 1 = clusters walk several column slabs
+  int streamk;           // 1: the kernel can split its tail tiles along K (workspace per plan)
 };
 
 // Variant tables, one per kernel translation unit.

@@ -29,6 +29,13 @@ struct sgemm_plan_s {
   int grid;
   int split;        // CTAs per cluster along K (skinny variants), else 1
   int64_t tiles;
+  // stream-K tail (tmat variants): dp_waves full waves, then sk_iters k-slices
+  // split over the grid; ws/flags are device memory owned by the plan.
+  int dp_waves;
+  int64_t sk_iters;
+  float* ws;
+  unsigned int* flags;
+  std::atomic<unsigned int> epoch;
 };
 
 // Per-device status word written by kernels (timeouts).  Its device address
@@ -198,9 +205,39 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->tiles = ((M + v->bm - 1) / v->bm) * ((N + v->bn - 1) / v->bn);
   int64_t grid = p->tiles;
   p->split = 1;
+  p->dp_waves = 0;
+  p->sk_iters = 0;
+  p->ws = nullptr;
+  p->flags = nullptr;
+  p->epoch.store(0);
   if (v->kind == kKindTma || v->kind == kKindCpa) {
     const int64_t slots = static_cast<int64_t>(sms) * ctas;
     if (grid > slots) grid = slots;
+    // Stream-K tail: when the tiles do not fill the last wave, split the
+    // k-slices of the leftover tiles over every CTA of a resident grid.
+    const int64_t KT = (K + v->bk - 1) / v->bk;
+    if (v->streamk && getenv("SGEMM_NO_STREAMK") == nullptr && p->tiles > slots && p->tiles % slots != 0 &&
+        KT >= 8) {
+      grid = slots;
+      p->dp_waves = static_cast<int>(p->tiles / slots);
+      p->sk_iters = (p->tiles % slots) * KT;
+      const size_t ws_bytes = static_cast<size_t>(slots) * v->bm * v->bn * sizeof(float);
+      void* ws = nullptr;
+      void* flags = nullptr;
+      if (cudaMalloc(&ws, ws_bytes) != cudaSuccess) {
+        delete p;
+        return SGEMM_ERR_CUDA;
+      }
+      if (cudaMalloc(&flags, static_cast<size_t>(slots) * sizeof(unsigned int)) != cudaSuccess ||
+          cudaMemset(flags, 0, static_cast<size_t>(slots) * sizeof(unsigned int)) != cudaSuccess) {
+        cudaFree(ws);
+        if (flags) cudaFree(flags);
+        delete p;
+        return SGEMM_ERR_CUDA;
+      }
+      p->ws = static_cast<float*>(ws);
+      p->flags = static_cast<unsigned int*>(flags);
+    }
   } else if (v->kind == kKindSkinny) {
     // Persistent clusters of S CTAs (S <= 8, the portable cluster size)
     // split K; each cluster walks column slabs.  Pick S and the cluster
@@ -329,6 +366,14 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   a.beta = beta;
   a.grid = grid;
   a.split_k = v->kind == kKindSkinny ? p->split : 1;
+  if (v == reg.all[p->config_id] && p->sk_iters > 0) {
+    a.dp_waves = p->dp_waves;
+    a.sk_iters = p->sk_iters;
+    a.ws = p->ws;
+    a.flags = p->flags;
+    // each run publishes under a new epoch, so flags need no reset
+    a.epoch = const_cast<sgemm_plan_s*>(p)->epoch.fetch_add(1u) + 1u;
+  }
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   sgemm_status_t st = status_addr(device, &a.status);
   if (st != SGEMM_OK) return st;
@@ -371,8 +416,12 @@ sgemm_status_t sgemm_run_host(sgemm_plan_t plan, float alpha, const float* hA, c
 }
 
 sgemm_status_t sgemm_plan_destroy(sgemm_plan_t plan) {
+  if (!plan) return SGEMM_OK;
+  sgemm_status_t st = SGEMM_OK;
+  if (plan->ws && cudaFree(plan->ws) != cudaSuccess) st = SGEMM_ERR_CUDA;
+  if (plan->flags && cudaFree(plan->flags) != cudaSuccess) st = SGEMM_ERR_CUDA;
   delete plan;
-  return SGEMM_OK;
+  return st;
 }
 
 sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
@@ -380,10 +429,12 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
   const Variant* v = registry().all[plan->config_id];
   snprintf(buf, n,
            "variant=%s kind=%s tile=%dx%dx%d stages=%d ffma2=%d threads=%d smem=%d grid=%d ctas_per_sm=%d "
-           "tiles=%lld sms=%d split=%d k_order=%s M=%lld N=%lld K=%lld",
+           "tiles=%lld sms=%d split=%d streamk=%d dp_waves=%d sk_tiles=%lld k_order=%s M=%lld N=%lld K=%lld",
            v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : "skinny", v->bm, v->bn,
            v->bk, v->stages, v->ffma2, v->threads, v->smem_bytes, plan->grid, plan->ctas_per_sm,
-           static_cast<long long>(plan->tiles), plan->num_sms, plan->split, (plan->split > 1 || v->kind == kKindSkinny) ? "split" : "sequential",
+           static_cast<long long>(plan->tiles), plan->num_sms, plan->split, plan->sk_iters > 0 ? 1 : 0, plan->dp_waves,
+           static_cast<long long>(plan->sk_iters > 0 ? plan->tiles - static_cast<int64_t>(plan->dp_waves) * plan->grid : 0),
+           (plan->split > 1 || v->kind == kKindSkinny || plan->sk_iters > 0) ? "split" : "sequential",
            static_cast<long long>(plan->M),
            static_cast<long long>(plan->N), static_cast<long long>(plan->K));
   return SGEMM_OK;

@@ -34,6 +34,15 @@
 //  * Persistent CTAs in grouped tile order, bounded waits with a status
 //    word, epilogue out = alpha*acc (beta == 0, C not read) or
 //    fmaf(alpha, acc, beta*C).
+//  * Stream-K tail (when the tile count is not a multiple of the grid):
+//    full waves of tiles run data-parallel; the k-slices of the remaining
+//    tiles are split evenly over all CTAs, partial tiles go through a
+//    per-CTA workspace slot and a release/acquire flag, and the CTA that
+//    owns a tile's last slice adds them to its own in CTA order (so results
+//    are reproducible, though not the single ascending-k chain).  This
+//    removes the idle SMs of the last partial wave ("Writing a Fast Matmul
+//    in CUDA", "Size effects": a partial last wave; split-K as the remedy
+//    in "What cuBLAS and CUTLASS add").
 #pragma once
 
 #include <cuda.h>
@@ -56,7 +65,23 @@ struct Params {
   int group_m;
   unsigned int* status;
   uint64_t timeout_ns;
+  // stream-K tail (sk_iters == 0: every tile data-parallel)
+  int dp_waves;          // tiles [0, dp_waves*grid) are data-parallel, tile b + i*grid for CTA b
+  int64_t sk_iters;      // k-slices of tiles [dp_waves*grid, tiles), split evenly over the CTAs
+  float* ws;             // one partial tile per CTA
+  unsigned int* flags;   // flags[b] == epoch: CTA b's partial tile is published
+  unsigned int epoch;
 };
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 template <int BM_, int BN, int STAGES>
 struct Shape {
@@ -99,24 +124,81 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   const int tiles_n = (p.N + BN - 1) / BN;
   const int num_tiles = tiles_m * tiles_n;
   const int KT = (p.K + BK - 1) / BK;
-  const int my_tiles = static_cast<int>(blockIdx.x) < num_tiles
-                           ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                           : 0;
-  const uint32_t total_it = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(KT);
+  // ---- this CTA's schedule: up to two stream-K segments first, then data-parallel tiles ----
+  // Stream-K: the k-slices of the tail tiles are numbered x = 0 .. sk_iters-1
+  // (tile-major) and CTA b takes x in [b*I/G, (b+1)*I/G).  Fewer tail tiles
+  // than CTAs means a range spans at most two tiles: the head of the later
+  // one (this CTA is a contributor: it publishes a partial tile) and the
+  // tail of the earlier one (this CTA owns the tile's last slice: it waits
+  // for the contributors, adds their partials in CTA order, and writes C).
+  // The contributor segment runs first, so nobody waits on a CTA that is
+  // itself waiting.
+  const int G = static_cast<int>(gridDim.x);
+  const int b = static_cast<int>(blockIdx.x);
+  const int sk_tile0 = p.sk_iters > 0 ? p.dp_waves * G : num_tiles;
+  int n_sk = 0;
+  int sk_tile_a = 0, sk_k0_a = 0, sk_k1_a = 0;  // first stream-K segment
+  int sk_tile_b = 0, sk_k0_b = 0, sk_k1_b = 0;  // second
+  if (p.sk_iters > 0) {
+    const int64_t s0 = (static_cast<int64_t>(b) * p.sk_iters) / G;
+    const int64_t e0 = (static_cast<int64_t>(b + 1) * p.sk_iters) / G;
+    if (s0 < e0) {
+      const int t_first = static_cast<int>(s0 / KT);
+      const int t_last = static_cast<int>((e0 - 1) / KT);
+      if (t_last != t_first) {  // head of t_last (contributor) first, then tail of t_first
+        sk_tile_a = sk_tile0 + t_last;
+        sk_k0_a = 0;
+        sk_k1_a = static_cast<int>(e0 - static_cast<int64_t>(t_last) * KT);
+        sk_tile_b = sk_tile0 + t_first;
+        sk_k0_b = static_cast<int>(s0 - static_cast<int64_t>(t_first) * KT);
+        sk_k1_b = KT;
+        n_sk = 2;
+      } else {
+        sk_tile_a = sk_tile0 + t_first;
+        sk_k0_a = static_cast<int>(s0 - static_cast<int64_t>(t_first) * KT);
+        sk_k1_a = static_cast<int>(e0 - static_cast<int64_t>(t_first) * KT);
+        n_sk = 1;
+      }
+    }
+  }
+  const int dp_count = p.sk_iters > 0 ? p.dp_waves
+                                      : (b < num_tiles ? (num_tiles - 1 - b) / G + 1 : 0);
+  const int nseg = n_sk + dp_count;
+  auto segment = [&](int i, int& tile, int& k0, int& k1) {
+    if (i == 0 && n_sk > 0) {
+      tile = sk_tile_a;
+      k0 = sk_k0_a;
+      k1 = sk_k1_a;
+    } else if (i == 1 && n_sk > 1) {
+      tile = sk_tile_b;
+      k0 = sk_k0_b;
+      k1 = sk_k1_b;
+    } else {
+      tile = b + (i - n_sk) * G;
+      k0 = 0;
+      k1 = KT;
+    }
+  };
+  uint32_t total_it = static_cast<uint32_t>(dp_count) * static_cast<uint32_t>(KT);
+  if (n_sk > 0) total_it += static_cast<uint32_t>(sk_k1_a - sk_k0_a);
+  if (n_sk > 1) total_it += static_cast<uint32_t>(sk_k1_b - sk_k0_b);
 
-  // producer cursor (thread 0): slices are issued in order
-  int c_lt = 0, c_kt = 0, c_tm = 0, c_tn = 0;
+  // producer cursor (thread 0): slices are issued in schedule order
+  int c_seg = 0, c_kt = 0, c_k1 = 0, c_tm = 0, c_tn = 0;
   auto issue = [&](uint32_t j) {
+    (void)j;
+    if (c_kt == c_k1) {  // enter the next segment
+      int tile, k0;
+      segment(c_seg++, tile, k0, c_k1);
+      c_kt = k0;
+      tile_coords(tile, tiles_m, tiles_n, p.group_m, c_tm, c_tn);
+    }
     const uint32_t s = j % STAGES;
-    if (c_kt == 0) tile_coords(blockIdx.x + c_lt * gridDim.x, tiles_m, tiles_n, p.group_m, c_tm, c_tn);
     const uint32_t dst = smem_base + s * S::kStageBytes;
     ptx::mbar_arrive_expect_tx(bar_full + 8 * s, S::kStageBytes);
     ptx::tma_load_2d(dst, &tmA, c_kt * BK, c_tm * BM, bar_full + 8 * s);
     ptx::tma_load_2d(dst + S::kStageA, &tmB, c_tn * BN, c_kt * BK, bar_full + 8 * s);
-    if (++c_kt == KT) {
-      c_kt = 0;
-      ++c_lt;
-    }
+    ++c_kt;
   };
 
   if (threadIdx.x == 0) {
@@ -168,7 +250,9 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   failed = __syncthreads_or(total_it > 0 && !transpose(0)) != 0;
 
   uint32_t it = 0;
-  for (int tile = blockIdx.x; tile < num_tiles && !failed; tile += gridDim.x) {
+  for (int seg = 0; seg < nseg && !failed; ++seg) {
+    int tile, seg_k0, seg_k1;
+    segment(seg, tile, seg_k0, seg_k1);
     int tm, tn;
     tile_coords(tile, tiles_m, tiles_n, p.group_m, tm, tn);
 
@@ -179,7 +263,7 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
-    for (int kt = 0; kt < KT; ++kt, ++it) {
+    for (int kt = seg_k0; kt < seg_k1; ++kt, ++it) {
       // the next slice's A, transposed ahead (its buffer was last read one slice ago)
       const bool bad = it + 1 < total_it && !transpose(it + 1);
       const uint32_t s = it % STAGES;
@@ -210,6 +294,55 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
       }
     }
     if (failed) break;
+
+    // ---------------- stream-K: publish, or gather the partial tiles ----------------
+    constexpr int kQ = 16;  // float4s per thread: acc[4][8] float2 = 64 floats
+    float4* ws4 = reinterpret_cast<float4*>(p.ws);
+    if (seg_k1 < KT) {  // contributor: partial tile to this CTA's slot, then the flag
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const int i = q >> 2, j2 = 2 * (q & 3);
+        ws4[(static_cast<int64_t>(b) * kQ + q) * S::kThreads + threadIdx.x] =
+            make_float4(acc[i][j2].x, acc[i][j2].y, acc[i][j2 + 1].x, acc[i][j2 + 1].y);
+      }
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) st_release_gpu(p.flags + b, p.epoch);
+      continue;
+    }
+    if (seg_k0 > 0) {  // finisher of a shared tile: wait for the contributors, add them in CTA order
+      const int64_t x0 = static_cast<int64_t>(tile - sk_tile0) * KT;  // first slice of this tile
+      const int c_first = static_cast<int>(((x0 + 1) * G - 1) / p.sk_iters);
+      bool timed_out = false;
+      if (threadIdx.x == 0) {
+        for (int c = c_first; c < b && !timed_out; ++c) {
+          if (ld_acquire_gpu(p.flags + c) == p.epoch) continue;
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (ld_acquire_gpu(p.flags + c) != p.epoch) {
+            if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+              atomicOr(p.status, kStatusTimeoutFull);
+              timed_out = true;
+              break;
+            }
+          }
+        }
+      }
+      failed = __syncthreads_or(timed_out) != 0;
+      if (failed) break;
+      // own slices (the tile's last) first, then the contributors' in CTA order
+#pragma unroll 1
+      for (int c = c_first; c < b; ++c) {
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+          const int i = q >> 2, j2 = 2 * (q & 3);
+          const float4 v = __ldcg(&ws4[(static_cast<int64_t>(c) * kQ + q) * S::kThreads + threadIdx.x]);
+          acc[i][j2].x += v.x;
+          acc[i][j2].y += v.y;
+          acc[i][j2 + 1].x += v.z;
+          acc[i][j2 + 1].y += v.w;
+        }
+      }
+    }
 
     // ---------------- epilogue ----------------
 #pragma unroll
@@ -274,12 +407,17 @@ struct Variant_ {
     p.group_m = 8;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
+    p.dp_waves = a.dp_waves;
+    p.sk_iters = a.sk_iters;
+    p.ws = a.ws;
+    p.flags = a.flags;
+    p.epoch = a.epoch;
     kernel<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
     return cudaGetLastError();
   }
   static Variant describe(const char* name) {
     return Variant{name, kKindTma, S::BM, BN, S::BK, STAGES, 1, S::kThreads, S::kSmemBytes, 128,
-                   &prepare, &occupancy, &launch};
+                   &prepare, &occupancy, &launch, 0, 1};
   }
 };
 

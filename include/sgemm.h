@@ -32,8 +32,13 @@
  * enqueues work on `stream` (a cudaStream_t; NULL is the legacy default
  * stream) and returns; results are ready when the stream reaches that point.
  * A plan is immutable after sgemm_plan returns and may be used from several
- * host threads and streams at once.  No entry point allocates device
- * memory inside sgemm_run.
+ * host threads.  No entry point allocates device memory inside sgemm_run.
+ * A plan whose description says streamk=1 owns a device workspace (one
+ * partial tile and one flag per CTA of its grid), allocated by sgemm_plan
+ * and freed by sgemm_plan_destroy; two runs of such a plan must not overlap
+ * in time (same stream, or streams ordered by events), since both would
+ * write the same workspace.  Every other plan may run on several streams
+ * at once.
  *
  * Errors: every entry point returns a status and never aborts.  Launch
  * failures map to SGEMM_ERR_CUDA.  Faults during execution surface at the
@@ -66,7 +71,12 @@ typedef enum {
 /*
  * Make a plan for one problem shape on the current device: validates the
  * dimensions, picks a kernel variant from the per-shape config table
- * (measured on GB300) and prepares it.  Allocates only host memory.
+ * (measured on GB300) and prepares it.  Allocates host memory, plus a
+ * device workspace of grid * tile_m * tile_n floats and grid flags
+ * (cudaMalloc) when the choice splits the last, partial wave of tiles
+ * along K across the whole grid (stream-K; describe reports streamk=1).
+ * That workspace makes the sum order along K for the tail tiles a fixed
+ * split: results stay bit-identical from run to run.
  * The environment variable SGEMM_FORCE_CONFIG=<variant name> overrides the
  * table choice.  *out is set only on SGEMM_OK.
  */
@@ -102,7 +112,8 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float *A, const f
 sgemm_status_t sgemm_run_host(sgemm_plan_t plan, float alpha, const float *hA, const float *hB,
                               float beta, float *hC, float *dA, float *dB, float *dC, void *stream);
 
-/* Free a plan (host memory only).  NULL is accepted. */
+/* Free a plan and its device workspace, if any (the device that was
+ * current at sgemm_plan must be current here).  NULL is accepted. */
 sgemm_status_t sgemm_plan_destroy(sgemm_plan_t plan);
 
 /*

@@ -378,3 +378,37 @@ def test_transposed_a_variants_take_any_lda(sg, oracle_mod):
             C, used = run_gpu(sg, A, B, C0, 0.5, 3.0, config=name, lda=lda, off_a=off_a)
             assert used == name
             assert_parity(C, Cref, S, K, f"{name} lda={lda} off_a={off_a}")
+
+
+@pytest.mark.parametrize("shape", [(2048, 2048, 1024), (1500, 3000, 780), (2560, 1408, 256)])
+def test_stream_k_tail(sg, oracle_mod, shape):
+    """Tile counts that overshoot the resident grid: full waves run
+    data-parallel and the leftover tiles are split along K across all CTAs
+    (partials through a workspace, added in CTA order)."""
+    M, N, K = shape
+    A, B, C0 = make_inputs(M, N, K, seed=M + 3 * N + K, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    names = [n for n in sg.config_names() if n.startswith("tmat")]
+    saw_streamk = False
+    for name in names:
+        plan = sg.Plan(M, N, K, config=name)
+        info = plan.info()
+        outs = []
+        for _ in range(3):  # three runs: three epochs on the same flags
+            dC = torch.from_numpy(C0).cuda()
+            plan.run(0.5, dA, dB, 3.0, dC)
+            torch.cuda.synchronize()
+            assert sg.device_status() == sg.SGEMM_OK
+            outs.append(dC.cpu().numpy())
+        plan.close()
+        assert all(np.array_equal(outs[0], o) for o in outs[1:]), f"{name}: runs differ"
+        if info["streamk"]:
+            saw_streamk = True
+            assert info["k_order"] == "split"
+        rows, cols = sample_rows_cols(M, N, n_rows=192, n_cols=192, seed=7)
+        Cs = outs[0][np.ix_(rows, cols)]
+        Cref, S = oracle_mod.sgemm_ref(np.ascontiguousarray(A[rows]), np.ascontiguousarray(B[:, cols]),
+                                       np.ascontiguousarray(C0[np.ix_(rows, cols)]), 0.5, 3.0)
+        assert_parity(Cs, Cref, S, K, f"{name} {shape} streamk={info['streamk']} dp_waves={info['dp_waves']}")
+    assert saw_streamk, "no variant split its tail for these shapes"
