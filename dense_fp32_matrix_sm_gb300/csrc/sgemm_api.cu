@@ -140,16 +140,23 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
 // The per-shape config table.  Keys are shape classes; values are variant
 // names.  The entries come from the measured sweeps on GB300.
 const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms) {
-  (void)K;
   if (ldb % 4 != 0) return "generic_64x64x16";
   if (M <= 16 && lda % 4 == 0) return "skinny_16x128x32_w4_s3_b3_ef_pa";
   if (lda % 4 != 0) return "cpa_128x128x32_s3_k8_b2";  // A copied 4 bytes at a time: any lda
   if (M * N <= 256 * 256) return "tma_128x64x32_w64x32_s3_quad_b3";
-  // 128 x 256 tiles when there are enough of them to fill every SM about
-  // ten times over (tile-count rounding then costs little); else 128 x 128
+  // Measured on GB300 with the stream-K tail (which removes most of the
+  // partial-wave loss once there is at least one full wave):
+  //  * 128 x 256 tiles from one full wave of them on, with K >= 256 (eight
+  //    or more k-slices per tile, the stream-K threshold): 63.7-66.6 TFLOP/s
+  //    from 2560^3 up, 2-4% above 128 x 128;
+  //  * 128 x 128 tiles down to three quarters of a wave (1536^3: 56.5 vs
+  //    54.4 for 128 x 64);
+  //  * below that, 128 x 64 tiles two to an SM (1024^3: 36.1 vs 24.4).
   const int64_t wide_tiles = ((M + 127) / 128) * ((N + 255) / 256);
-  if (wide_tiles >= 10 * static_cast<int64_t>(num_sms)) return "tmat_128x256x32_s3_b1";
-  return "tmat_128x128x32_s4_b1";
+  const int64_t square_tiles = ((M + 127) / 128) * ((N + 127) / 128);
+  if (wide_tiles >= num_sms && K >= 256) return "tmat_128x256x32_s3_b1";
+  if (4 * square_tiles >= 3 * static_cast<int64_t>(num_sms)) return "tmat_128x128x32_s4_b1";
+  return "tmat_128x64x32_s3_b2";
 }
 
 sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int config_id,
