@@ -42,6 +42,7 @@ SIGNATURES = {
     "sgemm_device_status": (_int, [_int]),
     "sgemm_set_wait_timeout_ns": (_int, [ctypes.c_uint64]),
     "sgemm_selftest_wait_timeout": (_int, [ctypes.c_uint64, _vp]),
+    "sgemm_run_static_scratch": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
 }
 
 _lib = None
@@ -259,3 +260,16 @@ def sgemm(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, stream=None, conf
     finally:
         plan.close()
     return C
+
+
+def run_static_scratch(M: int, N: int, K: int, alpha: float, A, B, beta: float, C, lda: Optional[int] = None,
+                       ldb: Optional[int] = None, ldc: Optional[int] = None, stream=None) -> None:
+    """Enqueue C = alpha*A*B + beta*C through sgemm_run_static_scratch: no plan and no allocation.
+    The scratch is shared per device, so calls must not overlap in time.
+    A, B, C: CUDA tensors or raw device addresses; ld* default to dense rows."""
+    M, N, K = int(M), int(N), int(K)
+    lda = int(lda) if lda is not None else max(1, K)
+    ldb = int(ldb) if ldb is not None else max(1, N)
+    ldc = int(ldc) if ldc is not None else max(1, N)
+    _check(lib().sgemm_run_static_scratch(M, N, K, lda, ldb, ldc, float(alpha), _ptr(A), _ptr(B), float(beta),
+                                          _ptr(C), _stream_handle(stream)), "sgemm_run_static_scratch")

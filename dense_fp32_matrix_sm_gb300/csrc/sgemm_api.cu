@@ -14,6 +14,7 @@
 #include <new>
 #include <vector>
 
+#include "api_internal.h"
 #include "kernels.h"
 #include "sgemm.h"
 
@@ -516,3 +517,34 @@ sgemm_status_t sgemm_selftest_wait_timeout(uint64_t timeout_ns, void* stream_) {
 }
 
 }  // extern "C"
+
+// ---- helpers shared with the static-scratch entry point (api_internal.h) ----
+namespace sgemm {
+
+sgemm_status_t api_check_dims(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc) {
+  return check_dims(M, N, K, lda, ldb, ldc);
+}
+
+const Variant* api_find_variant(const char* name) {
+  const int id = find_variant(name);
+  return id < 0 ? nullptr : registry().all[id];
+}
+
+sgemm_status_t api_status_word(int device, unsigned int** out) { return status_addr(device, out); }
+
+bool api_encoder_ready() { return encode_fn() != nullptr; }
+
+sgemm_status_t api_encode_maps(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                               const float* A, const float* B, LaunchArgs* a) {
+  sgemm_plan_s shape;  // only the shape fields are read
+  shape.M = M;
+  shape.N = N;
+  shape.K = K;
+  shape.lda = lda;
+  shape.ldb = ldb;
+  return encode_maps(v, &shape, A, B, a);
+}
+
+uint64_t api_wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+
+}  // namespace sgemm

@@ -156,6 +156,77 @@ sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns);
  */
 sgemm_status_t sgemm_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
 
+/*
+ * Size of the static scratch used by sgemm_run_static_scratch: one
+ * 128 x 256 float32 partial tile for each of at most
+ * SGEMM_STATIC_SCRATCH_MAX_CTAS CTAs (19,922,944 bytes), then one 32-bit
+ * flag per CTA padded to 768 bytes: 19,923,712 bytes (19.0 MiB) in all,
+ * reserved in device memory for each device whose context loads it.
+ */
+#define SGEMM_STATIC_SCRATCH_MAX_CTAS 152
+#define SGEMM_STATIC_SCRATCH_BYTES ((size_t)SGEMM_STATIC_SCRATCH_MAX_CTAS * 128 * 256 * 4 + 768)
+
+/*
+ * C = alpha*A*B + beta*C with no plan and no memory allocation: the
+ * 128 x 256 transposed-A kernel with its stream-K tail.  The pages have no
+ * counterpart to this entry point.  They describe the kernels, not how a
+ * library hands them workspace; it exists for deployment.
+ *
+ * Who cannot allocate, and why:
+ *   - a caller inside a framework whose caching allocator already holds the
+ *     device's memory (PyTorch's, for one).  cudaMalloc can then fail even
+ *     though the framework has free blocks, and memory taken outside the
+ *     pool is not given back to it.
+ *   - a caller on a latency-bound path.  cudaFree waits for the whole
+ *     device, and cudaMalloc can take far longer than a GEMM.
+ *   - a caller with nowhere to keep a plan, such as a hook called per batch
+ *     with no set-up or tear-down of its own.  Making and destroying a
+ *     stream-K plan on every call would allocate and free each time.
+ *
+ * Arguments are sgemm_plan's dimensions and leading dimensions followed by
+ * sgemm_run's arguments, with the same meaning, layout and ownership; A, B,
+ * C are device pointers on the current device.  Enqueues on `stream` and
+ * returns.  Results are bit-identical to sgemm_run of a plan made with the
+ * variant "tmat_128x256x32_s3_b1" (k_order=split when the tail is split).
+ *
+ * Scratch: the stream-K workspace and its flags sit in one file-scope
+ * __device__ array of SGEMM_STATIC_SCRATCH_BYTES (see above).  Only the
+ * flags must start at zero: the first call on each device clears them,
+ * and they are cleared again when the call counter wraps.  A partial tile
+ * is always written before its flag is raised, so the workspace needs no
+ * clearing.
+ *
+ * First-call set-up, once per device, with that device current:
+ *   - looks up the array's device address (cudaGetSymbolAddress, which
+ *     loads the module holding it);
+ *   - sets the kernel's shared-memory limit and reads its occupancy;
+ *   - clears the flags with cudaMemsetAsync on `stream`.
+ * Make that first call before any stream capture.  After set-up a call
+ * makes no allocation, host or device.
+ *
+ * Concurrency: every call on a device shares that device's scratch.  Calls
+ * that overlap in time race and give wrong results or SGEMM_ERR_TIMEOUT in
+ * the status word.  This holds for calls on two streams not ordered by
+ * events, and for calls from two host threads at once.  Serialise them:
+ * one stream, or event ordering.
+ *
+ * Errors:
+ *   - SGEMM_ERR_INVALID_ARG and the dimension rules are as for sgemm_plan
+ *     and sgemm_run.
+ *   - SGEMM_ERR_UNSUPPORTED when this kernel cannot take the layout: lda or
+ *     ldb not a multiple of 4, or A or B not 16-byte aligned.  These need
+ *     sgemm_plan and sgemm_run.
+ *   - SGEMM_ERR_UNSUPPORTED also when the call would need more scratch than
+ *     the array holds: a stream-K grid of more than
+ *     SGEMM_STATIC_SCRATCH_MAX_CTAS CTAs, on a device with more SMs than
+ *     GB300's 152.  On GB300 every shape fits.
+ * M == 0 or N == 0 launches nothing.  K == 0 or alpha == 0 scales C by
+ * beta and uses no scratch.
+ */
+sgemm_status_t sgemm_run_static_scratch(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                        int64_t ldc, float alpha, const float *A, const float *B,
+                                        float beta, float *C, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,6 +70,21 @@ def test_invalid_arguments_rejected_without_gpu(lib):
     assert lib.sgemm_plan_destroy(None) == 0
 
 
+def test_static_scratch_rejects_before_cuda(lib):
+    """sgemm_run_static_scratch checks its arguments before any CUDA call."""
+    f = lib.sgemm_run_static_scratch
+    dummy = 4096  # never dereferenced: every case returns before a launch
+    assert f(-1, 4, 4, 4, 4, 4, 1.0, dummy, dummy, 0.0, dummy, None) == -1   # negative M
+    assert f(4, 8, 8, 7, 8, 8, 1.0, dummy, dummy, 0.0, dummy, None) == -1    # lda < K
+    assert f(4, 8, 8, 8, 8, 8, 1.0, dummy, dummy, 0.0, None, None) == -1     # C missing
+    assert f(4, 8, 8, 8, 8, 8, 1.0, None, dummy, 0.0, dummy, None) == -1     # A missing with a product
+    assert f(0, 8, 8, 8, 8, 8, 1.0, None, None, 0.0, None, None) == 0        # M == 0: nothing to do
+    assert f(4, 8, 8, 10, 8, 8, 1.0, dummy, dummy, 0.0, dummy, None) == -2   # lda % 4 != 0
+    assert f(4, 8, 8, 8, 10, 8, 1.0, dummy, dummy, 0.0, dummy, None) == -2   # ldb % 4 != 0
+    assert f(4, 8, 8, 8, 8, 8, 1.0, dummy + 4, dummy, 0.0, dummy, None) == -2  # A not 16-byte aligned
+    assert f(2 ** 31, 8, 8, 8, 8, 8, 1.0, dummy, dummy, 0.0, dummy, None) == -2  # M beyond int32
+
+
 def test_status_strings_and_configs(lib):
     import dense_fp32_matrix_sm_gb300 as s
 
