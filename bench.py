@@ -41,6 +41,7 @@ if ROOT not in sys.path:
 METRIC = "FP32 SGEMM GFLOP/s at 4096^3 on 1 GB300; % of FP32 FFMA peak"
 FMA_LANES_PER_SM = 128          # FP32 lanes per SM (4 sub-partitions x 32)
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = ["tma_kernel.cuh", "cpa_kernel.cuh", "tmat_kernel.cuh", "tile_order.cuh", "kernel_skinny.cu", "kernel_generic.cu", "ptx.cuh", "kernels.h"]
 
@@ -356,12 +357,27 @@ def run_ours(args):
                 traffic = rec.get("dram_bytes_per_launch")
         except (ValueError, OSError):
             traffic = None
-    out["roofline"] = {"bound": "alu", "achieved": round(achieved_tflops, 3),
-                       "peak": round(peak_tflops, 3), "unit": "TFLOP/s",
-                       "frac": round(achieved_tflops / peak_tflops, 4), "traffic": traffic,
-                       "peak_basis": "SMs x 128 FP32 lanes x 2 FLOP x median SM clock sampled during the "
-                                     "timed steps (FFMA pipe; not a tensor-core path)",
-                       "algorithmic_bytes": w.algorithmic_bytes()}
+    # The bound follows the workload's arithmetic intensity: below the ridge
+    # (FFMA peak / measured HBM copy bandwidth) the kernel is bound by HBM.
+    hbm_gbs = peaks.get("hbm_gbs") or FALLBACK_HBM_GBS
+    hbm_basis = ("MEASURED_PEAKS.json hbm_gbs, STREAM-style copy, burst (of measured)" if peaks.get("hbm_gbs")
+                 else "fallback 6.8 TB/s (of fallback)")
+    intensity = w.flops / w.algorithmic_bytes()
+    ridge = peak_tflops * 1e12 / (hbm_gbs * 1e9)
+    if intensity < ridge:
+        achieved_gbs = w.algorithmic_bytes() / (ms * 1e-3) / 1e9
+        out["roofline"] = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
+                           "frac": round(achieved_gbs / hbm_gbs, 4), "traffic": traffic, "peak_basis": hbm_basis,
+                           "algorithmic_bytes": w.algorithmic_bytes(),
+                           "intensity_flop_per_byte": round(intensity, 2), "ridge_flop_per_byte": round(ridge, 2)}
+    else:
+        out["roofline"] = {"bound": "alu", "achieved": round(achieved_tflops, 3),
+                           "peak": round(peak_tflops, 3), "unit": "TFLOP/s",
+                           "frac": round(achieved_tflops / peak_tflops, 4), "traffic": traffic,
+                           "peak_basis": "SMs x 128 FP32 lanes x 2 FLOP x median SM clock sampled during the "
+                                         "timed steps (FFMA pipe; not a tensor-core path)",
+                           "algorithmic_bytes": w.algorithmic_bytes(),
+                           "intensity_flop_per_byte": round(intensity, 2), "ridge_flop_per_byte": round(ridge, 2)}
     out["clocks"] = {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "sm_mhz_min",
                                                  "power_w_max", "samples")}
 

@@ -379,8 +379,18 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
     a.sk_iters = p->sk_iters;
     a.ws = p->ws;
     a.flags = p->flags;
-    // each run publishes under a new epoch, so flags need no reset
-    a.epoch = const_cast<sgemm_plan_s*>(p)->epoch.fetch_add(1u) + 1u;
+    // each run publishes under a new epoch, so flags need no reset --
+    // except when the counter wraps: then a flag may hold any earlier
+    // value, so clear them all and start again from 1
+    sgemm_plan_s* mp = const_cast<sgemm_plan_s*>(p);
+    unsigned int e = mp->epoch.fetch_add(1u) + 1u;
+    if (e == 0u) {
+      if (cudaMemsetAsync(p->flags, 0, static_cast<size_t>(p->grid) * sizeof(unsigned int), stream) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+      mp->epoch.store(1u);
+      e = 1u;
+    }
+    a.epoch = e;
   }
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   sgemm_status_t st = status_addr(device, &a.status);

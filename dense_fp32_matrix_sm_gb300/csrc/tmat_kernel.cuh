@@ -3,7 +3,9 @@
 // tmat_variants.cu).
 //
 // C = alpha*A*B + beta*C, row-major float32, single-rounding fp32 FMAs in
-// ascending k for every output (bit-identical to the float32 fma chain).
+// ascending k for every output of a data-parallel tile (bit-identical to
+// the float32 fma chain); tiles of a stream-K tail add fixed-order partial
+// sums instead (see below).
 //
 // The inner loop is the fast paired-FMA form: each FFMA2 multiplies a
 // register PAIR holding two rows of A at one k, (A[m][k], A[m+1][k]), by
