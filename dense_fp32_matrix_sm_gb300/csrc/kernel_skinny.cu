@@ -108,6 +108,41 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
   return v;
 }
 
+// One 32-deep slice in the paired form: this warp's k-quads q = gw, gw + GW,
+// ... of the stage (A at As, B at Bs4 = this lane's float4 column of its
+// group), accumulated into accp[p][j] = {C[2p][4l + j], C[2p + 1][4l + j]}.
+template <int BN, int GW>
+__device__ __forceinline__ void pa_slice(const float* As, const float4* Bs4, float* atw, int gw, int lane,
+                                         float2 (&accp)[kSBM / 2][4]) {
+#pragma unroll
+  for (int qq = 0; qq < (kSBK / 4) / GW; ++qq) {
+    // Transpose this warp's k-quad of A (16 rows x 4 k) into atw[k][m]:
+    // lane takes row l/2, k pair 2*(l%2); rows are 32 floats apart and
+    // k = 2, 3 sit 16 floats further in, so the 32 writes hit 32 banks.
+    const int q = gw + GW * qq;
+    {
+      const int m = lane >> 1, h = lane & 1;
+      const float2 v = *reinterpret_cast<const float2*>(As + m * kSBK + ((q ^ (m & 7)) << 2) + 2 * h);
+      atw[(2 * h) * 32 + 16 * h + m] = v.x;
+      atw[(2 * h + 1) * 32 + 16 * h + m] = v.y;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const float4 b = Bs4[(4 * q + kk) * (BN / 4)];
+      const float bb[4] = {b.x, b.y, b.z, b.w};
+      const float* ak = atw + kk * 32 + 16 * ((kk >> 1) & 1);
+#pragma unroll
+      for (int pp = 0; pp < kSBM / 2; ++pp) {
+        const float2 ap = *reinterpret_cast<const float2*>(ak + 2 * pp);  // rows 2pp, 2pp+1
+#pragma unroll
+        for (int j = 0; j < 4; ++j) accp[pp][j] = __ffma2_rn(ap, make_float2(bb[j], bb[j]), accp[pp][j]);
+      }
+    }
+    __syncwarp();  // the next quad overwrites atw
+  }
+}
+
 template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST, bool PAIRA>
 __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     sgemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -197,33 +232,7 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
               ptx::mbar_test_wait(bar_full + 8 * ((it + 1) % STAGES), ((it + 1) / STAGES) & 1u);
       const float* As = reinterpret_cast<const float*>(smem + s * S::kStageBytes);
       const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + group * 32 + lane;
-#pragma unroll
-      for (int qq = 0; qq < S::kQuadsPerWarp && PAIRA; ++qq) {
-        // Transpose this warp's k-quad of A (16 rows x 4 k) into atw[k][m]:
-        // lane takes row l/2, k pair 2*(l%2); rows are 32 floats apart and
-        // k = 2, 3 sit 16 floats further in, so the 32 writes hit 32 banks.
-        const int q = gw + GW * qq;
-        {
-          const int m = lane >> 1, h = lane & 1;
-          const float2 v = *reinterpret_cast<const float2*>(As + m * kSBK + ((q ^ (m & 7)) << 2) + 2 * h);
-          atw[(2 * h) * 32 + 16 * h + m] = v.x;
-          atw[(2 * h + 1) * 32 + 16 * h + m] = v.y;
-        }
-        __syncwarp();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const float4 b = Bs4[(4 * q + kk) * (BN / 4)];
-          const float bb[4] = {b.x, b.y, b.z, b.w};
-          const float* ak = atw + kk * 32 + 16 * ((kk >> 1) & 1);
-#pragma unroll
-          for (int pp = 0; pp < kSBM / 2; ++pp) {
-            const float2 ap = *reinterpret_cast<const float2*>(ak + 2 * pp);  // rows 2pp, 2pp+1
-#pragma unroll
-            for (int j = 0; j < 4; ++j) accp[pp][j] = __ffma2_rn(ap, make_float2(bb[j], bb[j]), accp[pp][j]);
-          }
-        }
-        __syncwarp();  // the next quad overwrites atw
-      }
+      if constexpr (PAIRA) pa_slice<BN, GW>(As, Bs4, atw, gw, lane, accp);
 #pragma unroll
       for (int qq = 0; qq < S::kQuadsPerWarp && !PAIRA; ++qq) {
         const int q = gw + GW * qq;
@@ -302,6 +311,253 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Stream-K form: one resident wave, no clusters.  The work units are
+// (column slab, 32-deep k-slice) pairs numbered slab-major, U in all; CTA b
+// of G streams units [b*U/G, (b+1)*U/G) through one TMA ring without
+// draining between slabs.  Its range covers the tail of slab s_first, any
+// whole slabs, and the head of slab s_last; it runs the head first.
+//  * a whole slab is written straight to C;
+//  * a head (or a piece inside one slab) is a contributor: its 16 x BN
+//    partial tile goes to workspace slot b, then flags[b] = epoch (release);
+//  * the tail of s_first is the finisher: it waits (acquire, bounded) for
+//    the flags of the CTAs c_first .. b-1 that hold the slab's earlier
+//    slices, adds their partials in CTA order after its own, and writes C.
+// Every contributor piece is its CTA's first piece, so a finisher never
+// waits on a CTA that is itself waiting.  The sum order is fixed (results
+// are reproducible run to run; k_order=split).
+struct SkinnySkParams {
+  float* C;
+  int64_t ldc;
+  int M, N, K;
+  float alpha, beta;
+  unsigned int* status;
+  uint64_t timeout_ns;
+  float* ws;             // kSBM x BN floats per CTA
+  unsigned int* flags;   // one per CTA
+  unsigned int epoch;
+};
+
+template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST>
+__global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
+    sgemm_skinny_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           const SkinnySkParams p) {
+  using S = SkinnyShape<BN, GW, STAGES>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ int s_failed;
+  const uint32_t raw_base = ptx::smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+  const uint32_t smem_base = ptx::smem_addr(smem);
+  float* partial = reinterpret_cast<float*>(smem + S::kRingBytes);  // [16][BN]
+  constexpr int kBarOff = S::kRingBytes + S::kPartialBytes + S::kWarps * S::kAtwBytes;
+  float* atw = reinterpret_cast<float*>(smem + S::kRingBytes + S::kPartialBytes) + (threadIdx.x >> 5) * (S::kAtwBytes / 4);
+  const uint32_t bar_full = smem_base + kBarOff;
+  unsigned int* released = reinterpret_cast<unsigned int*>(smem + kBarOff + STAGES * 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int group = warp / GW;
+  const int gw = warp % GW;
+  const int G = static_cast<int>(gridDim.x);
+  const int b = static_cast<int>(blockIdx.x);
+  const int KT = (p.K + kSBK - 1) / kSBK;
+  const int nslabs = (p.N + BN - 1) / BN;
+  const int64_t U = static_cast<int64_t>(nslabs) * KT;
+  const int64_t s0 = (static_cast<int64_t>(b) * U) / G;
+  const int64_t e0 = (static_cast<int64_t>(b + 1) * U) / G;
+  const uint32_t total_it = static_cast<uint32_t>(e0 - s0);
+  const int s_first = total_it ? static_cast<int>(s0 / KT) : 0;
+  const int s_last = total_it ? static_cast<int>((e0 - 1) / KT) : 0;
+  const int64_t head_begin = static_cast<int64_t>(s_last) * KT;
+  // the head of s_last runs first when the range spans several slabs
+  const uint32_t head_len = s_last > s_first ? static_cast<uint32_t>(e0 - head_begin) : 0u;
+  const int npieces = total_it ? s_last - s_first + 1 : 0;
+
+  auto unit_of = [&](uint32_t j) -> int64_t { return j < head_len ? head_begin + j : s0 + (j - head_len); };
+  auto issue = [&](uint32_t j) {
+    const uint32_t s = j % STAGES;
+    const int64_t u = unit_of(j);
+    const int kt = static_cast<int>(u % KT);
+    const int n0 = static_cast<int>(u / KT) * BN;
+    const uint32_t dst = smem_base + s * S::kStageBytes;
+    ptx::mbar_arrive_expect_tx(bar_full + 8 * s, S::kStageBytes);
+    ptx::tma_load_2d(dst, &tmA, kt * kSBK, 0, bar_full + 8 * s);
+    if constexpr (EVICT_FIRST) {
+      ptx::tma_load_2d_hint(dst + S::kStageA, &tmB, n0, kt * kSBK, bar_full + 8 * s, ptx::l2_policy_evict_first());
+    } else {
+      ptx::tma_load_2d(dst + S::kStageA, &tmB, n0, kt * kSBK, bar_full + 8 * s);
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    s_failed = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(bar_full + 8 * s, 1);
+      released[s] = 0u;
+    }
+    ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB);
+    for (uint32_t j = 0; j < STAGES && j < total_it; ++j) issue(j);
+  }
+  __syncthreads();
+
+  uint32_t it = 0;
+  bool ready = false;
+#pragma unroll 1
+  for (int pc = 0; pc < npieces; ++pc) {
+    int slab, k0, k1;
+    if (head_len > 0 && pc == 0) {
+      slab = s_last;
+      k0 = 0;
+      k1 = static_cast<int>(head_len);
+    } else {
+      slab = s_first + (head_len > 0 ? pc - 1 : pc);
+      const int64_t lo = static_cast<int64_t>(slab) * KT;
+      k0 = static_cast<int>((s0 > lo ? s0 : lo) - lo);
+      k1 = static_cast<int>((e0 < lo + KT ? e0 : lo + KT) - lo);
+    }
+    const int n0 = slab * BN;
+    float2 accp[kSBM / 2][4];
+#pragma unroll
+    for (int q = 0; q < kSBM / 2; ++q)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) accp[q][j] = make_float2(0.f, 0.f);
+
+#pragma unroll 1
+    for (int kt = k0; kt < k1; ++kt, ++it) {
+      if (*reinterpret_cast<volatile int*>(&s_failed)) continue;
+      const uint32_t s = it % STAGES;
+      if (!ready && !ptx::mbar_wait(bar_full + 8 * s, (it / STAGES) & 1u, p.timeout_ns)) {
+        atomicOr(p.status, kStatusTimeoutFull);
+        *reinterpret_cast<volatile int*>(&s_failed) = 1;
+        continue;
+      }
+      ready = it + 1 < total_it &&
+              ptx::mbar_test_wait(bar_full + 8 * ((it + 1) % STAGES), ((it + 1) / STAGES) & 1u);
+      const float* As = reinterpret_cast<const float*>(smem + s * S::kStageBytes);
+      const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + group * 32 + lane;
+      pa_slice<BN, GW>(As, Bs4, atw, gw, lane, accp);
+      __syncwarp();
+      if (lane == 0) {
+        const unsigned int before = ptx::atom_add_acq_rel_cta(&released[s], 1u);
+        if ((before + 1u) % S::kWarps == 0u && it + STAGES < total_it) {
+          ptx::fence_proxy_async_smem();
+          issue(it + STAGES);
+        }
+      }
+    }
+
+    // this piece's GW warp partials into `partial`, in warp order
+#pragma unroll 1
+    for (int w = 0; w < GW; ++w) {
+      if (gw == w) {
+        float4* part4 = reinterpret_cast<float4*>(partial);
+#pragma unroll
+        for (int m = 0; m < kSBM; ++m) {
+          const int pp = m >> 1;
+          const float4 v = (m & 1) ? make_float4(accp[pp][0].y, accp[pp][1].y, accp[pp][2].y, accp[pp][3].y)
+                                   : make_float4(accp[pp][0].x, accp[pp][1].x, accp[pp][2].x, accp[pp][3].x);
+          float4* d = part4 + m * (BN / 4) + group * 32 + lane;
+          if (w == 0) {
+            *d = v;
+          } else {
+            const float4 o = *d;
+            *d = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+          }
+        }
+      }
+      __syncthreads();
+    }
+
+    constexpr int kTile4 = kSBM * BN / 4;  // float4s in a partial tile
+    const float4* part4 = reinterpret_cast<const float4*>(partial);
+    float4* ws4 = reinterpret_cast<float4*>(p.ws);
+    if (k1 < KT) {  // contributor: partial tile to slot b, then the flag
+      for (int i = threadIdx.x; i < kTile4; i += S::kThreads) ws4[static_cast<int64_t>(b) * kTile4 + i] = part4[i];
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) ptx::st_release_gpu(p.flags + b, p.epoch);
+      continue;
+    }
+    int c_first = b;
+    if (k0 > 0) {  // finisher: wait for the CTAs holding this slab's earlier slices
+      const int64_t x0 = static_cast<int64_t>(slab) * KT;
+      c_first = static_cast<int>(((x0 + 1) * G - 1) / U);
+      bool timed_out = false;
+      if (threadIdx.x == 0) {
+        for (int c = c_first; c < b && !timed_out; ++c) {
+          if (ptx::ld_acquire_gpu(p.flags + c) == p.epoch) continue;
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (ptx::ld_acquire_gpu(p.flags + c) != p.epoch) {
+            if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+              atomicOr(p.status, kStatusTimeoutFull);
+              timed_out = true;
+              break;
+            }
+          }
+        }
+      }
+      if (__syncthreads_or(timed_out)) c_first = b;  // give up on the partials; the status word says why
+    }
+    // own partial, then the contributors' in CTA order; then the epilogue
+    for (int i = threadIdx.x; i < kTile4; i += S::kThreads) {
+      float4 v = part4[i];
+      for (int c = c_first; c < b; ++c) {
+        const float4 o = __ldcg(&ws4[static_cast<int64_t>(c) * kTile4 + i]);
+        v.x += o.x;
+        v.y += o.y;
+        v.z += o.z;
+        v.w += o.w;
+      }
+      const int m = (4 * i) / BN;
+      const int n = n0 + (4 * i) % BN;
+      if (m < p.M) {
+        float* crow = p.C + static_cast<int64_t>(m) * p.ldc;
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (n + j < p.N) crow[n + j] = p.beta == 0.f ? p.alpha * vv[j] : fmaf(p.alpha, vv[j], p.beta * crow[n + j]);
+        }
+      }
+    }
+    __syncthreads();  // the next piece rewrites `partial`
+  }
+}
+
+template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST>
+struct SkinnySkVariant {
+  using S = SkinnyShape<BN, GW, STAGES>;
+  static constexpr auto kernel = sgemm_skinny_sk_kernel<BN, GW, STAGES, MINB, EVICT_FIRST>;
+  static cudaError_t prepare() {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  }
+  static cudaError_t occupancy(int* ctas) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kernel, S::kThreads, S::kSmemBytes);
+  }
+  static cudaError_t launch(const LaunchArgs& a, cudaStream_t stream) {
+    SkinnySkParams p;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    p.ws = a.ws;
+    p.flags = a.flags;
+    p.epoch = a.epoch;
+    kernel<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    return cudaGetLastError();
+  }
+  static Variant describe(const char* name) {
+    return Variant{name, kKindSkinny, kSBM, BN, kSBK, STAGES, 1, S::kThreads, S::kSmemBytes, 128, &prepare, &occupancy,
+                   &launch, 0, 1};
+  }
+};
+
 template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST, bool PAIRA = false, int PERSIST = 0>
 struct SkinnyVariant {
   using S = SkinnyShape<BN, GW, STAGES>;
@@ -346,6 +602,9 @@ struct SkinnyVariant {
 
 const Variant kSkinnyVariants[] = {
     SkinnyVariant<128, 4, 3, 3, true, true>::describe("skinny_16x128x32_w4_s3_b3_ef_pa"),
+    SkinnySkVariant<128, 4, 3, 3, true>::describe("skinny_sk_16x128x32_w4_s3_b3_ef"),
+    SkinnySkVariant<128, 4, 4, 3, true>::describe("skinny_sk_16x128x32_w4_s4_b3_ef"),
+    SkinnySkVariant<128, 4, 3, 3, false>::describe("skinny_sk_16x128x32_w4_s3_b3"),
     SkinnyVariant<128, 4, 3, 3, true, false>::describe("skinny_16x128x32_w4_s3_b3_ef"),
     SkinnyVariant<128, 4, 3, 3, true, true, 1>::describe("skinny_16x128x32_w4_s3_b3_ef_pa_persist"),
     SkinnyVariant<128, 4, 3, 3, false, true>::describe("skinny_16x128x32_w4_s3_b3_pa"),

@@ -142,7 +142,18 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
 // names.  The entries come from the measured sweeps on GB300.
 const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms) {
   if (ldb % 4 != 0) return "generic_64x64x16";
-  if (M <= 16 && lda % 4 == 0) return "skinny_16x128x32_w4_s3_b3_ef_pa";
+  if (M <= 16 && lda % 4 == 0) {
+    // Few rows: the stream-K form once there are enough (128-column slab,
+    // 32-deep k-slice) units to keep one resident wave streaming and enough
+    // slabs that each finisher adds only a few partial tiles.  Measured:
+    // 16 x 16384 x 8192 0.109 ms against 0.124 for the cluster form;
+    // 16 x 8192 x 4096 0.044 against 0.047; but 16 x 4096 x 8192 (32 slabs)
+    // 0.046 against 0.039 and 16 x 4096 x 4096 0.036 against 0.026.
+    const int64_t slabs = (N + 127) / 128;
+    const int64_t units = slabs * ((K + 31) / 32);
+    return slabs >= 64 && units >= 48 * static_cast<int64_t>(num_sms) ? "skinny_sk_16x128x32_w4_s3_b3_ef"
+                                                                       : "skinny_16x128x32_w4_s3_b3_ef_pa";
+  }
   if (lda % 4 != 0) return "cpa_128x128x32_s3_k8_b2";  // A copied 4 bytes at a time: any lda
   if (M * N <= 256 * 256) return "tma_128x64x32_w64x32_s3_quad_b3";
   // Measured on GB300 with the stream-K tail (which removes most of the
@@ -238,6 +249,33 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       }
       if (cudaMalloc(&flags, static_cast<size_t>(slots) * sizeof(unsigned int)) != cudaSuccess ||
           cudaMemset(flags, 0, static_cast<size_t>(slots) * sizeof(unsigned int)) != cudaSuccess) {
+        cudaFree(ws);
+        if (flags) cudaFree(flags);
+        delete p;
+        return SGEMM_ERR_CUDA;
+      }
+      p->ws = static_cast<float*>(ws);
+      p->flags = static_cast<unsigned int*>(flags);
+    }
+  } else if (v->kind == kKindSkinny && v->streamk) {
+    // Stream-K few-row kernel: one resident wave over (slab, k-slice) units;
+    // every CTA gets at least one unit.  Empty problems and K == 0 never
+    // launch it and need no workspace.
+    const int64_t KT = (K + v->bk - 1) / v->bk;
+    const int64_t units = p->tiles * KT;
+    const int64_t slots = static_cast<int64_t>(sms) * ctas;
+    grid = units < slots ? units : slots;
+    if (units > 0) {
+      p->sk_iters = units;
+      const size_t ws_bytes = static_cast<size_t>(grid) * v->bm * v->bn * sizeof(float);
+      void* ws = nullptr;
+      void* flags = nullptr;
+      if (cudaMalloc(&ws, ws_bytes) != cudaSuccess) {
+        delete p;
+        return SGEMM_ERR_CUDA;
+      }
+      if (cudaMalloc(&flags, static_cast<size_t>(grid) * sizeof(unsigned int)) != cudaSuccess ||
+          cudaMemset(flags, 0, static_cast<size_t>(grid) * sizeof(unsigned int)) != cudaSuccess) {
         cudaFree(ws);
         if (flags) cudaFree(flags);
         delete p;

@@ -75,16 +75,6 @@ struct Params {
   unsigned int epoch;
 };
 
-__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 template <int BM_, int BN, int STAGES>
 struct Shape {
   static constexpr int BM = BM_;
@@ -309,7 +299,7 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
       }
       __threadfence();
       __syncthreads();
-      if (threadIdx.x == 0) st_release_gpu(p.flags + b, p.epoch);
+      if (threadIdx.x == 0) ptx::st_release_gpu(p.flags + b, p.epoch);
       continue;
     }
     if (seg_k0 > 0) {  // finisher of a shared tile: wait for the contributors, add them in CTA order
@@ -318,9 +308,9 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
       bool timed_out = false;
       if (threadIdx.x == 0) {
         for (int c = c_first; c < b && !timed_out; ++c) {
-          if (ld_acquire_gpu(p.flags + c) == p.epoch) continue;
+          if (ptx::ld_acquire_gpu(p.flags + c) == p.epoch) continue;
           const uint64_t t0 = ptx::globaltimer_ns();
-          while (ld_acquire_gpu(p.flags + c) != p.epoch) {
+          while (ptx::ld_acquire_gpu(p.flags + c) != p.epoch) {
             if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
               atomicOr(p.status, kStatusTimeoutFull);
               timed_out = true;

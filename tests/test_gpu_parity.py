@@ -157,7 +157,10 @@ def test_medium_full_compare(sg, oracle_mod, shape):
 # ---- few rows: the cluster split-K kernel ---------------------------------------
 
 SKINNY_CASES = [(16, 16384 // 8, 8192 // 4), (1, 300, 1000), (7, 129, 33), (16, 128, 32), (13, 1000, 4097),
-                (16, 2048, 96), (3, 5000, 8), (16, 77, 1), (9, 4096, 2000)]
+                (16, 2048, 96), (3, 5000, 8), (16, 77, 1), (9, 4096, 2000),
+                # stream-K few-row kernel: ranges covering whole slabs (600 slabs x 2 k-slices),
+                # one unit per CTA with 128 contributors per slab, and ragged N and K
+                (16, 76800, 64), (16, 384, 4096), (5, 1000, 3000)]
 
 
 @pytest.mark.parametrize("shape", SKINNY_CASES)
