@@ -13,6 +13,7 @@ enum VariantKind : int {
   kKindTma = 1,      // TMA-fed multi-stage pipeline, needs 16-byte aligned A/B rows
   kKindSkinny = 2,   // small-M streaming kernel, needs 16-byte aligned A/B rows
   kKindCpa = 3,      // A by cp.async (transposed, any alignment), B by TMA (16-byte aligned rows)
+  kKindTc = 4,       // tensor cores, operands split into two TF32 parts (any alignment; plan workspace)
 };
 
 // Everything one launch needs.  Tensor maps are encoded by the caller per
@@ -36,6 +37,13 @@ struct LaunchArgs {
   unsigned int epoch;
   unsigned int* status;  // per-device status word (error bits)
   uint64_t timeout_ns;   // limit for every in-kernel wait
+  // split-TF32 tensor-core variants: A_hi, A_lo (M x split_ld), then B_hi,
+  // B_lo transposed (N x split_ld) in one plan-owned buffer, described by
+  // tmA (A_hi), tmA2 (A_lo), tmB (B_hi), tmB2 (B_lo)
+  float* split;
+  int64_t split_ld;
+  CUtensorMap tmA2;
+  CUtensorMap tmB2;
 };
 
 struct Variant {
@@ -64,6 +72,7 @@ const Variant* tma_variants_c(int* count);
 const Variant* skinny_variants(int* count);
 const Variant* cpa_variants(int* count);
 const Variant* tmat_variants(int* count);
+const Variant* tc_variants(int* count);
 
 // C = beta * C (K == 0 or alpha == 0), any leading dimension.
 cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaStream_t stream);

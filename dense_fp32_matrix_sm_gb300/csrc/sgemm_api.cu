@@ -37,6 +37,10 @@ struct sgemm_plan_s {
   float* ws;
   unsigned int* flags;
   std::atomic<unsigned int> epoch;
+  // split-TF32 tensor-core variants: operand buffer and its four tensor maps
+  float* tc_split;
+  int64_t tc_split_ld;
+  CUtensorMap tc_maps[4];
 };
 
 // Per-device status word written by kernels (timeouts).  Its device address
@@ -69,6 +73,8 @@ struct Registry {
     v = cpa_variants(&n);
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
     v = tmat_variants(&n);
+    for (int i = 0; i < n; ++i) all.push_back(&v[i]);
+    v = tc_variants(&n);
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
   }
 };
@@ -126,8 +132,11 @@ sgemm_status_t check_dims(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
 }
 
 bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb) {
-  (void)K;
   if (v->kind == kKindGeneric) return true;
+  // split-TF32: the split kernels read A and B with plain loads (any layout).
+  // The split leaves ~3 * 2^-22 |a b| per product; K >= 16 keeps that well
+  // inside the acceptance bound 4 K 2^-24 |A||B|.
+  if (v->kind == kKindTc) return K >= 16;
   if (ldb % 4 != 0) return false;  // TMA row strides must be multiples of 16 bytes
   if (v->kind == kKindCpa) return true;  // A is copied 4 bytes at a time: any lda
   if (lda % 4 != 0) return false;
@@ -229,6 +238,8 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->ws = nullptr;
   p->flags = nullptr;
   p->epoch.store(0);
+  p->tc_split = nullptr;
+  p->tc_split_ld = 0;
   if (v->kind == kKindTma || v->kind == kKindCpa) {
     const int64_t slots = static_cast<int64_t>(sms) * ctas;
     if (grid > slots) grid = slots;
@@ -283,6 +294,41 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       }
       p->ws = static_cast<float*>(ws);
       p->flags = static_cast<unsigned int*>(flags);
+    }
+  } else if (v->kind == kKindTc) {
+    // One 128 x 256 tile per CTA.  The plan owns the split operands
+    // (A_hi, A_lo: M x kp; B_hi, B_lo transposed: N x kp) and encodes their
+    // four tensor maps once: 32-float (128-byte, swizzled) k-slices of 128
+    // rows of A and 256 rows of B.
+    if (p->tiles > 0 && K > 0) {
+      const int64_t kp = (K + 3) / 4 * 4;  // 16-byte row stride for TMA
+      const size_t bytes = static_cast<size_t>(2 * (M + N) * kp) * sizeof(float);
+      void* buf = nullptr;
+      if (cudaMalloc(&buf, bytes) != cudaSuccess) {
+        delete p;
+        return SGEMM_ERR_CUDA;
+      }
+      p->tc_split = static_cast<float*>(buf);
+      p->tc_split_ld = kp;
+      float* parts[4] = {p->tc_split, p->tc_split + M * kp, p->tc_split + 2 * M * kp,
+                         p->tc_split + (2 * M + N) * kp};
+      const int64_t rows[4] = {M, M, N, N};
+      const cuuint32_t box_rows[4] = {static_cast<cuuint32_t>(v->bm), static_cast<cuuint32_t>(v->bm),
+                                      static_cast<cuuint32_t>(v->bn), static_cast<cuuint32_t>(v->bn)};
+      EncodeTiledFn enc = encode_fn();
+      for (int i = 0; i < 4; ++i) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows[i])};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kp) * 4};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(v->bk), box_rows[i]};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&p->tc_maps[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, parts[i], dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+          cudaFree(buf);
+          delete p;
+          return SGEMM_ERR_CUDA;
+        }
+      }
     }
   } else if (v->kind == kKindSkinny) {
     // Persistent clusters of S CTAs (S <= 8, the portable cluster size)
@@ -391,7 +437,7 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   const Variant* v = reg.all[p->config_id];
   int grid = p->grid;
   const bool a_needs_16 = v->kind == kKindTma || v->kind == kKindSkinny;
-  if (v->kind != kKindGeneric &&
+  if (v->kind != kKindGeneric && v->kind != kKindTc &&
       ((a_needs_16 && (reinterpret_cast<uintptr_t>(A) & 15) != 0) || (reinterpret_cast<uintptr_t>(B) & 15) != 0)) {
     v = reg.all[p->generic_id];
     grid = 0;
@@ -433,7 +479,14 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   sgemm_status_t st = status_addr(device, &a.status);
   if (st != SGEMM_OK) return st;
-  if (v->kind != kKindGeneric && v->tma_swizzle_a >= 0) {
+  if (v->kind == kKindTc) {
+    a.split = p->tc_split;
+    a.split_ld = p->tc_split_ld;
+    a.tmA = p->tc_maps[0];
+    a.tmA2 = p->tc_maps[1];
+    a.tmB = p->tc_maps[2];
+    a.tmB2 = p->tc_maps[3];
+  } else if (v->kind != kKindGeneric && v->tma_swizzle_a >= 0) {
     st = encode_maps(v, p, A, B, &a);
     if (st != SGEMM_OK) return st;
   }
@@ -476,6 +529,7 @@ sgemm_status_t sgemm_plan_destroy(sgemm_plan_t plan) {
   sgemm_status_t st = SGEMM_OK;
   if (plan->ws && cudaFree(plan->ws) != cudaSuccess) st = SGEMM_ERR_CUDA;
   if (plan->flags && cudaFree(plan->flags) != cudaSuccess) st = SGEMM_ERR_CUDA;
+  if (plan->tc_split && cudaFree(plan->tc_split) != cudaSuccess) st = SGEMM_ERR_CUDA;
   delete plan;
   return st;
 }
@@ -486,11 +540,12 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
   snprintf(buf, n,
            "variant=%s kind=%s tile=%dx%dx%d stages=%d ffma2=%d threads=%d smem=%d grid=%d ctas_per_sm=%d "
            "tiles=%lld sms=%d split=%d streamk=%d dp_waves=%d sk_tiles=%lld k_order=%s M=%lld N=%lld K=%lld",
-           v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : "skinny", v->bm, v->bn,
+           v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : v->kind == kKindTc ? "tc" : "skinny", v->bm, v->bn,
            v->bk, v->stages, v->ffma2, v->threads, v->smem_bytes, plan->grid, plan->ctas_per_sm,
            static_cast<long long>(plan->tiles), plan->num_sms, plan->split, plan->sk_iters > 0 ? 1 : 0, plan->dp_waves,
            static_cast<long long>(plan->sk_iters > 0 ? plan->tiles - static_cast<int64_t>(plan->dp_waves) * plan->grid : 0),
-           (plan->split > 1 || v->kind == kKindSkinny || plan->sk_iters > 0) ? "split" : "sequential",
+           v->kind == kKindTc ? "tf32x3"
+           : (plan->split > 1 || v->kind == kKindSkinny || plan->sk_iters > 0) ? "split" : "sequential",
            static_cast<long long>(plan->M),
            static_cast<long long>(plan->N), static_cast<long long>(plan->K));
   return SGEMM_OK;
@@ -498,7 +553,9 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
 
 sgemm_status_t sgemm_plan_launches(sgemm_plan_t plan, int* out) {
   if (!plan || !out) return SGEMM_ERR_INVALID_ARG;
-  *out = (plan->M == 0 || plan->N == 0) ? 0 : 1;
+  // the split-TF32 variants launch two operand-split kernels before the GEMM
+  const Variant* v = registry().all[plan->config_id];
+  *out = (plan->M == 0 || plan->N == 0) ? 0 : v->kind == kKindTc && plan->K > 0 ? 3 : 1;
   return SGEMM_OK;
 }
 

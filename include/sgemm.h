@@ -15,6 +15,22 @@
  * "k_order=split" (a split-K plan adds fixed-order partial sums).  The
  * epilogue is out = alpha*acc (beta == 0) or fmaf(alpha, acc, beta*C_old).
  *
+ * One variant computes differently and is never picked by the shape table:
+ * "tf32x3_128x256x32_s2" (sgemm_plan_with_config or SGEMM_FORCE_CONFIG).
+ *   - Operation: the same C = alpha*A*B + beta*C on the tensor cores.
+ *   - Method: each operand is split as x = hi + lo into two TF32 values (round to
+ *     nearest; |x - hi - lo| <= 2^-22 |x|), and the product is
+ *     hi*hi + hi*lo + lo*hi accumulated in float32 (k_order=tf32x3).
+ *   - Accuracy: results stay within the acceptance bound
+ *     |C - C_ref| <= 4 K 2^-24 |A||B| + 1e-6. The plan refuses K < 16 with
+ *     SGEMM_ERR_UNSUPPORTED.
+ *   - Limits: it needs finite inputs below about 2^127 in magnitude, where
+ *     the split cannot overflow.
+ *   - Memory: the plan allocates 2 (M + N) round_up(K, 4) floats for the split
+ *     operands.
+ *   - Launches: each run launches three kernels (two splits, then the GEMM).
+ *   - Layout: any alignment and leading dimension are accepted.
+ *
  * Conventions (BLAS readings where the pages are silent):
  *   - lda >= max(1, K), ldb >= max(1, N), ldc >= max(1, N), else
  *     SGEMM_ERR_INVALID_ARG.  Dimensions above 2^31 - 1 give

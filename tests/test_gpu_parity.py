@@ -119,7 +119,7 @@ def _shape_cases(n=40, seed=0):
     return sorted(cases)
 
 
-@pytest.mark.parametrize("variant_idx", range(24))
+@pytest.mark.parametrize("variant_idx", range(40))
 def test_shape_sweep_every_variant(sg, oracle_mod, variant_idx):
     names = _variants(sg)
     if variant_idx >= len(names):
@@ -415,3 +415,51 @@ def test_stream_k_tail(sg, oracle_mod, shape):
                                        np.ascontiguousarray(C0[np.ix_(rows, cols)]), 0.5, 3.0)
         assert_parity(Cs, Cref, S, K, f"{name} {shape} streamk={info['streamk']} dp_waves={info['dp_waves']}")
     assert saw_streamk, "no variant split its tail for these shapes"
+
+
+# ---- split-TF32 tensor-core variant (reported apart from the FFMA path) -------
+
+TC = "tf32x3_128x256x32_s2"
+
+
+@pytest.mark.parametrize("case", [
+    # (M, N, K, lda pad, ldb pad, ldc pad, A offset, B offset, alpha, beta, distribution)
+    (1024, 1024, 1024, 0, 0, 0, 0, 0, 1.0, 0.0, "normal"),
+    (1000, 1100, 999, 1, 3, 5, 1, 2, 0.5, 3.0, "normal"),
+    (300, 2000, 517, 0, 0, 0, 0, 0, -1.25, 1.0, "normal"),
+    (129, 257, 16, 0, 0, 0, 0, 0, 1.0, 0.0, "normal"),
+    # all-positive inputs: partial sums grow to |A||B|, the worst case for accumulator rounding
+    (512, 768, 4096, 0, 0, 0, 0, 0, 1.0, 0.0, "positive"),
+])
+def test_split_tf32_variant(sg, oracle_mod, case):
+    M, N, K, pa, pb, pc, oa, ob, alpha, beta, dist = case
+    d = ("uniform", 1.0) if dist == "normal" else ("uniform", 1.0)
+    A, B, C0 = make_inputs(M, N, K, seed=M + N + K, dist_a=("normal", 1.0) if dist == "normal" else d, dist_b=d)
+    if dist == "positive":
+        A, B = np.abs(A), np.abs(B)
+    Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
+    C, used = run_gpu(sg, A, B, C0, alpha, beta, config=TC, lda=K + pa, ldb=N + pb, ldc=N + pc, off_a=oa,
+                      off_b=ob)
+    assert used == TC and run_gpu.last_info["k_order"] == "tf32x3"
+    assert_parity(C, Cref, S, K, f"{TC} {M}x{N}x{K} {dist}")
+    C2, _ = run_gpu(sg, A, B, C0, alpha, beta, config=TC, lda=K + pa, ldb=N + pb, ldc=N + pc, off_a=oa, off_b=ob)
+    assert np.array_equal(C, C2)
+
+
+def test_split_tf32_rejects_short_k(sg):
+    with pytest.raises(sg.SgemmError) as e:
+        sg.Plan(256, 256, 15, config=TC)
+    assert e.value.status == sg.SGEMM_ERR_UNSUPPORTED
+    plan = sg.Plan(256, 256, 16, config=TC)
+    assert plan.launches == 3
+    plan.close()
+
+
+def test_split_tf32_full_size_sample(sg, oracle_mod):
+    w = WORKLOADS["square4096"]
+    A, B, C0 = workload_inputs(w)
+    C, used = run_gpu(sg, A, B, C0, w.alpha, w.beta, config=TC)
+    rows, cols = sample_rows_cols(w.M, w.N, tile_n=256, seed=5)
+    Cref, S = oracle_mod.sgemm_ref(np.ascontiguousarray(A[rows]), np.ascontiguousarray(B[:, cols]),
+                                   np.ascontiguousarray(C0[np.ix_(rows, cols)]), w.alpha, w.beta)
+    assert_parity(C[np.ix_(rows, cols)], Cref, S, w.K, f"{TC} square4096 sample")
