@@ -265,6 +265,54 @@ def time_steps(torch, fn, steps: int, flush, stream):
     return [s.elapsed_time(e) for s, e in evs]
 
 
+TC_VARIANT = "tf32x3_128x256x32_s2"
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tensor rates, TF32 over BF16
+
+
+def tc_leg(torch, sg, w, dA, dB, dC0, stream, flush, warmup, steps, dist, peaks):
+    """Time the split-TF32 variant like the main leg (L2 flushed, CUDA events) and
+    report its agreement with the FFMA kernel on one fresh product."""
+    plan = sg.Plan(w.M, w.N, w.K, config=TC_VARIANT)
+    launches = plan.launches
+    tC = dC0.clone()
+
+    def tc_step():
+        plan.run(w.alpha, dA, dB, w.beta, tC, stream)
+
+    for _ in range(warmup):
+        flush()
+        tc_step()
+    torch.cuda.synchronize()
+    times = time_steps(torch, tc_step, steps, flush, stream)
+    if sg.device_status() != sg.SGEMM_OK:
+        raise SystemExit("kernel status word set during the split-TF32 steps")
+    ms = max_over_ranks(torch, dist, statistics.fmean(times))
+    # one fresh product from each path, compared elementwise
+    c_tc = dC0.clone()
+    plan.run(w.alpha, dA, dB, w.beta, c_tc, stream)
+    ffma = sg.Plan(w.M, w.N, w.K)
+    c_ff = dC0.clone()
+    ffma.run(w.alpha, dA, dB, w.beta, c_ff, stream)
+    torch.cuda.synchronize()
+    rel = float(((c_tc - c_ff).abs().max() / c_ff.abs().max().clamp_min(1e-30)).item())
+    ffma.close()
+    desc = plan.describe()
+    plan.close()
+    bf16 = peaks.get("bf16_tflops")
+    peak = round((bf16 if bf16 else 1900.0) * TF32_PER_BF16, 1)
+    tensor_tflops = 3 * w.flops / (ms * 1e-3) / 1e12  # three TF32 products per FP32 multiply-add
+    return {"variant": TC_VARIANT, "value": round(w.flops / (ms * 1e-3) / 1e9, 1), "unit": "GFLOP/s",
+            "ms_per_step": round(ms, 4), "steps": steps, "gpu_launches": launches * steps,
+            "k_order": "tf32x3", "max_abs_diff_vs_ffma_rel_to_max_abs_c": rel,
+            "roofline": {"bound": "tensor", "achieved": round(tensor_tflops, 1), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(tensor_tflops / peak, 4), "traffic": None,
+                         "peak_basis": ("MEASURED_PEAKS.json bf16_tflops (burst) x nominal TF32/BF16 ratio 1.1/2.25 "
+                                        "(of measured)" if bf16 else "fallback 1.9 PF bf16 x 1.1/2.25 (of fallback)"),
+                         "achieved_basis": "3 x 2MNK TF32 tensor FLOPs over the whole step (the two split kernels "
+                                           "included)"},
+            "plan": desc}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -421,6 +469,11 @@ def run_ours(args):
         out["cublas_context"] = {"gflops": round(w.flops / (cb_ms * 1e-3) / 1e9, 1), "ms": round(cb_ms, 4),
                                  "call": "torch.matmul/addmm fp32, allow_tf32=False",
                                  "float32_matmul_precision": torch.get_float32_matmul_precision()}
+
+        # The split-TF32 tensor-core variant on the same workload, reported on
+        # its own: never the FFMA figure above.
+        if TC_VARIANT in sg.config_names() and w.K >= 16:
+            out["tf32x3"] = tc_leg(torch, sg, w, dA, dB, dC0, stream, flush, warmup, min(steps, 100), dist, peaks)
 
         if rank == 0 and world == 1:
             import oracle

@@ -43,6 +43,7 @@ SIGNATURES = {
     "sgemm_set_wait_timeout_ns": (_int, [ctypes.c_uint64]),
     "sgemm_selftest_wait_timeout": (_int, [ctypes.c_uint64, _vp]),
     "sgemm_run_static_scratch": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
+    "sgemm_plan_ex": (_int, [_int, _int, _int, _i64, _i64, _i64, _i64, _i64, _i64, _int, ctypes.POINTER(_vp)]),
 }
 
 _lib = None
@@ -149,14 +150,25 @@ class Plan:
     """
 
     def __init__(self, M: int, N: int, K: int, lda: Optional[int] = None, ldb: Optional[int] = None,
-                 ldc: Optional[int] = None, config=None):
+                 ldc: Optional[int] = None, config=None, order: str = "row", transa: bool = False,
+                 transb: bool = False):
         l = lib()
         self.M, self.N, self.K = int(M), int(N), int(K)
-        self.lda = int(lda) if lda is not None else max(1, self.K)
-        self.ldb = int(ldb) if ldb is not None else max(1, self.N)
-        self.ldc = int(ldc) if ldc is not None else max(1, self.N)
+        row = order == "row"
+        if order not in ("row", "col"):
+            raise ValueError("order must be 'row' or 'col'")
+        # default leading dimensions: dense stored matrices in the given order
+        a_rows, a_cols = (self.K, self.M) if transa else (self.M, self.K)
+        b_rows, b_cols = (self.N, self.K) if transb else (self.K, self.N)
+        self.lda = int(lda) if lda is not None else max(1, a_cols if row else a_rows)
+        self.ldb = int(ldb) if ldb is not None else max(1, b_cols if row else b_rows)
+        self.ldc = int(ldc) if ldc is not None else max(1, self.N if row else self.M)
         h = ctypes.c_void_p()
-        if config is None:
+        if not row or transa or transb:
+            cid = -1 if config is None else (config if isinstance(config, int) else config_id(config))
+            st = l.sgemm_plan_ex(0 if row else 1, 1 if transa else 0, 1 if transb else 0, self.M, self.N, self.K,
+                                 self.lda, self.ldb, self.ldc, cid, ctypes.byref(h))
+        elif config is None:
             st = l.sgemm_plan(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, ctypes.byref(h))
         else:
             cid = config if isinstance(config, int) else config_id(config)

@@ -168,6 +168,33 @@ cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaSt
   return cudaGetLastError();
 }
 
+// out (cols x rows, ld_out) = transpose of in (rows x cols, ld_in), through a
+// 32 x 33 shared tile so both the reads and the writes are coalesced.
+__global__ void transpose_kernel(const float* __restrict__ in, int64_t ld_in, int rows, int cols,
+                                 float* __restrict__ out, int64_t ld_out) {
+  __shared__ float t[32][33];
+  const int c0 = blockIdx.x * 32;
+  const int r0 = blockIdx.y * 32;
+  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+    const int r = r0 + j, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) t[j][threadIdx.x] = in[static_cast<int64_t>(r) * ld_in + c];
+  }
+  __syncthreads();
+  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+    const int c = c0 + j, r = r0 + threadIdx.x;
+    if (c < cols && r < rows) out[static_cast<int64_t>(c) * ld_out + r] = t[threadIdx.x][j];
+  }
+}
+
+cudaError_t launch_transpose(const float* in, int64_t ld_in, int rows, int cols, float* out, int64_t ld_out,
+                             cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const dim3 grid((cols + 31) / 32, (rows + 31) / 32);
+  if (grid.y > 65535u) return cudaErrorInvalidValue;
+  transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(in, ld_in, rows, cols, out, ld_out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
   return cudaGetLastError();

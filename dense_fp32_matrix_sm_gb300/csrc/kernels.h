@@ -44,6 +44,10 @@ struct LaunchArgs {
   int64_t split_ld;
   CUtensorMap tmA2;
   CUtensorMap tmB2;
+  // split-TF32 variants read A and B themselves: a_trans = 1 means A is
+  // stored K x M (row-major, lda), b_trans = 1 means B is stored N x K
+  int a_trans;
+  int b_trans;
 };
 
 struct Variant {
@@ -76,6 +80,10 @@ const Variant* tc_variants(int* count);
 
 // C = beta * C (K == 0 or alpha == 0), any leading dimension.
 cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaStream_t stream);
+
+// out (cols x rows, ld_out) = in (rows x cols, ld_in) transposed.
+cudaError_t launch_transpose(const float* in, int64_t ld_in, int rows, int cols, float* out, int64_t ld_out,
+                             cudaStream_t stream);
 
 // One-thread kernel that waits on a barrier phase nothing completes.
 cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream);

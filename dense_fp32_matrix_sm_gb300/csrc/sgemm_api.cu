@@ -41,6 +41,17 @@ struct sgemm_plan_s {
   float* tc_split;
   int64_t tc_split_ld;
   CUtensorMap tc_maps[4];
+  // sgemm_plan_ex: the problem as given, reduced to row-major (after the
+  // column-major swap of A and B); ta / tb: that operand is stored
+  // transposed (A as K x M, B as N x K) with leading dimension ex_lda /
+  // ex_ldb.  ex_wa / ex_wb: plan-owned buffers the run transposes it into
+  // (none for the split-TF32 variants, which read both layouts).
+  int ex_order;
+  int ex_swap;
+  int ex_ta, ex_tb;
+  int64_t ex_lda, ex_ldb;
+  float* ex_wa;
+  float* ex_wb;
 };
 
 // Per-device status word written by kernels (timeouts).  Its device address
@@ -240,6 +251,13 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->epoch.store(0);
   p->tc_split = nullptr;
   p->tc_split_ld = 0;
+  p->ex_order = SGEMM_ROW_MAJOR;
+  p->ex_swap = 0;
+  p->ex_ta = p->ex_tb = 0;
+  p->ex_lda = lda;
+  p->ex_ldb = ldb;
+  p->ex_wa = nullptr;
+  p->ex_wb = nullptr;
   if (v->kind == kKindTma || v->kind == kKindCpa) {
     const int64_t slots = static_cast<int64_t>(sms) * ctas;
     if (grid > slots) grid = slots;
@@ -414,6 +432,63 @@ sgemm_status_t sgemm_plan_with_config(int64_t M, int64_t N, int64_t K, int64_t l
   return make_plan(M, N, K, lda, ldb, ldc, config_id, out);
 }
 
+sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64_t N, int64_t K, int64_t lda,
+                             int64_t ldb, int64_t ldc, int config_id, sgemm_plan_t* out) {
+  if (!out) return SGEMM_ERR_INVALID_ARG;
+  if ((order != SGEMM_ROW_MAJOR && order != SGEMM_COL_MAJOR) || (transa != SGEMM_NO_TRANS && transa != SGEMM_TRANS) ||
+      (transb != SGEMM_NO_TRANS && transb != SGEMM_TRANS))
+    return SGEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+  // leading dimensions of the stored matrices, in the given order
+  const int64_t a_rows = transa ? K : M, a_cols = transa ? M : K;
+  const int64_t b_rows = transb ? N : K, b_cols = transb ? K : N;
+  const bool row = order == SGEMM_ROW_MAJOR;
+  if (lda < std::max<int64_t>(1, row ? a_cols : a_rows) || ldb < std::max<int64_t>(1, row ? b_cols : b_rows) ||
+      ldc < std::max<int64_t>(1, row ? N : M))
+    return SGEMM_ERR_INVALID_ARG;
+  // Column-major C = op(A) op(B) is the row-major C^T = op(B)^T op(A)^T over
+  // the same memory: swap the operands and their transpose flags.
+  const int swap = row ? 0 : 1;
+  const int64_t M2 = swap ? N : M, N2 = swap ? M : N;
+  const int ta = swap ? transb : transa, tb = swap ? transa : transb;
+  const int64_t lda2 = swap ? ldb : lda, ldb2 = swap ? lda : ldb;
+  if (M2 > 0x7fffffff || N2 > 0x7fffffff || K > 0x7fffffff) return SGEMM_ERR_UNSUPPORTED;
+
+  const Registry& reg = registry();
+  if (config_id >= static_cast<int>(reg.all.size())) return SGEMM_ERR_INVALID_ARG;
+  int forced = config_id;
+  if (forced < 0) {
+    const char* env = getenv("SGEMM_FORCE_CONFIG");
+    if (env && *env) forced = find_variant(env);
+  }
+  const bool native = forced >= 0 && reg.all[forced]->kind == kKindTc;  // reads either layout itself
+  // the row-major, untransposed operands the other kernels read: a
+  // transposed operand goes through a plan buffer with a 16-byte row stride
+  const int64_t lda_eff = ta && !native ? std::max<int64_t>(4, (K + 3) / 4 * 4) : (ta ? std::max<int64_t>(1, K) : lda2);
+  const int64_t ldb_eff = tb && !native ? std::max<int64_t>(4, (N2 + 3) / 4 * 4) : (tb ? std::max<int64_t>(1, N2) : ldb2);
+  sgemm_plan_t p = nullptr;
+  sgemm_status_t st = make_plan(M2, N2, K, lda_eff, ldb_eff, ldc, config_id, &p);
+  if (st != SGEMM_OK) return st;
+  p->ex_order = order;
+  p->ex_swap = swap;
+  p->ex_ta = ta;
+  p->ex_tb = tb;
+  p->ex_lda = lda2;
+  p->ex_ldb = ldb2;
+  if (!native && registry().all[p->config_id]->kind != kKindTc) {
+    if (ta && M2 > 0 && K > 0 && cudaMalloc(reinterpret_cast<void**>(&p->ex_wa), sizeof(float) * M2 * lda_eff) != cudaSuccess) {
+      sgemm_plan_destroy(p);
+      return SGEMM_ERR_CUDA;
+    }
+    if (tb && N2 > 0 && K > 0 && cudaMalloc(reinterpret_cast<void**>(&p->ex_wb), sizeof(float) * K * ldb_eff) != cudaSuccess) {
+      sgemm_plan_destroy(p);
+      return SGEMM_ERR_CUDA;
+    }
+  }
+  *out = p;
+  return SGEMM_OK;
+}
+
 sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const float* B, float beta, float* C,
                          void* stream_) {
   if (!plan) return SGEMM_ERR_INVALID_ARG;
@@ -435,6 +510,22 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
 
   const Registry& reg = registry();
   const Variant* v = reg.all[p->config_id];
+  // sgemm_plan_ex: column-major runs the row-major product of the swapped
+  // operands; a transposed operand is first transposed into the plan's
+  // buffer (the split-TF32 variants read it as stored instead)
+  if (p->ex_swap) std::swap(A, B);
+  if (p->ex_wa) {
+    if (launch_transpose(A, p->ex_lda, static_cast<int>(p->K), static_cast<int>(p->M), p->ex_wa, p->lda, stream) !=
+        cudaSuccess)
+      return SGEMM_ERR_CUDA;
+    A = p->ex_wa;
+  }
+  if (p->ex_wb) {
+    if (launch_transpose(B, p->ex_ldb, static_cast<int>(p->N), static_cast<int>(p->K), p->ex_wb, p->ldb, stream) !=
+        cudaSuccess)
+      return SGEMM_ERR_CUDA;
+    B = p->ex_wb;
+  }
   int grid = p->grid;
   const bool a_needs_16 = v->kind == kKindTma || v->kind == kKindSkinny;
   if (v->kind != kKindGeneric && v->kind != kKindTc &&
@@ -482,6 +573,10 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   if (v->kind == kKindTc) {
     a.split = p->tc_split;
     a.split_ld = p->tc_split_ld;
+    a.a_trans = p->ex_ta;
+    a.b_trans = p->ex_tb;
+    a.lda = p->ex_lda;
+    a.ldb = p->ex_ldb;
     a.tmA = p->tc_maps[0];
     a.tmA2 = p->tc_maps[1];
     a.tmB = p->tc_maps[2];
@@ -504,10 +599,15 @@ sgemm_status_t sgemm_run_host(sgemm_plan_t plan, float alpha, const float* hA, c
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   const size_t fs = sizeof(float);
   if (product) {
-    if (cudaMemcpy2DAsync(dA, p->lda * fs, hA, p->lda * fs, p->K * fs, p->M, cudaMemcpyHostToDevice, stream) !=
+    // stored shapes in row-major terms (a column-major plan holds them swapped)
+    const int64_t ra = p->ex_ta ? p->K : p->M, ca = p->ex_ta ? p->M : p->K;
+    const int64_t rb = p->ex_tb ? p->N : p->K, cb = p->ex_tb ? p->K : p->N;
+    const int64_t ra_u = p->ex_swap ? rb : ra, ca_u = p->ex_swap ? cb : ca, lda_u = p->ex_swap ? p->ex_ldb : p->ex_lda;
+    const int64_t rb_u = p->ex_swap ? ra : rb, cb_u = p->ex_swap ? ca : cb, ldb_u = p->ex_swap ? p->ex_lda : p->ex_ldb;
+    if (cudaMemcpy2DAsync(dA, lda_u * fs, hA, lda_u * fs, ca_u * fs, ra_u, cudaMemcpyHostToDevice, stream) !=
         cudaSuccess)
       return SGEMM_ERR_CUDA;
-    if (cudaMemcpy2DAsync(dB, p->ldb * fs, hB, p->ldb * fs, p->N * fs, p->K, cudaMemcpyHostToDevice, stream) !=
+    if (cudaMemcpy2DAsync(dB, ldb_u * fs, hB, ldb_u * fs, cb_u * fs, rb_u, cudaMemcpyHostToDevice, stream) !=
         cudaSuccess)
       return SGEMM_ERR_CUDA;
   }
@@ -530,6 +630,8 @@ sgemm_status_t sgemm_plan_destroy(sgemm_plan_t plan) {
   if (plan->ws && cudaFree(plan->ws) != cudaSuccess) st = SGEMM_ERR_CUDA;
   if (plan->flags && cudaFree(plan->flags) != cudaSuccess) st = SGEMM_ERR_CUDA;
   if (plan->tc_split && cudaFree(plan->tc_split) != cudaSuccess) st = SGEMM_ERR_CUDA;
+  if (plan->ex_wa && cudaFree(plan->ex_wa) != cudaSuccess) st = SGEMM_ERR_CUDA;
+  if (plan->ex_wb && cudaFree(plan->ex_wb) != cudaSuccess) st = SGEMM_ERR_CUDA;
   delete plan;
   return st;
 }
@@ -539,15 +641,18 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
   const Variant* v = registry().all[plan->config_id];
   snprintf(buf, n,
            "variant=%s kind=%s tile=%dx%dx%d stages=%d ffma2=%d threads=%d smem=%d grid=%d ctas_per_sm=%d "
-           "tiles=%lld sms=%d split=%d streamk=%d dp_waves=%d sk_tiles=%lld k_order=%s M=%lld N=%lld K=%lld",
+           "tiles=%lld sms=%d split=%d streamk=%d dp_waves=%d sk_tiles=%lld k_order=%s M=%lld N=%lld K=%lld "
+           "order=%s op=%c%c",
            v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : v->kind == kKindTc ? "tc" : "skinny", v->bm, v->bn,
            v->bk, v->stages, v->ffma2, v->threads, v->smem_bytes, plan->grid, plan->ctas_per_sm,
            static_cast<long long>(plan->tiles), plan->num_sms, plan->split, plan->sk_iters > 0 ? 1 : 0, plan->dp_waves,
            static_cast<long long>(plan->sk_iters > 0 ? plan->tiles - static_cast<int64_t>(plan->dp_waves) * plan->grid : 0),
            v->kind == kKindTc ? "tf32x3"
            : (plan->split > 1 || v->kind == kKindSkinny || plan->sk_iters > 0) ? "split" : "sequential",
-           static_cast<long long>(plan->M),
-           static_cast<long long>(plan->N), static_cast<long long>(plan->K));
+           static_cast<long long>(plan->ex_swap ? plan->N : plan->M),
+           static_cast<long long>(plan->ex_swap ? plan->M : plan->N), static_cast<long long>(plan->K),
+           plan->ex_order == SGEMM_COL_MAJOR ? "col" : "row",
+           (plan->ex_swap ? plan->ex_tb : plan->ex_ta) ? 'T' : 'N', (plan->ex_swap ? plan->ex_ta : plan->ex_tb) ? 'T' : 'N');
   return SGEMM_OK;
 }
 
@@ -556,6 +661,7 @@ sgemm_status_t sgemm_plan_launches(sgemm_plan_t plan, int* out) {
   // the split-TF32 variants launch two operand-split kernels before the GEMM
   const Variant* v = registry().all[plan->config_id];
   *out = (plan->M == 0 || plan->N == 0) ? 0 : v->kind == kKindTc && plan->K > 0 ? 3 : 1;
+  if (*out > 0 && plan->K > 0) *out += (plan->ex_wa ? 1 : 0) + (plan->ex_wb ? 1 : 0);
   return SGEMM_OK;
 }
 

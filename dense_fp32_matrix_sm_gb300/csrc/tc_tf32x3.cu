@@ -15,9 +15,10 @@
 // 3 * 2^-22 |a b| plus the accumulator's float32 rounding.
 //
 // Kernels (all launched by one sgemm_run):
-//  * split_rows: A (M x K, lda) -> A_hi, A_lo (M x kp, K-major);
-//  * split_transpose: B (K x N, ldb) -> B_hi, B_lo transposed (N x kp,
-//    K-major), through a 32 x 33 shared tile;
+//  * split_rows / split_transpose: A -> A_hi, A_lo (M x kp) and B -> B_hi,
+//    B_lo (N x kp), both K-major.  An operand already stored K-major (A as
+//    M x K, or B given transposed as N x K) is split row by row; the other
+//    layout is transposed through a 32 x 33 shared tile while splitting;
 //  * tf32x3_kernel: one 128 x 256 output tile per CTA.  Warp 0 issues TMA
 //    copies of the four 32-deep operand slices (128-byte swizzle) into a
 //    two-stage ring; warp 1 owns 256 TMEM columns and issues, per slice,
@@ -286,11 +287,20 @@ cudaError_t launch(const LaunchArgs& a, cudaStream_t stream) {
   float* al = ah + static_cast<int64_t>(a.M) * kp;
   float* bh = al + static_cast<int64_t>(a.M) * kp;
   float* bl = bh + static_cast<int64_t>(a.N) * kp;
-  const int64_t na = static_cast<int64_t>(a.M) * a.K;
-  const int blocks_a = static_cast<int>((na + 255) / 256 < 152 * 16 ? (na + 255) / 256 : 152 * 16);
-  split_rows_kernel<<<blocks_a, 256, 0, stream>>>(a.A, a.lda, a.M, a.K, ah, al, kp);
-  dim3 tgrid((a.N + 31) / 32, (a.K + 31) / 32);
-  split_transpose_kernel<<<tgrid, dim3(32, 8), 0, stream>>>(a.B, a.ldb, a.K, a.N, bh, bl, kp);
+  // both operands end K-major: A as M x kp, B as N x kp
+  auto rows_grid = [](int64_t n) { return static_cast<int>((n + 255) / 256 < 152 * 16 ? (n + 255) / 256 : 152 * 16); };
+  if (a.a_trans) {  // A stored K x M
+    split_transpose_kernel<<<dim3((a.M + 31) / 32, (a.K + 31) / 32), dim3(32, 8), 0, stream>>>(a.A, a.lda, a.K, a.M,
+                                                                                            ah, al, kp);
+  } else {
+    split_rows_kernel<<<rows_grid(static_cast<int64_t>(a.M) * a.K), 256, 0, stream>>>(a.A, a.lda, a.M, a.K, ah, al, kp);
+  }
+  if (a.b_trans) {  // B stored N x K: already K-major
+    split_rows_kernel<<<rows_grid(static_cast<int64_t>(a.N) * a.K), 256, 0, stream>>>(a.B, a.ldb, a.N, a.K, bh, bl, kp);
+  } else {
+    split_transpose_kernel<<<dim3((a.N + 31) / 32, (a.K + 31) / 32), dim3(32, 8), 0, stream>>>(a.B, a.ldb, a.K, a.N,
+                                                                                            bh, bl, kp);
+  }
   TcParams p;
   p.C = a.C;
   p.ldc = a.ldc;

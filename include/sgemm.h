@@ -107,6 +107,42 @@ sgemm_status_t sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
 sgemm_status_t sgemm_plan_with_config(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                       int64_t ldc, int config_id, sgemm_plan_t *out);
 
+/* Storage order and operand transposition for sgemm_plan_ex. */
+enum { SGEMM_ROW_MAJOR = 0, SGEMM_COL_MAJOR = 1 };
+enum { SGEMM_NO_TRANS = 0, SGEMM_TRANS = 1 };
+
+/*
+ * Plan C = alpha * op(A) * op(B) + beta * C for any storage order and
+ * transposition (the BLAS SGEMM interface): op(A) is M x K, op(B) is K x N,
+ * C is M x N.
+ *   - order: SGEMM_ROW_MAJOR or SGEMM_COL_MAJOR, for all three matrices.
+ *   - transa: A is stored M x K (SGEMM_NO_TRANS) or K x M (SGEMM_TRANS).
+ *     transb: B is stored K x N or N x K.
+ *   - lda, ldb, ldc: the distance between consecutive rows (row-major) or
+ *     columns (column-major) of the stored matrices. Each must be at least
+ *     that matrix's row length (row-major) or column length (column-major),
+ *     and at least 1; otherwise SGEMM_ERR_INVALID_ARG.
+ *   - config_id: -1 for the shape table, else a variant id as for
+ *     sgemm_plan_with_config.
+ *
+ * sgemm_run and sgemm_run_host take A, B and C as stored.
+ *
+ * How it runs:
+ *   - A column-major product runs as the row-major product
+ *     C^T = op(B)^T op(A)^T over the same memory.
+ *   - The FFMA kernels read row-major operands stored untransposed. A
+ *     transposed operand is first transposed on the GPU into a buffer the
+ *     plan allocates (cudaMalloc), one extra kernel per run.
+ *   - The split-TF32 variant reads either layout directly.
+ * Runs of a plan with such a buffer must not overlap in time.
+ *
+ * The pages cover the row-major, untransposed product only; the other
+ * layouts follow the BLAS SGEMM conventions. cuBLAS's layout coverage is
+ * noted in "Writing a Fast Matmul in CUDA", "What cuBLAS and CUTLASS add".
+ */
+sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64_t N, int64_t K, int64_t lda,
+                             int64_t ldb, int64_t ldc, int config_id, sgemm_plan_t *out);
+
 /*
  * Enqueue C = alpha*A*B + beta*C on `stream` (a cudaStream_t, may be NULL).
  * A, B, C are device pointers with the plan's shape and leading dimensions.

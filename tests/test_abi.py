@@ -70,6 +70,21 @@ def test_invalid_arguments_rejected_without_gpu(lib):
     assert lib.sgemm_plan_destroy(None) == 0
 
 
+def test_plan_ex_rejects_before_cuda(lib):
+    """sgemm_plan_ex checks order, flags and stored leading dimensions before any CUDA call."""
+    h = ctypes.c_void_p()
+    f = lib.sgemm_plan_ex
+    assert f(2, 0, 0, 8, 8, 8, 8, 8, 8, -1, ctypes.byref(h)) == -1        # bad order
+    assert f(0, 3, 0, 8, 8, 8, 8, 8, 8, -1, ctypes.byref(h)) == -1        # bad transa
+    assert f(0, 1, 0, 64, 32, 16, 63, 32, 32, -1, ctypes.byref(h)) == -1  # row-major A^T (K x M) needs lda >= M
+    assert f(0, 0, 1, 64, 32, 16, 16, 15, 32, -1, ctypes.byref(h)) == -1  # row-major B^T (N x K) needs ldb >= K
+    assert f(1, 0, 0, 64, 32, 16, 63, 16, 64, -1, ctypes.byref(h)) == -1  # column-major A (M x K) needs lda >= M
+    assert f(1, 0, 0, 64, 32, 16, 64, 16, 63, -1, ctypes.byref(h)) == -1  # column-major C needs ldc >= M
+    assert f(0, 0, 0, -1, 32, 16, 16, 32, 32, -1, ctypes.byref(h)) == -1  # negative M
+    assert f(0, 0, 0, 8, 8, 8, 8, 8, 8, -1, None) == -1                   # no output
+    assert not h.value
+
+
 def test_static_scratch_rejects_before_cuda(lib):
     """sgemm_run_static_scratch checks its arguments before any CUDA call."""
     f = lib.sgemm_run_static_scratch

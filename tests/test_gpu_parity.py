@@ -7,6 +7,8 @@ index inside every edge tile).  Kernels that keep ascending-k order are also
 compared bit for bit against the float32 fused-multiply-add chain when
 alpha = 1 and beta = 0.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -463,3 +465,74 @@ def test_split_tf32_full_size_sample(sg, oracle_mod):
     Cref, S = oracle_mod.sgemm_ref(np.ascontiguousarray(A[rows]), np.ascontiguousarray(B[:, cols]),
                                    np.ascontiguousarray(C0[np.ix_(rows, cols)]), w.alpha, w.beta)
     assert_parity(C[np.ix_(rows, cols)], Cref, S, w.K, f"{TC} square4096 sample")
+
+
+# ---- storage order and transposition (sgemm_plan_ex) --------------------------
+
+def _stored(X, order, trans, pad):
+    """Memory (row-major view) and leading dimension of logical operand X stored
+    as X or X^T (trans) in `order`, each row/column padded by `pad` floats."""
+    S = X.T if trans else X
+    mem = S if order == "row" else S.T  # a column-major matrix is its transpose in row-major memory
+    mem = np.ascontiguousarray(mem, dtype=np.float32)
+    return mem, mem.shape[1] + pad
+
+
+@pytest.mark.parametrize("order", ["row", "col"])
+@pytest.mark.parametrize("ta,tb", [(False, False), (False, True), (True, False), (True, True)])
+@pytest.mark.parametrize("shape,config,pad", [((257, 131, 77), None, 0), ((200, 300, 100), None, 3),
+                                              ((12, 1000, 515), None, 0), ((300, 520, 96), "tf32x3_128x256x32_s2", 1)])
+def test_order_and_transpose(sg, oracle_mod, order, ta, tb, shape, config, pad):
+    M, N, K = shape
+    opA, opB, C0 = make_inputs(M, N, K, seed=M + 2 * N + 3 * K + ta + 2 * tb, dist_a=("normal", 1.0),
+                               dist_b=("normal", 1.0))
+    alpha, beta = 0.75, -1.5
+    Cref, S = oracle_mod.sgemm_ref(opA, opB, C0, alpha, beta)
+    memA, lda = _stored(opA, order, ta, pad)
+    memB, ldb = _stored(opB, order, tb, pad)
+    memC, ldc = _stored(C0, order, False, pad)
+    dA, pA, _ = _to_dev(memA, lda)
+    dB, pB, _ = _to_dev(memB, ldb)
+    dC, pC, _ = _to_dev(memC, ldc)
+    plan = sg.Plan(M, N, K, lda, ldb, ldc, config=config, order=order, transa=ta, transb=tb)
+    info = plan.info()
+    assert info["order"] == order and info["op"] == ("T" if ta else "N") + ("T" if tb else "N")
+    assert info["M"] == M and info["N"] == N
+    plan.run(alpha, pA, pB, beta, pC)
+    torch.cuda.synchronize()
+    assert sg.device_status() == sg.SGEMM_OK
+    out = _from_dev(dC, memC.shape[0], memC.shape[1], ldc)
+    C = out if order == "row" else out.T
+    plan.close()
+    assert_parity(C, Cref, S, K, f"{order} op={info['op']} {shape} {info['variant']}")
+
+
+def test_order_and_transpose_host_buffers(sg, oracle_mod):
+    """sgemm_run_host copies each operand with its stored shape."""
+    M, N, K = 150, 90, 70
+    opA, opB, C0 = make_inputs(M, N, K, seed=31, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
+    Cref, S = oracle_mod.sgemm_ref(opA, opB, C0, 1.0, 2.0)
+    memA, lda = _stored(opA, "col", True, 0)
+    memB, ldb = _stored(opB, "col", False, 0)
+    memC, ldc = _stored(C0, "col", False, 0)
+    plan = sg.Plan(M, N, K, lda, ldb, ldc, order="col", transa=True, transb=False)
+    hA = torch.from_numpy(memA).pin_memory()
+    hB = torch.from_numpy(memB).pin_memory()
+    hC = torch.from_numpy(memC.copy()).pin_memory()
+    dA = torch.empty_like(hA, device="cuda")
+    dB = torch.empty_like(hB, device="cuda")
+    dC = torch.empty_like(hC, device="cuda")
+    plan.run_host(1.0, hA, hB, 2.0, hC, dA, dB, dC)
+    torch.cuda.synchronize()
+    plan.close()
+    assert_parity(hC.numpy().T, Cref, S, K, "col-major TN via host buffers")
+
+
+def test_plan_ex_argument_errors(sg):
+    l = sg.lib()
+    h = ctypes.c_void_p()
+    # row-major A stored K x M needs lda >= M; column-major C needs ldc >= M
+    assert l.sgemm_plan_ex(0, 1, 0, 64, 32, 16, 63, 32, 32, -1, ctypes.byref(h)) == sg.SGEMM_ERR_INVALID_ARG
+    assert l.sgemm_plan_ex(1, 0, 0, 64, 32, 16, 64, 16, 63, -1, ctypes.byref(h)) == sg.SGEMM_ERR_INVALID_ARG
+    assert l.sgemm_plan_ex(2, 0, 0, 64, 32, 16, 64, 16, 64, -1, ctypes.byref(h)) == sg.SGEMM_ERR_INVALID_ARG
+    assert l.sgemm_plan_ex(0, 2, 0, 64, 32, 16, 64, 32, 32, -1, ctypes.byref(h)) == sg.SGEMM_ERR_INVALID_ARG
