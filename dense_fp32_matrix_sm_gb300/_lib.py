@@ -44,6 +44,8 @@ SIGNATURES = {
     "sgemm_selftest_wait_timeout": (_int, [ctypes.c_uint64, _vp]),
     "sgemm_run_static_scratch": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "sgemm_plan_ex": (_int, [_int, _int, _int, _i64, _i64, _i64, _i64, _i64, _i64, _int, ctypes.POINTER(_vp)]),
+    "sgemm_plan_batched": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _int,
+                                  ctypes.POINTER(_vp)]),
 }
 
 _lib = None
@@ -151,7 +153,8 @@ class Plan:
 
     def __init__(self, M: int, N: int, K: int, lda: Optional[int] = None, ldb: Optional[int] = None,
                  ldc: Optional[int] = None, config=None, order: str = "row", transa: bool = False,
-                 transb: bool = False):
+                 transb: bool = False, batch: Optional[int] = None, stride_a: int = 0, stride_b: int = 0,
+                 stride_c: int = 0):
         l = lib()
         self.M, self.N, self.K = int(M), int(N), int(K)
         row = order == "row"
@@ -164,7 +167,13 @@ class Plan:
         self.ldb = int(ldb) if ldb is not None else max(1, b_cols if row else b_rows)
         self.ldc = int(ldc) if ldc is not None else max(1, self.N if row else self.M)
         h = ctypes.c_void_p()
-        if not row or transa or transb:
+        if batch is not None:
+            if not row or transa or transb:
+                raise ValueError("strided batches are row-major and untransposed")
+            cid = -1 if config is None else (config if isinstance(config, int) else config_id(config))
+            st = l.sgemm_plan_batched(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, int(batch), int(stride_a),
+                                      int(stride_b), int(stride_c), cid, ctypes.byref(h))
+        elif not row or transa or transb:
             cid = -1 if config is None else (config if isinstance(config, int) else config_id(config))
             st = l.sgemm_plan_ex(0 if row else 1, 1 if transa else 0, 1 if transb else 0, self.M, self.N, self.K,
                                  self.lda, self.ldb, self.ldc, cid, ctypes.byref(h))

@@ -36,11 +36,15 @@ struct GenericParams {
   int64_t lda, ldb, ldc;
   int M, N, K;
   float alpha, beta;
+  int64_t stride_a, stride_b, stride_c;  // batch z = blockIdx.z
 };
 
-__global__ void __launch_bounds__(kGThreads) sgemm_generic_kernel(const GenericParams p) {
+__global__ void __launch_bounds__(kGThreads) sgemm_generic_kernel(GenericParams p) {
   __shared__ float As[kGBK][kGBM + 1];
   __shared__ float Bs[kGBK][kGBN];
+  p.A += blockIdx.z * p.stride_a;
+  p.B += blockIdx.z * p.stride_b;
+  p.C += blockIdx.z * p.stride_c;
 
   const int tiles_n = (p.N + kGBN - 1) / kGBN;
   const int tm = blockIdx.x / tiles_n;
@@ -117,21 +121,24 @@ cudaError_t generic_occupancy(int* ctas) {
 }
 
 cudaError_t generic_launch(const LaunchArgs& a, cudaStream_t stream) {
-  GenericParams p{a.A, a.B, a.C, a.lda, a.ldb, a.ldc, a.M, a.N, a.K, a.alpha, a.beta};
+  GenericParams p{a.A, a.B, a.C, a.lda, a.ldb, a.ldc, a.M, a.N, a.K, a.alpha, a.beta, a.stride_a, a.stride_b,
+                  a.stride_c};
   const int64_t tiles = static_cast<int64_t>((a.M + kGBM - 1) / kGBM) * ((a.N + kGBN - 1) / kGBN);
-  if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  sgemm_generic_kernel<<<static_cast<unsigned>(tiles), kGThreads, 0, stream>>>(p);
+  const int batch = a.batch > 1 ? a.batch : 1;
+  if (tiles > 0x7fffffff || batch > 65535) return cudaErrorInvalidConfiguration;
+  sgemm_generic_kernel<<<dim3(static_cast<unsigned>(tiles), 1, batch), kGThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 const Variant kGenericVariants[] = {
     Variant{"generic_64x64x16", kKindGeneric, kGBM, kGBN, kGBK, 1, 0, kGThreads, 0, 0, &generic_prepare,
-            &generic_occupancy, &generic_launch},
+            &generic_occupancy, &generic_launch, 0, 0, 1},
 };
 
 // C = beta*C over an M x N window with row stride ldc; beta == 0 writes zeros
 // without reading C.
-__global__ void scale_kernel(float* C, int64_t ldc, int M, int N, float beta) {
+__global__ void scale_kernel(float* C, int64_t ldc, int M, int N, float beta, int64_t stride_c) {
+  C += blockIdx.y * stride_c;  // batch
   const int64_t total = static_cast<int64_t>(M) * N;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -159,12 +166,15 @@ const Variant* generic_variants(int* count) {
   return kGenericVariants;
 }
 
-cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaStream_t stream) {
+cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaStream_t stream, int batch,
+                         int64_t stride_c) {
   const int64_t total = static_cast<int64_t>(M) * N;
   int blocks = static_cast<int>((total + 255) / 256);
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
-  scale_kernel<<<blocks, 256, 0, stream>>>(C, ldc, M, N, beta);
+  if (batch < 1) batch = 1;
+  if (batch > 65535) return cudaErrorInvalidConfiguration;
+  scale_kernel<<<dim3(blocks, batch), 256, 0, stream>>>(C, ldc, M, N, beta, stride_c);
   return cudaGetLastError();
 }
 

@@ -48,6 +48,10 @@ struct LaunchArgs {
   // stored K x M (row-major, lda), b_trans = 1 means B is stored N x K
   int a_trans;
   int b_trans;
+  // strided batch (variants with batched = 1): product z reads A + z*stride_a,
+  // B + z*stride_b and writes C + z*stride_c, z = 0 .. batch-1
+  int batch;
+  int64_t stride_a, stride_b, stride_c;
 };
 
 struct Variant {
@@ -66,6 +70,7 @@ struct Variant {
   cudaError_t (*launch)(const LaunchArgs& args, cudaStream_t stream);
   int persistent;        // few-row kernels: 1 = clusters walk several column slabs
   int streamk;           // 1: the kernel can split its tail tiles along K (workspace per plan)
+  int batched;           // 1: runs strided batches (TMA variants: 3-D tensor maps, batch outermost)
 };
 
 // Variant tables, one per kernel translation unit.
@@ -78,8 +83,10 @@ const Variant* cpa_variants(int* count);
 const Variant* tmat_variants(int* count);
 const Variant* tc_variants(int* count);
 
-// C = beta * C (K == 0 or alpha == 0), any leading dimension.
-cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaStream_t stream);
+// C = beta * C (K == 0 or alpha == 0), any leading dimension; `batch`
+// matrices stride_c apart.
+cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaStream_t stream, int batch = 1,
+                         int64_t stride_c = 0);
 
 // out (cols x rows, ld_out) = in (rows x cols, ld_in) transposed.
 cudaError_t launch_transpose(const float* in, int64_t ld_in, int rows, int cols, float* out, int64_t ld_out,

@@ -22,6 +22,7 @@ using namespace sgemm;
 
 struct sgemm_plan_s {
   int64_t M, N, K, lda, ldb, ldc;
+  int64_t batch, stride_a, stride_b, stride_c;  // strided batch (batch 1: a single product)
   int device;
   int num_sms;
   int config_id;
@@ -142,7 +143,17 @@ sgemm_status_t check_dims(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
   return SGEMM_OK;
 }
 
-bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb) {
+bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                      int64_t batch = 1, int64_t stride_a = 0, int64_t stride_b = 0) {
+  if (batch > 1) {
+    if (!v->batched) return false;
+    if (v->kind == kKindGeneric) return batch <= 65535;
+    // 3-D tensor maps: 16-byte batch strides that do not overlap the matrices,
+    // or 0 for an operand shared by every product
+    if (stride_a % 4 != 0 || stride_b % 4 != 0 || (stride_a != 0 && stride_a < M * lda) ||
+        (stride_b != 0 && stride_b < K * ldb))
+      return false;
+  }
   if (v->kind == kKindGeneric) return true;
   // split-TF32: the split kernels read A and B with plain loads (any layout).
   // The split leaves ~3 * 2^-22 |a b| per product; K >= 16 keeps that well
@@ -160,7 +171,21 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
 
 // The per-shape config table.  Keys are shape classes; values are variant
 // names.  The entries come from the measured sweeps on GB300.
-const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms) {
+const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms, int64_t batch = 1,
+                         int64_t stride_a = 0, int64_t stride_b = 0) {
+  if (batch > 1) {
+    // Strided batches run on the batched variants only: the transposed-A
+    // family when TMA can take the layout (tile counts over the whole batch),
+    // else the scalar-load kernel.
+    if (ldb % 4 != 0 || lda % 4 != 0 || stride_a % 4 != 0 || stride_b % 4 != 0 ||
+        (stride_a != 0 && stride_a < M * lda) || (stride_b != 0 && stride_b < K * ldb))
+      return "generic_64x64x16";
+    const int64_t wide = batch * ((M + 127) / 128) * ((N + 255) / 256);
+    const int64_t square = batch * ((M + 127) / 128) * ((N + 127) / 128);
+    if (wide >= num_sms && K >= 256 && M > 64) return "tmat_128x256x32_s3_b1";
+    if (4 * square >= 3 * static_cast<int64_t>(num_sms) && M > 64) return "tmat_128x128x32_s4_b1";
+    return "tmat_128x64x32_s3_b2";
+  }
   if (ldb % 4 != 0) return "generic_64x64x16";
   if (M <= 16 && lda % 4 == 0) {
     // Few rows: the stream-K form once there are enough (128-column slab,
@@ -192,7 +217,8 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
 }
 
 sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int config_id,
-                         sgemm_plan_t* out) {
+                         sgemm_plan_t* out, int64_t batch = 1, int64_t stride_a = 0, int64_t stride_b = 0,
+                         int64_t stride_c = 0) {
   if (!out) return SGEMM_ERR_INVALID_ARG;
   sgemm_status_t st = check_dims(M, N, K, lda, ldb, ldc);
   if (st != SGEMM_OK) return st;
@@ -210,12 +236,12 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       config_id = find_variant(forced);
       if (config_id < 0) return SGEMM_ERR_INVALID_ARG;
     } else {
-      config_id = find_variant(table_choice(M, N, K, lda, ldb, sms));
+      config_id = find_variant(table_choice(M, N, K, lda, ldb, sms, batch, stride_a, stride_b));
       if (config_id < 0) config_id = reg.first_generic;
     }
   }
   const Variant* v = reg.all[config_id];
-  if (!variant_supports(v, M, N, K, lda, ldb)) return SGEMM_ERR_UNSUPPORTED;
+  if (!variant_supports(v, M, N, K, lda, ldb, batch, stride_a, stride_b)) return SGEMM_ERR_UNSUPPORTED;
   if (v->kind != kKindGeneric && v->tma_swizzle_a >= 0 && !encode_fn()) return SGEMM_ERR_CUDA;
 
   unsigned int* status = nullptr;
@@ -236,12 +262,16 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->lda = lda;
   p->ldb = ldb;
   p->ldc = ldc;
+  p->batch = batch;
+  p->stride_a = stride_a;
+  p->stride_b = stride_b;
+  p->stride_c = stride_c;
   p->device = device;
   p->num_sms = sms;
   p->config_id = config_id;
   p->generic_id = reg.first_generic;
   p->ctas_per_sm = ctas;
-  p->tiles = ((M + v->bm - 1) / v->bm) * ((N + v->bn - 1) / v->bn);
+  p->tiles = ((M + v->bm - 1) / v->bm) * ((N + v->bn - 1) / v->bn) * batch;
   int64_t grid = p->tiles;
   p->split = 1;
   p->dp_waves = 0;
@@ -391,12 +421,18 @@ sgemm_status_t encode_maps(const Variant* v, const sgemm_plan_s* p, const float*
                            LaunchArgs* a) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return SGEMM_ERR_CUDA;
+  // batched variants take 3-D maps, the batch outermost (a single product is a batch of one)
+  const cuuint32_t rank = v->batched && p->batch > 1 ? 3 : 2;
+  // an operand shared by every product (stride 0) is a batch of one
+  const cuuint64_t nb_a = static_cast<cuuint64_t>(p->batch > 1 && p->stride_a != 0 ? p->batch : 1);
+  const cuuint64_t nb_b = static_cast<cuuint64_t>(p->batch > 1 && p->stride_b != 0 ? p->batch : 1);
   if (v->kind != kKindCpa) {  // the transposed-A kernels copy A themselves
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->lda) * 4};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(v->bk), static_cast<cuuint32_t>(v->bm)};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&a->tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides, box, estr,
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->M), nb_a};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p->lda) * 4,
+                                   static_cast<cuuint64_t>(nb_a > 1 ? p->stride_a : p->M * p->lda) * 4};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(v->bk), static_cast<cuuint32_t>(v->bm), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(&a->tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<float*>(A), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
                      v->tma_swizzle_a == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                      : v->tma_swizzle_a == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -405,11 +441,12 @@ sgemm_status_t encode_maps(const Variant* v, const sgemm_plan_s* p, const float*
     if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
   }
   {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->N), static_cast<cuuint64_t>(p->K)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->ldb) * 4};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(v->bn), static_cast<cuuint32_t>(v->bk)};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&a->tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides, box, estr,
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->N), static_cast<cuuint64_t>(p->K), nb_b};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p->ldb) * 4,
+                                   static_cast<cuuint64_t>(nb_b > 1 ? p->stride_b : p->K * p->ldb) * 4};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(v->bn), static_cast<cuuint32_t>(v->bk), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(&a->tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<float*>(B), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
@@ -430,6 +467,18 @@ sgemm_status_t sgemm_plan_with_config(int64_t M, int64_t N, int64_t K, int64_t l
                                       int config_id, sgemm_plan_t* out) {
   if (config_id < 0) return SGEMM_ERR_INVALID_ARG;
   return make_plan(M, N, K, lda, ldb, ldc, config_id, out);
+}
+
+sgemm_status_t sgemm_plan_batched(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                  int64_t batch, int64_t stride_a, int64_t stride_b, int64_t stride_c, int config_id,
+                                  sgemm_plan_t* out) {
+  if (!out) return SGEMM_ERR_INVALID_ARG;
+  if (batch < 0 || stride_a < 0 || stride_b < 0 || stride_c < 0) return SGEMM_ERR_INVALID_ARG;
+  // the products' C matrices must not overlap (A and B may be shared: stride 0)
+  if (batch > 1 && M > 0 && N > 0 && stride_c < (M - 1) * ldc + N) return SGEMM_ERR_INVALID_ARG;
+  if (batch > 65535) return SGEMM_ERR_UNSUPPORTED;
+  if (config_id < -1) return SGEMM_ERR_INVALID_ARG;
+  return make_plan(M, N, K, lda, ldb, ldc, config_id, out, batch, stride_a, stride_b, stride_c);
 }
 
 sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64_t N, int64_t K, int64_t lda,
@@ -493,7 +542,7 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
                          void* stream_) {
   if (!plan) return SGEMM_ERR_INVALID_ARG;
   const sgemm_plan_s* p = plan;
-  if (p->M == 0 || p->N == 0) return SGEMM_OK;
+  if (p->M == 0 || p->N == 0 || p->batch == 0) return SGEMM_OK;
   if (!C) return SGEMM_ERR_INVALID_ARG;
   const bool product = p->K > 0 && alpha != 0.f;
   if (product && (!A || !B)) return SGEMM_ERR_INVALID_ARG;
@@ -503,7 +552,8 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
 
   if (!product) {
-    return launch_scale(C, p->ldc, static_cast<int>(p->M), static_cast<int>(p->N), beta, stream) == cudaSuccess
+    return launch_scale(C, p->ldc, static_cast<int>(p->M), static_cast<int>(p->N), beta, stream,
+                        static_cast<int>(p->batch), p->stride_c) == cudaSuccess
                ? SGEMM_OK
                : SGEMM_ERR_CUDA;
   }
@@ -549,6 +599,10 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   a.beta = beta;
   a.grid = grid;
   a.split_k = v->kind == kKindSkinny ? p->split : 1;
+  a.batch = static_cast<int>(p->batch);
+  a.stride_a = p->stride_a;
+  a.stride_b = p->stride_b;
+  a.stride_c = p->stride_c;
   if (v == reg.all[p->config_id] && p->sk_iters > 0) {
     a.dp_waves = p->dp_waves;
     a.sk_iters = p->sk_iters;
@@ -592,35 +646,41 @@ sgemm_status_t sgemm_run_host(sgemm_plan_t plan, float alpha, const float* hA, c
                               float* hC, float* dA, float* dB, float* dC, void* stream_) {
   if (!plan) return SGEMM_ERR_INVALID_ARG;
   const sgemm_plan_s* p = plan;
-  if (p->M == 0 || p->N == 0) return SGEMM_OK;
+  if (p->M == 0 || p->N == 0 || p->batch == 0) return SGEMM_OK;
   if (!hC || !dC) return SGEMM_ERR_INVALID_ARG;
   const bool product = p->K > 0 && alpha != 0.f;
   if (product && (!hA || !hB || !dA || !dB)) return SGEMM_ERR_INVALID_ARG;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   const size_t fs = sizeof(float);
+  // one 2-D copy per matrix of the batch (a single product is a batch of one)
+  const int64_t nb = p->batch > 1 ? p->batch : 1;
   if (product) {
     // stored shapes in row-major terms (a column-major plan holds them swapped)
     const int64_t ra = p->ex_ta ? p->K : p->M, ca = p->ex_ta ? p->M : p->K;
     const int64_t rb = p->ex_tb ? p->N : p->K, cb = p->ex_tb ? p->K : p->N;
     const int64_t ra_u = p->ex_swap ? rb : ra, ca_u = p->ex_swap ? cb : ca, lda_u = p->ex_swap ? p->ex_ldb : p->ex_lda;
     const int64_t rb_u = p->ex_swap ? ra : rb, cb_u = p->ex_swap ? ca : cb, ldb_u = p->ex_swap ? p->ex_lda : p->ex_ldb;
-    if (cudaMemcpy2DAsync(dA, lda_u * fs, hA, lda_u * fs, ca_u * fs, ra_u, cudaMemcpyHostToDevice, stream) !=
-        cudaSuccess)
-      return SGEMM_ERR_CUDA;
-    if (cudaMemcpy2DAsync(dB, ldb_u * fs, hB, ldb_u * fs, cb_u * fs, rb_u, cudaMemcpyHostToDevice, stream) !=
-        cudaSuccess)
-      return SGEMM_ERR_CUDA;
+    for (int64_t z = 0; z < nb; ++z) {
+      if (cudaMemcpy2DAsync(dA + z * p->stride_a, lda_u * fs, hA + z * p->stride_a, lda_u * fs, ca_u * fs, ra_u,
+                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+      if (cudaMemcpy2DAsync(dB + z * p->stride_b, ldb_u * fs, hB + z * p->stride_b, ldb_u * fs, cb_u * fs, rb_u,
+                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    }
   }
   if (beta != 0.f) {
-    if (cudaMemcpy2DAsync(dC, p->ldc * fs, hC, p->ldc * fs, p->N * fs, p->M, cudaMemcpyHostToDevice, stream) !=
-        cudaSuccess)
-      return SGEMM_ERR_CUDA;
+    for (int64_t z = 0; z < nb; ++z)
+      if (cudaMemcpy2DAsync(dC + z * p->stride_c, p->ldc * fs, hC + z * p->stride_c, p->ldc * fs, p->N * fs, p->M,
+                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
   }
   sgemm_status_t st = sgemm_run(plan, alpha, dA, dB, beta, dC, stream_);
   if (st != SGEMM_OK) return st;
-  if (cudaMemcpy2DAsync(hC, p->ldc * fs, dC, p->ldc * fs, p->N * fs, p->M, cudaMemcpyDeviceToHost, stream) !=
-      cudaSuccess)
-    return SGEMM_ERR_CUDA;
+  for (int64_t z = 0; z < nb; ++z)
+    if (cudaMemcpy2DAsync(hC + z * p->stride_c, p->ldc * fs, dC + z * p->stride_c, p->ldc * fs, p->N * fs, p->M,
+                          cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return SGEMM_ERR_CUDA;
   return SGEMM_OK;
 }
 
@@ -642,7 +702,7 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
   snprintf(buf, n,
            "variant=%s kind=%s tile=%dx%dx%d stages=%d ffma2=%d threads=%d smem=%d grid=%d ctas_per_sm=%d "
            "tiles=%lld sms=%d split=%d streamk=%d dp_waves=%d sk_tiles=%lld k_order=%s M=%lld N=%lld K=%lld "
-           "order=%s op=%c%c",
+           "order=%s op=%c%c batch=%lld",
            v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : v->kind == kKindTc ? "tc" : "skinny", v->bm, v->bn,
            v->bk, v->stages, v->ffma2, v->threads, v->smem_bytes, plan->grid, plan->ctas_per_sm,
            static_cast<long long>(plan->tiles), plan->num_sms, plan->split, plan->sk_iters > 0 ? 1 : 0, plan->dp_waves,
@@ -652,7 +712,8 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
            static_cast<long long>(plan->ex_swap ? plan->N : plan->M),
            static_cast<long long>(plan->ex_swap ? plan->M : plan->N), static_cast<long long>(plan->K),
            plan->ex_order == SGEMM_COL_MAJOR ? "col" : "row",
-           (plan->ex_swap ? plan->ex_tb : plan->ex_ta) ? 'T' : 'N', (plan->ex_swap ? plan->ex_ta : plan->ex_tb) ? 'T' : 'N');
+           (plan->ex_swap ? plan->ex_tb : plan->ex_ta) ? 'T' : 'N', (plan->ex_swap ? plan->ex_ta : plan->ex_tb) ? 'T' : 'N',
+           static_cast<long long>(plan->batch));
   return SGEMM_OK;
 }
 
@@ -660,7 +721,7 @@ sgemm_status_t sgemm_plan_launches(sgemm_plan_t plan, int* out) {
   if (!plan || !out) return SGEMM_ERR_INVALID_ARG;
   // the split-TF32 variants launch two operand-split kernels before the GEMM
   const Variant* v = registry().all[plan->config_id];
-  *out = (plan->M == 0 || plan->N == 0) ? 0 : v->kind == kKindTc && plan->K > 0 ? 3 : 1;
+  *out = (plan->M == 0 || plan->N == 0 || plan->batch == 0) ? 0 : v->kind == kKindTc && plan->K > 0 ? 3 : 1;
   if (*out > 0 && plan->K > 0) *out += (plan->ex_wa ? 1 : 0) + (plan->ex_wb ? 1 : 0);
   return SGEMM_OK;
 }
@@ -753,6 +814,8 @@ sgemm_status_t api_encode_maps(const Variant* v, int64_t M, int64_t N, int64_t K
   shape.K = K;
   shape.lda = lda;
   shape.ldb = ldb;
+  shape.batch = 1;
+  shape.stride_a = shape.stride_b = shape.stride_c = 0;
   return encode_maps(v, &shape, A, B, a);
 }
 

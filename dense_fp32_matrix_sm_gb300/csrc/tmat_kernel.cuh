@@ -73,6 +73,11 @@ struct Params {
   float* ws;             // one partial tile per CTA
   unsigned int* flags;   // flags[b] == epoch: CTA b's partial tile is published
   unsigned int epoch;
+  // strided batch: tiles are numbered batch-outermost; A and B come through
+  // 3-D tensor maps (batch = the third coordinate), C is offset by stride_c
+  int batch;
+  int64_t stride_c;
+  int a_batched, b_batched;  // 0: the operand is shared by every product (read at batch 0)
 };
 
 template <int BM_, int BN, int STAGES>
@@ -96,7 +101,7 @@ struct Shape {
   static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * kAtBytes + STAGES * 8 + 1024;
 };
 
-template <int BM_, int BN, int STAGES, int MINB>
+template <int BM_, int BN, int STAGES, int MINB, bool BATCHED>
 __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
     sgemm_tmat_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const Params p) {
@@ -114,7 +119,18 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   const int lane = threadIdx.x & 31;
   const int tiles_m = (p.M + BM - 1) / BM;
   const int tiles_n = (p.N + BN - 1) / BN;
-  const int num_tiles = tiles_m * tiles_n;
+  const int tiles_per_batch = tiles_m * tiles_n;
+  const int num_tiles = BATCHED ? tiles_per_batch * p.batch : tiles_per_batch;
+  // tile -> (batch z, tile row, tile column), grouped order within a batch
+  auto decode = [&](int tile, int& z, int& tm, int& tn) {
+    if constexpr (BATCHED) {
+      z = tile / tiles_per_batch;
+      tile_coords(tile - z * tiles_per_batch, tiles_m, tiles_n, p.group_m, tm, tn);
+    } else {
+      z = 0;
+      tile_coords(tile, tiles_m, tiles_n, p.group_m, tm, tn);
+    }
+  };
   const int KT = (p.K + BK - 1) / BK;
   // ---- this CTA's schedule: up to two stream-K segments first, then data-parallel tiles ----
   // Stream-K: the k-slices of the tail tiles are numbered x = 0 .. sk_iters-1
@@ -176,20 +192,25 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   if (n_sk > 1) total_it += static_cast<uint32_t>(sk_k1_b - sk_k0_b);
 
   // producer cursor (thread 0): slices are issued in schedule order
-  int c_seg = 0, c_kt = 0, c_k1 = 0, c_tm = 0, c_tn = 0;
+  int c_seg = 0, c_kt = 0, c_k1 = 0, c_tm = 0, c_tn = 0, c_z = 0;
   auto issue = [&](uint32_t j) {
     (void)j;
     if (c_kt == c_k1) {  // enter the next segment
       int tile, k0;
       segment(c_seg++, tile, k0, c_k1);
       c_kt = k0;
-      tile_coords(tile, tiles_m, tiles_n, p.group_m, c_tm, c_tn);
+      decode(tile, c_z, c_tm, c_tn);
     }
     const uint32_t s = j % STAGES;
     const uint32_t dst = smem_base + s * S::kStageBytes;
     ptx::mbar_arrive_expect_tx(bar_full + 8 * s, S::kStageBytes);
-    ptx::tma_load_2d(dst, &tmA, c_kt * BK, c_tm * BM, bar_full + 8 * s);
-    ptx::tma_load_2d(dst + S::kStageA, &tmB, c_tn * BN, c_kt * BK, bar_full + 8 * s);
+    if constexpr (BATCHED) {
+      ptx::tma_load_3d(dst, &tmA, c_kt * BK, c_tm * BM, c_z * p.a_batched, bar_full + 8 * s);
+      ptx::tma_load_3d(dst + S::kStageA, &tmB, c_tn * BN, c_kt * BK, c_z * p.b_batched, bar_full + 8 * s);
+    } else {
+      ptx::tma_load_2d(dst, &tmA, c_kt * BK, c_tm * BM, bar_full + 8 * s);
+      ptx::tma_load_2d(dst + S::kStageA, &tmB, c_tn * BN, c_kt * BK, bar_full + 8 * s);
+    }
     ++c_kt;
   };
 
@@ -245,8 +266,9 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   for (int seg = 0; seg < nseg && !failed; ++seg) {
     int tile, seg_k0, seg_k1;
     segment(seg, tile, seg_k0, seg_k1);
-    int tm, tn;
-    tile_coords(tile, tiles_m, tiles_n, p.group_m, tm, tn);
+    int tz, tm, tn;
+    decode(tile, tz, tm, tn);
+    float* const Cz = BATCHED ? p.C + tz * p.stride_c : p.C;
 
     // acc[i][j] = {C[row 16i+2g][col j], C[row 16i+2g+1][col j]}, col j = 4c + 16(j/4) + j%4
     float2 acc[4][8];
@@ -343,7 +365,7 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
       for (int e = 0; e < 2; ++e) {
         const int row = tm * BM + wm * 64 + 16 * i + 2 * g + e;
         if (row >= p.M) continue;
-        float* crow = p.C + static_cast<int64_t>(row) * p.ldc;
+        float* crow = Cz + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int col = tn * BN + wn * 32 + 4 * c + 16 * h;
@@ -379,9 +401,14 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
 template <int BM_, int BN, int STAGES, int MINB>
 struct Variant_ {
   using S = Shape<BM_, BN, STAGES>;
-  static constexpr auto kernel = sgemm_tmat_kernel<BM_, BN, STAGES, MINB>;
+  // a single product runs the plain 2-D kernel; strided batches their own instantiation
+  static constexpr auto kernel = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, false>;
+  static constexpr auto kernel_batched = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, true>;
   static cudaError_t prepare() {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    return e != cudaSuccess ? e
+                            : cudaFuncSetAttribute(kernel_batched, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   S::kSmemBytes);
   }
   static cudaError_t occupancy(int* ctas) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kernel, S::kThreads, S::kSmemBytes);
@@ -395,7 +422,8 @@ struct Variant_ {
     p.K = a.K;
     p.alpha = a.alpha;
     p.beta = a.beta;
-    p.vec_c = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && (a.ldc % 4 == 0);
+    p.vec_c = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && (a.ldc % 4 == 0) &&
+              (a.batch <= 1 || a.stride_c % 4 == 0);
     p.group_m = 8;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
@@ -404,12 +432,20 @@ struct Variant_ {
     p.ws = a.ws;
     p.flags = a.flags;
     p.epoch = a.epoch;
-    kernel<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    p.batch = a.batch > 1 ? a.batch : 1;
+    p.stride_c = a.stride_c;
+    p.a_batched = a.batch > 1 && a.stride_a != 0;
+    p.b_batched = a.batch > 1 && a.stride_b != 0;
+    if (p.batch > 1) {
+      kernel_batched<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    } else {
+      kernel<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    }
     return cudaGetLastError();
   }
   static Variant describe(const char* name) {
     return Variant{name, kKindTma, S::BM, BN, S::BK, STAGES, 1, S::kThreads, S::kSmemBytes, 128,
-                   &prepare, &occupancy, &launch, 0, 1};
+                   &prepare, &occupancy, &launch, 0, 1, 1};
   }
 };
 

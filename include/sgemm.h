@@ -107,6 +107,39 @@ sgemm_status_t sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
 sgemm_status_t sgemm_plan_with_config(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                       int64_t ldc, int config_id, sgemm_plan_t *out);
 
+/*
+ * Plan a strided batch of `batch` independent products of one shape:
+ * C_z = alpha * A_z * B_z + beta * C_z, z = 0 .. batch-1, with
+ * A_z = A + z*stride_a, B_z = B + z*stride_b, C_z = C + z*stride_c (in floats),
+ * all row-major with the leading dimensions of sgemm_plan. Run it with
+ * sgemm_run (or sgemm_run_host) on the base pointers.
+ *
+ * Argument rules:
+ *   - A and B may be shared between products (stride 0).
+ *   - The C matrices must not overlap: stride_c >= (M-1)*ldc + N when
+ *     batch > 1, else SGEMM_ERR_INVALID_ARG.
+ *   - batch == 0 is a valid empty plan.
+ *   - batch > 65535 gives SGEMM_ERR_UNSUPPORTED.
+ *   - config_id: -1 for the table, else a variant id. Variants that do not
+ *     run batches refuse batch > 1 with SGEMM_ERR_UNSUPPORTED.
+ *
+ * How it runs:
+ *   - Every product of the batch runs in one launch.
+ *   - Transposed-A kernels: 3-D tensor maps, batch outermost. They need
+ *     stride_a and stride_b to be multiples of 4 that either do not overlap
+ *     the matrices or are 0 (one operand shared by every product); their
+ *     grid and stream-K tail span the whole batch.
+ *   - Otherwise the scalar-load kernel runs, the batch on its third grid
+ *     dimension.
+ *
+ * The pages do not batch; this is the BLAS-style strided batch. Many small
+ * products, one per attention head for instance, are the motivating case in
+ * "How a Matmul Kernel Gets Fast", "What this means for real workloads".
+ */
+sgemm_status_t sgemm_plan_batched(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                  int64_t batch, int64_t stride_a, int64_t stride_b, int64_t stride_c, int config_id,
+                                  sgemm_plan_t *out);
+
 /* Storage order and operand transposition for sgemm_plan_ex. */
 enum { SGEMM_ROW_MAJOR = 0, SGEMM_COL_MAJOR = 1 };
 enum { SGEMM_NO_TRANS = 0, SGEMM_TRANS = 1 };

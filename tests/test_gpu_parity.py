@@ -536,3 +536,63 @@ def test_plan_ex_argument_errors(sg):
     assert l.sgemm_plan_ex(1, 0, 0, 64, 32, 16, 64, 16, 63, -1, ctypes.byref(h)) == sg.SGEMM_ERR_INVALID_ARG
     assert l.sgemm_plan_ex(2, 0, 0, 64, 32, 16, 64, 16, 64, -1, ctypes.byref(h)) == sg.SGEMM_ERR_INVALID_ARG
     assert l.sgemm_plan_ex(0, 2, 0, 64, 32, 16, 64, 32, 32, -1, ctypes.byref(h)) == sg.SGEMM_ERR_INVALID_ARG
+
+
+# ---- strided batches (sgemm_plan_batched) -------------------------------------
+
+@pytest.mark.parametrize("case", [
+    # (M, N, K, batch, config, shared A?)  None = the table's choice
+    (96, 80, 72, 7, None, False),                       # small products: 128 x 64 tiles over the batch
+    (300, 520, 260, 3, None, False),                    # ragged tiles in every product
+    (640, 1024, 256, 9, "tmat_128x256x32_s3_b1", False),  # 180 tiles: a stream-K tail over batches 7 and 8
+    (640, 768, 256, 4, "tmat_128x128x32_s4_b1", True),  # A shared by every product (stride 0)
+    (65, 33, 17, 9, "generic_64x64x16", False),
+])
+def test_strided_batch(sg, oracle_mod, case):
+    M, N, K, batch, config, shared_a = case
+    rng = np.random.default_rng(M * N + K + batch)
+    A = rng.standard_normal((1 if shared_a else batch, M, K), dtype=np.float32)
+    B = rng.standard_normal((batch, K, N), dtype=np.float32)
+    C0 = rng.uniform(-1, 1, (batch, M, N)).astype(np.float32)
+    alpha, beta = 1.25, 0.5
+    # strides padded past the matrices (16-byte multiples), A shared when stride_a = 0
+    sa = 0 if shared_a else M * K + 8
+    sb, sc = K * N + 4, M * N + 12
+    dA = torch.zeros(max(1, (0 if shared_a else batch - 1) * sa + M * K), device="cuda")
+    dB = torch.zeros((batch - 1) * sb + K * N, device="cuda")
+    dC = torch.zeros((batch - 1) * sc + M * N, device="cuda")
+    for z in range(batch):
+        if not shared_a or z == 0:
+            dA[z * sa: z * sa + M * K] = torch.from_numpy(A[z].ravel())
+        dB[z * sb: z * sb + K * N] = torch.from_numpy(B[z].ravel())
+        dC[z * sc: z * sc + M * N] = torch.from_numpy(C0[z].ravel())
+    plan = sg.Plan(M, N, K, config=config, batch=batch, stride_a=sa, stride_b=sb, stride_c=sc)
+    info = plan.info()
+    assert info["batch"] == batch
+    plan.run(alpha, dA, dB, beta, dC)
+    torch.cuda.synchronize()
+    assert sg.device_status() == sg.SGEMM_OK
+    out = dC.cpu().numpy()
+    for z in range(batch):
+        Cref, S = oracle_mod.sgemm_ref(A[0 if shared_a else z], B[z], C0[z], alpha, beta)
+        Cz = out[z * sc: z * sc + M * N].reshape(M, N)
+        assert_parity(Cz, Cref, S, K, f"batch {z}/{batch} {info['variant']} {M}x{N}x{K}")
+        # the padding between products is untouched
+        if z + 1 < batch:
+            assert np.all(out[z * sc + M * N: (z + 1) * sc] == 0.0)
+    plan.close()
+
+
+def test_strided_batch_argument_errors(sg):
+    l = sg.lib()
+    h = ctypes.c_void_p()
+    f = l.sgemm_plan_batched
+    assert f(64, 64, 64, 64, 64, 64, 2, 4096, 4096, 4095, -1, ctypes.byref(h)) == sg.SGEMM_ERR_INVALID_ARG  # C overlap
+    assert f(64, 64, 64, 64, 64, 64, -1, 4096, 4096, 4096, -1, ctypes.byref(h)) == sg.SGEMM_ERR_INVALID_ARG
+    assert f(64, 64, 64, 64, 64, 64, 70000, 4096, 4096, 4096, -1, ctypes.byref(h)) == sg.SGEMM_ERR_UNSUPPORTED
+    skinny = sg.config_id("skinny_16x128x32_w4_s3_b3_ef_pa")
+    assert f(16, 256, 64, 64, 256, 256, 2, 1024, 16384, 4096, skinny, ctypes.byref(h)) == sg.SGEMM_ERR_UNSUPPORTED
+    empty = sg.Plan(64, 64, 64, batch=0)
+    assert empty.launches == 0
+    empty.run(1.0, 0, 0, 0.0, 0)  # nothing to do
+    empty.close()
