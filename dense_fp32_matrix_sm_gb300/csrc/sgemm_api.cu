@@ -169,6 +169,25 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
   return true;
 }
 
+// Tile width for the transposed-A family, over `batch` products of M x N x K.
+// Measured on GB300 with the stream-K tail (which removes most of the
+// partial-wave loss once there is at least one full wave):
+//  * 128 x 256 tiles from one full wave of them on, with K >= 256 (eight or
+//    more k-slices per tile, the stream-K threshold): 63.7-66.6 TFLOP/s from
+//    2560^3 up, 2-4% above 128 x 128;
+//  * 128 x 128 tiles down to three quarters of a wave (1536^3: 56.5 vs 54.4
+//    for 128 x 64);
+//  * below that, 128 x 64 tiles two to an SM (1024^3: 36.1 vs 24.4);
+//  * never a tile more than twice as wide as N: 64 x (512 x 64 x 512) ran
+//    14.5 TFLOP/s on 256-wide tiles, three quarters of each tile empty.
+const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms) {
+  const int64_t wide_tiles = batch * ((M + 127) / 128) * ((N + 255) / 256);
+  const int64_t square_tiles = batch * ((M + 127) / 128) * ((N + 127) / 128);
+  if (N > 128 && wide_tiles >= num_sms && K >= 256) return "tmat_128x256x32_s3_b1";
+  if (N > 64 && 4 * square_tiles >= 3 * static_cast<int64_t>(num_sms)) return "tmat_128x128x32_s4_b1";
+  return "tmat_128x64x32_s3_b2";
+}
+
 // The per-shape config table.  Keys are shape classes; values are variant
 // names.  The entries come from the measured sweeps on GB300.
 const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms, int64_t batch = 1,
@@ -180,11 +199,7 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     if (ldb % 4 != 0 || lda % 4 != 0 || stride_a % 4 != 0 || stride_b % 4 != 0 ||
         (stride_a != 0 && stride_a < M * lda) || (stride_b != 0 && stride_b < K * ldb))
       return "generic_64x64x16";
-    const int64_t wide = batch * ((M + 127) / 128) * ((N + 255) / 256);
-    const int64_t square = batch * ((M + 127) / 128) * ((N + 127) / 128);
-    if (wide >= num_sms && K >= 256 && M > 64) return "tmat_128x256x32_s3_b1";
-    if (4 * square >= 3 * static_cast<int64_t>(num_sms) && M > 64) return "tmat_128x128x32_s4_b1";
-    return "tmat_128x64x32_s3_b2";
+    return tmat_choice(M, N, K, batch, num_sms);
   }
   if (ldb % 4 != 0) return "generic_64x64x16";
   if (M <= 16 && lda % 4 == 0) {
@@ -201,19 +216,7 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   }
   if (lda % 4 != 0) return "cpa_128x128x32_s3_k8_b2";  // A copied 4 bytes at a time: any lda
   if (M * N <= 256 * 256) return "tma_128x64x32_w64x32_s3_quad_b3";
-  // Measured on GB300 with the stream-K tail (which removes most of the
-  // partial-wave loss once there is at least one full wave):
-  //  * 128 x 256 tiles from one full wave of them on, with K >= 256 (eight
-  //    or more k-slices per tile, the stream-K threshold): 63.7-66.6 TFLOP/s
-  //    from 2560^3 up, 2-4% above 128 x 128;
-  //  * 128 x 128 tiles down to three quarters of a wave (1536^3: 56.5 vs
-  //    54.4 for 128 x 64);
-  //  * below that, 128 x 64 tiles two to an SM (1024^3: 36.1 vs 24.4).
-  const int64_t wide_tiles = ((M + 127) / 128) * ((N + 255) / 256);
-  const int64_t square_tiles = ((M + 127) / 128) * ((N + 127) / 128);
-  if (wide_tiles >= num_sms && K >= 256) return "tmat_128x256x32_s3_b1";
-  if (4 * square_tiles >= 3 * static_cast<int64_t>(num_sms)) return "tmat_128x128x32_s4_b1";
-  return "tmat_128x64x32_s3_b2";
+  return tmat_choice(M, N, K, 1, num_sms);
 }
 
 sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int config_id,
