@@ -41,17 +41,25 @@ namespace sgemm {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 32;  // one 128-byte swizzle row of float32
-constexpr int STAGES = 2;
 constexpr int kTileA = BM * BK * 4;  // 16 KB
-constexpr int kTileB = BN * BK * 4;  // 32 KB
-constexpr int kStageBytes = 2 * kTileA + 2 * kTileB;
 constexpr int kBarBytes = 256;
-constexpr int kSmemBytes = STAGES * kStageBytes + kBarBytes + 1024;
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;
-static_assert(kTileA % 1024 == 0 && kTileB % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+
+// Tile width BN (the MMA's N and the TMEM columns) and ring depth.
+template <int BN, int STAGES>
+struct TcShape {
+  static constexpr int kTileB = BN * BK * 4;
+  static constexpr int kStageBytes = 2 * kTileA + 2 * kTileB;
+  static constexpr int kSmemBytes = STAGES * kStageBytes + kBarBytes + 1024;
+  static constexpr uint32_t kTmemCols = BN;
+  // D float32, A and B TF32, both K-major, M = 128, N = BN
+  static constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                     (static_cast<uint32_t>(BM >> 4) << 24);
+  static_assert(BN == 128 || BN == 256, "UMMA N of 128 or 256");
+  static_assert(kTileA % 1024 == 0 && kTileB % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
 
 struct TcParams {
   float* C;
@@ -59,6 +67,7 @@ struct TcParams {
   int M, N, K;
   float alpha, beta;
   int group_m;
+  int vec_c;  // C 16-byte aligned with ldc % 4 == 0: float4 epilogue
   unsigned int* status;
   uint64_t timeout_ns;
 };
@@ -69,18 +78,57 @@ __device__ __forceinline__ float to_tf32(float x) {
   return __uint_as_float(r);
 }
 
-// Rows of X (rows x cols, ldx) -> hi, lo (rows x cols, ldh).
+// Rows of X (rows x cols, ldx) -> hi, lo (rows x cols, ldh).  Block row
+// blockIdx.y covers rows blockIdx.y, + gridDim.y, ...; blockIdx.x a span of
+// 4 * blockDim.x columns, read and written as float4 when VEC (X 16-byte
+// aligned, ldx and cols multiples of 4; ldh always is).
+template <bool VEC>
 __global__ void split_rows_kernel(const float* __restrict__ X, int64_t ldx, int rows, int cols, float* __restrict__ hi,
                                   float* __restrict__ lo, int64_t ldh) {
-  const int64_t total = static_cast<int64_t>(rows) * cols;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / cols;
-    const int64_t c = i - r * cols;
-    const float x = X[r * ldx + c];
-    const float h = to_tf32(x);
-    hi[r * ldh + c] = h;
-    lo[r * ldh + c] = to_tf32(x - h);
+  const int c = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (c >= cols) return;
+  for (int r = blockIdx.y; r < rows; r += gridDim.y) {
+    const float* x = X + static_cast<int64_t>(r) * ldx + c;
+    float v[4];
+    if constexpr (VEC) {
+      const float4 q = __ldcs(reinterpret_cast<const float4*>(x));
+      v[0] = q.x, v[1] = q.y, v[2] = q.z, v[3] = q.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = c + j < cols ? x[j] : 0.f;
+    }
+    float h[4], l[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      h[j] = to_tf32(v[j]);
+      l[j] = to_tf32(v[j] - h[j]);
+    }
+    float* ho = hi + static_cast<int64_t>(r) * ldh + c;
+    float* lo_ = lo + static_cast<int64_t>(r) * ldh + c;
+    if constexpr (VEC) {
+      *reinterpret_cast<float4*>(ho) = make_float4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<float4*>(lo_) = make_float4(l[0], l[1], l[2], l[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (c + j < cols) {
+          ho[j] = h[j];
+          lo_[j] = l[j];
+        }
+    }
+  }
+}
+
+void launch_split_rows(const float* X, int64_t ldx, int rows, int cols, float* hi, float* lo, int64_t ldh,
+                       cudaStream_t stream) {
+  const int threads = 128;
+  const int gx = (cols + 4 * threads - 1) / (4 * threads);
+  const int gy = rows < 4096 ? rows : 4096;
+  const bool vec = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && ldx % 4 == 0 && cols % 4 == 0;
+  if (vec) {
+    split_rows_kernel<true><<<dim3(gx, gy), threads, 0, stream>>>(X, ldx, rows, cols, hi, lo, ldh);
+  } else {
+    split_rows_kernel<false><<<dim3(gx, gy), threads, 0, stream>>>(X, ldx, rows, cols, hi, lo, ldh);
   }
 }
 
@@ -117,15 +165,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor: D float32, A and B TF32, both K-major, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
-
-__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -150,10 +195,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     tf32x3_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
                   const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
                   const TcParams p) {
+  using S = TcShape<BN, STAGES>;
+  constexpr int kTileB = S::kTileB;
+  constexpr int kStageBytes = S::kStageBytes;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_base = ptx::smem_addr(smem_raw);
   unsigned char* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
@@ -186,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(ptx::smem_addr(tmem_slot)),
-                 "r"(kTmemCols)
+                 "r"(S::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -232,9 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t al = smem_desc_sw128(st + kTileA + 32 * kk);
         const uint64_t bh = smem_desc_sw128(st + 2 * kTileA + 32 * kk);
         const uint64_t bl = smem_desc_sw128(st + 2 * kTileA + kTileB + 32 * kk);
-        mma_tf32(tmem, al, bh, (kb | kk) != 0 ? 1u : 0u);
-        mma_tf32(tmem, ah, bl, 1u);
-        mma_tf32(tmem, ah, bh, 1u);
+        mma_tf32(tmem, al, bh, S::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+        mma_tf32(tmem, ah, bl, S::kIdesc, 1u);
+        mma_tf32(tmem, ah, bh, S::kIdesc, 1u);
       }
       mma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
     }
@@ -253,12 +302,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok || row >= p.M) continue;
       float* crow = p.C + static_cast<int64_t>(row) * p.ldc;
       const int col0 = tn * BN + cc;
+      if (p.vec_c && col0 + 32 <= p.N) {  // this thread's 32 columns as eight float4
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int col = col0 + j;
-        if (col < p.N) {
-          const float v = __uint_as_float(r[j]);
-          crow[col] = p.beta == 0.f ? p.alpha * v : fmaf(p.alpha, v, p.beta * crow[col]);
+        for (int j = 0; j < 32; j += 4) {
+          float4* d = reinterpret_cast<float4*>(crow + col0 + j);
+          const float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                       __uint_as_float(r[j + 3]));
+          if (p.beta == 0.f) {
+            *d = make_float4(p.alpha * v.x, p.alpha * v.y, p.alpha * v.z, p.alpha * v.w);
+          } else {
+            const float4 o = *d;
+            *d = make_float4(fmaf(p.alpha, v.x, p.beta * o.x), fmaf(p.alpha, v.y, p.beta * o.y),
+                             fmaf(p.alpha, v.z, p.beta * o.z), fmaf(p.alpha, v.w, p.beta * o.w));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int col = col0 + j;
+          if (col < p.N) {
+            const float v = __uint_as_float(r[j]);
+            crow[col] = p.beta == 0.f ? p.alpha * v : fmaf(p.alpha, v, p.beta * crow[col]);
+          }
         }
       }
     }
@@ -267,58 +332,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(S::kTmemCols) : "memory");
   }
 }
 
-cudaError_t prepare() {
-  return cudaFuncSetAttribute(tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-}
-
-cudaError_t occupancy(int* ctas) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, tf32x3_kernel, kThreads, kSmemBytes);
-}
-
-// a.split: A_hi, A_lo (M x kp), then B_hi, B_lo transposed (N x kp); the
-// tensor maps in a (tmA, tmA2, tmB, tmB2) describe those four buffers.
-cudaError_t launch(const LaunchArgs& a, cudaStream_t stream) {
+// Operand split for one run: A_hi, A_lo (M x kp), then B_hi, B_lo (N x kp),
+// both K-major, in a.split; the tensor maps in a (tmA, tmA2, tmB, tmB2)
+// describe those four buffers.
+void launch_split(const LaunchArgs& a, cudaStream_t stream) {
   const int64_t kp = a.split_ld;
   float* ah = a.split;
   float* al = ah + static_cast<int64_t>(a.M) * kp;
   float* bh = al + static_cast<int64_t>(a.M) * kp;
   float* bl = bh + static_cast<int64_t>(a.N) * kp;
   // both operands end K-major: A as M x kp, B as N x kp
-  auto rows_grid = [](int64_t n) { return static_cast<int>((n + 255) / 256 < 152 * 16 ? (n + 255) / 256 : 152 * 16); };
   if (a.a_trans) {  // A stored K x M
     split_transpose_kernel<<<dim3((a.M + 31) / 32, (a.K + 31) / 32), dim3(32, 8), 0, stream>>>(a.A, a.lda, a.K, a.M,
                                                                                             ah, al, kp);
   } else {
-    split_rows_kernel<<<rows_grid(static_cast<int64_t>(a.M) * a.K), 256, 0, stream>>>(a.A, a.lda, a.M, a.K, ah, al, kp);
+    launch_split_rows(a.A, a.lda, a.M, a.K, ah, al, kp, stream);
   }
   if (a.b_trans) {  // B stored N x K: already K-major
-    split_rows_kernel<<<rows_grid(static_cast<int64_t>(a.N) * a.K), 256, 0, stream>>>(a.B, a.ldb, a.N, a.K, bh, bl, kp);
+    launch_split_rows(a.B, a.ldb, a.N, a.K, bh, bl, kp, stream);
   } else {
     split_transpose_kernel<<<dim3((a.N + 31) / 32, (a.K + 31) / 32), dim3(32, 8), 0, stream>>>(a.B, a.ldb, a.K, a.N,
                                                                                             bh, bl, kp);
   }
-  TcParams p;
-  p.C = a.C;
-  p.ldc = a.ldc;
-  p.M = a.M;
-  p.N = a.N;
-  p.K = a.K;
-  p.alpha = a.alpha;
-  p.beta = a.beta;
-  p.group_m = 8;
-  p.status = a.status;
-  p.timeout_ns = a.timeout_ns;
-  tf32x3_kernel<<<a.grid, kThreads, kSmemBytes, stream>>>(a.tmA, a.tmA2, a.tmB, a.tmB2, p);
-  return cudaGetLastError();
 }
 
+template <int BN, int STAGES>
+struct TcVariant {
+  using S = TcShape<BN, STAGES>;
+  static constexpr auto kernel = tf32x3_kernel<BN, STAGES>;
+  static cudaError_t prepare() {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  }
+  static cudaError_t occupancy(int* ctas) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kernel, kThreads, S::kSmemBytes);
+  }
+  static cudaError_t launch(const LaunchArgs& a, cudaStream_t stream) {
+    launch_split(a, stream);
+    TcParams p;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    p.group_m = 8;
+    p.vec_c = (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 4 == 0;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    kernel<<<a.grid, kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmA2, a.tmB, a.tmB2, p);
+    return cudaGetLastError();
+  }
+  static Variant describe(const char* name) {
+    return Variant{name, kKindTc, BM, BN, BK, STAGES, 0, kThreads, S::kSmemBytes, 128, &prepare, &occupancy,
+                   &launch, 0, 0};
+  }
+};
+
 const Variant kVariants[] = {
-    Variant{"tf32x3_128x256x32_s2", kKindTc, BM, BN, BK, STAGES, 0, kThreads, kSmemBytes, 128, &prepare, &occupancy,
-            &launch, 0, 0},
+    TcVariant<256, 2>::describe("tf32x3_128x256x32_s2"),
+    TcVariant<128, 3>::describe("tf32x3_128x128x32_s3"),
 };
 
 }  // namespace tc
