@@ -596,3 +596,30 @@ def test_strided_batch_argument_errors(sg):
     assert empty.launches == 0
     empty.run(1.0, 0, 0, 0.0, 0)  # nothing to do
     empty.close()
+
+
+# ---- a C of more than 2^31 elements: 64-bit offsets in every epilogue ---------
+
+@pytest.mark.parametrize("config,off_a", [(None, 0), ("generic_64x64x16", 1), ("tf32x3_128x128x32_s3", 0)])
+def test_c_beyond_2_31_elements(sg, oracle_mod, config, off_a):
+    M, N, K = 65536 + 17, 32768 + 9, 40
+    assert M * N > 2 ** 31
+    rng = np.random.default_rng(17)  # A and B only: a host C0 of this size is not needed (beta = 0)
+    A = rng.standard_normal((M, K), dtype=np.float32)
+    B = rng.standard_normal((K, N), dtype=np.float32)
+    ldb = N + 3  # 16-byte rows for the TMA-fed kernels
+    dA, pA, lda = _to_dev(A, None, off_a)
+    dB, pB, _ = _to_dev(B, ldb)
+    dC = torch.full((M, N), float("nan"), device="cuda")  # beta = 0: every entry must be written
+    plan = sg.Plan(M, N, K, lda, ldb, N, config=config)
+    plan.run(1.0, pA, pB, 0.0, dC)
+    torch.cuda.synchronize()
+    assert sg.device_status() == sg.SGEMM_OK
+    used = plan.config_name
+    plan.close()
+    rows = np.array([0, 1, 2 ** 31 // N - 1, 2 ** 31 // N, 2 ** 31 // N + 1, M - 2, M - 1])
+    assert (rows * N).max() > 2 ** 31
+    Cs = dC[torch.from_numpy(rows).cuda()].cpu().numpy()
+    del dC
+    Cref, S = oracle_mod.sgemm_ref(np.ascontiguousarray(A[rows]), B, None, 1.0, 0.0)
+    assert_parity(Cs, Cref, S, K, f"{used} rows {rows.tolist()} of {M}x{N}")
