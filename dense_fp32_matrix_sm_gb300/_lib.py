@@ -44,6 +44,9 @@ SIGNATURES = {
     "sgemm_selftest_wait_timeout": (_int, [ctypes.c_uint64, _vp]),
     "sgemm_run_static_scratch": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "sgemm_plan_ex": (_int, [_int, _int, _int, _i64, _i64, _i64, _i64, _i64, _i64, _int, ctypes.POINTER(_vp)]),
+    "sgemm_run_host_pipelined": (_int, [_vp, _int, _f32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _f32,
+                                        ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                        ctypes.POINTER(_vp), _vp]),
     "sgemm_plan_batched": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _int,
                                   ctypes.POINTER(_vp)]),
 }
@@ -199,6 +202,15 @@ class Plan:
         """Host buffers in, host result out: H2D copies, the kernel, D2H copy, all on `stream`."""
         _check(lib().sgemm_run_host(self._h, float(alpha), _ptr(hA), _ptr(hB), float(beta), _ptr(hC),
                                     _ptr(dA), _ptr(dB), _ptr(dC), _stream_handle(stream)), "sgemm_run_host")
+
+    def run_host_pipelined(self, alpha: float, hA, hB, beta: float, hC, dA2, dB2, dC2, stream=None) -> None:
+        """len(hC) products from host buffers through two device buffer sets (dA2, dB2, dC2: pairs),
+        copies overlapped with the kernels; all results are in host memory once `stream` gets there."""
+        n = len(hC)
+        arr = lambda xs: (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+        _check(lib().sgemm_run_host_pipelined(self._h, n, float(alpha), arr(hA), arr(hB), float(beta), arr(hC),
+                                              arr(dA2), arr(dB2), arr(dC2), _stream_handle(stream)),
+               "sgemm_run_host_pipelined")
 
     def describe(self) -> str:
         buf = ctypes.create_string_buffer(512)

@@ -53,6 +53,12 @@ struct sgemm_plan_s {
   int64_t ex_lda, ex_ldb;
   float* ex_wa;
   float* ex_wb;
+  // sgemm_run_host_pipelined: copy streams (host to device, device to host)
+  // and, per buffer set b, events loaded / computed / stored; made on first use
+  std::mutex pipe_mutex;
+  bool pipe_ready;
+  cudaStream_t pipe_h2d, pipe_d2h;
+  cudaEvent_t pipe_ev[2][3];
 };
 
 // Per-device status word written by kernels (timeouts).  Its device address
@@ -291,6 +297,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->ex_ldb = ldb;
   p->ex_wa = nullptr;
   p->ex_wb = nullptr;
+  p->pipe_ready = false;
   if (v->kind == kKindTma || v->kind == kKindCpa) {
     const int64_t slots = static_cast<int64_t>(sms) * ctas;
     if (grid > slots) grid = slots;
@@ -454,6 +461,47 @@ sgemm_status_t encode_maps(const Variant* v, const sgemm_plan_s* p, const float*
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
   }
+  return SGEMM_OK;
+}
+
+// Host-to-device copies of one product's inputs (A and B when there is a
+// product, C when beta != 0) with their stored shapes, one 2-D copy per
+// matrix of a batch; and the device-to-host copy of its result.
+sgemm_status_t copy_inputs(const sgemm_plan_s* p, bool product, float beta, const float* hA, const float* hB,
+                           const float* hC, float* dA, float* dB, float* dC, cudaStream_t stream) {
+  const size_t fs = sizeof(float);
+  const int64_t nb = p->batch > 1 ? p->batch : 1;
+  if (product) {
+    // stored shapes in row-major terms (a column-major plan holds them swapped)
+    const int64_t ra = p->ex_ta ? p->K : p->M, ca = p->ex_ta ? p->M : p->K;
+    const int64_t rb = p->ex_tb ? p->N : p->K, cb = p->ex_tb ? p->K : p->N;
+    const int64_t ra_u = p->ex_swap ? rb : ra, ca_u = p->ex_swap ? cb : ca, lda_u = p->ex_swap ? p->ex_ldb : p->ex_lda;
+    const int64_t rb_u = p->ex_swap ? ra : rb, cb_u = p->ex_swap ? ca : cb, ldb_u = p->ex_swap ? p->ex_lda : p->ex_ldb;
+    for (int64_t z = 0; z < nb; ++z) {
+      if (cudaMemcpy2DAsync(dA + z * p->stride_a, lda_u * fs, hA + z * p->stride_a, lda_u * fs, ca_u * fs, ra_u,
+                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+      if (cudaMemcpy2DAsync(dB + z * p->stride_b, ldb_u * fs, hB + z * p->stride_b, ldb_u * fs, cb_u * fs, rb_u,
+                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    }
+  }
+  if (beta != 0.f) {
+    for (int64_t z = 0; z < nb; ++z)
+      if (cudaMemcpy2DAsync(dC + z * p->stride_c, p->ldc * fs, hC + z * p->stride_c, p->ldc * fs, p->N * fs, p->M,
+                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+  }
+  return SGEMM_OK;
+}
+
+sgemm_status_t copy_output(const sgemm_plan_s* p, float* hC, const float* dC, cudaStream_t stream) {
+  const size_t fs = sizeof(float);
+  const int64_t nb = p->batch > 1 ? p->batch : 1;
+  for (int64_t z = 0; z < nb; ++z)
+    if (cudaMemcpy2DAsync(hC + z * p->stride_c, p->ldc * fs, dC + z * p->stride_c, p->ldc * fs, p->N * fs, p->M,
+                          cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return SGEMM_ERR_CUDA;
   return SGEMM_OK;
 }
 
@@ -654,36 +702,74 @@ sgemm_status_t sgemm_run_host(sgemm_plan_t plan, float alpha, const float* hA, c
   const bool product = p->K > 0 && alpha != 0.f;
   if (product && (!hA || !hB || !dA || !dB)) return SGEMM_ERR_INVALID_ARG;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  const size_t fs = sizeof(float);
-  // one 2-D copy per matrix of the batch (a single product is a batch of one)
-  const int64_t nb = p->batch > 1 ? p->batch : 1;
-  if (product) {
-    // stored shapes in row-major terms (a column-major plan holds them swapped)
-    const int64_t ra = p->ex_ta ? p->K : p->M, ca = p->ex_ta ? p->M : p->K;
-    const int64_t rb = p->ex_tb ? p->N : p->K, cb = p->ex_tb ? p->K : p->N;
-    const int64_t ra_u = p->ex_swap ? rb : ra, ca_u = p->ex_swap ? cb : ca, lda_u = p->ex_swap ? p->ex_ldb : p->ex_lda;
-    const int64_t rb_u = p->ex_swap ? ra : rb, cb_u = p->ex_swap ? ca : cb, ldb_u = p->ex_swap ? p->ex_lda : p->ex_ldb;
-    for (int64_t z = 0; z < nb; ++z) {
-      if (cudaMemcpy2DAsync(dA + z * p->stride_a, lda_u * fs, hA + z * p->stride_a, lda_u * fs, ca_u * fs, ra_u,
-                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
+  sgemm_status_t st = copy_inputs(p, product, beta, hA, hB, hC, dA, dB, dC, stream);
+  if (st != SGEMM_OK) return st;
+  st = sgemm_run(plan, alpha, dA, dB, beta, dC, stream_);
+  if (st != SGEMM_OK) return st;
+  return copy_output(p, hC, dC, stream);
+}
+
+sgemm_status_t sgemm_run_host_pipelined(sgemm_plan_t plan, int count, float alpha, const float* const* hA,
+                                        const float* const* hB, float beta, float* const* hC, float* const* dA,
+                                        float* const* dB, float* const* dC, void* stream_) {
+  if (!plan || count < 0) return SGEMM_ERR_INVALID_ARG;
+  sgemm_plan_s* p = plan;
+  if (count == 0 || p->M == 0 || p->N == 0 || p->batch == 0) return SGEMM_OK;
+  const bool product = p->K > 0 && alpha != 0.f;
+  if (!hC || !dC || !dC[0] || !dC[1]) return SGEMM_ERR_INVALID_ARG;
+  if (product && (!hA || !hB || !dA || !dB || !dA[0] || !dA[1] || !dB[0] || !dB[1])) return SGEMM_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i)
+    if (!hC[i] || (product && (!hA[i] || !hB[i]))) return SGEMM_ERR_INVALID_ARG;
+  {
+    std::lock_guard<std::mutex> lock(p->pipe_mutex);
+    if (!p->pipe_ready) {
+      if (cudaStreamCreateWithFlags(&p->pipe_h2d, cudaStreamNonBlocking) != cudaSuccess) return SGEMM_ERR_CUDA;
+      if (cudaStreamCreateWithFlags(&p->pipe_d2h, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaStreamDestroy(p->pipe_h2d);
         return SGEMM_ERR_CUDA;
-      if (cudaMemcpy2DAsync(dB + z * p->stride_b, ldb_u * fs, hB + z * p->stride_b, ldb_u * fs, cb_u * fs, rb_u,
-                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
-        return SGEMM_ERR_CUDA;
+      }
+      for (int b = 0; b < 2; ++b)
+        for (int e = 0; e < 3; ++e)
+          if (cudaEventCreateWithFlags(&p->pipe_ev[b][e], cudaEventDisableTiming) != cudaSuccess) return SGEMM_ERR_CUDA;
+      p->pipe_ready = true;
     }
   }
-  if (beta != 0.f) {
-    for (int64_t z = 0; z < nb; ++z)
-      if (cudaMemcpy2DAsync(dC + z * p->stride_c, p->ldc * fs, hC + z * p->stride_c, p->ldc * fs, p->N * fs, p->M,
-                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
+  cudaStream_t compute = static_cast<cudaStream_t>(stream_);
+  enum { kLoaded = 0, kComputed = 1, kStored = 2 };
+  // Work already on the caller's stream (earlier writes to the buffers or
+  // the host arrays) comes first: both copy streams wait for it.
+  if (cudaEventRecord(p->pipe_ev[0][kComputed], compute) != cudaSuccess ||
+      cudaStreamWaitEvent(p->pipe_h2d, p->pipe_ev[0][kComputed], 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->pipe_d2h, p->pipe_ev[0][kComputed], 0) != cudaSuccess)
+    return SGEMM_ERR_CUDA;
+  for (int i = 0; i < count; ++i) {
+    const int b = i & 1;
+    cudaEvent_t* ev = p->pipe_ev[b];
+    if (i >= 2) {
+      // buffer set b is free once product i-2 has been computed (A, B read)
+      // and its result copied out (C)
+      if (cudaStreamWaitEvent(p->pipe_h2d, ev[kComputed], 0) != cudaSuccess ||
+          cudaStreamWaitEvent(p->pipe_h2d, ev[kStored], 0) != cudaSuccess)
         return SGEMM_ERR_CUDA;
-  }
-  sgemm_status_t st = sgemm_run(plan, alpha, dA, dB, beta, dC, stream_);
-  if (st != SGEMM_OK) return st;
-  for (int64_t z = 0; z < nb; ++z)
-    if (cudaMemcpy2DAsync(hC + z * p->stride_c, p->ldc * fs, dC + z * p->stride_c, p->ldc * fs, p->N * fs, p->M,
-                          cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    }
+    sgemm_status_t st = copy_inputs(p, product, beta, product ? hA[i] : nullptr, product ? hB[i] : nullptr, hC[i],
+                                    product ? dA[b] : nullptr, product ? dB[b] : nullptr, dC[b], p->pipe_h2d);
+    if (st != SGEMM_OK) return st;
+    if (cudaEventRecord(ev[kLoaded], p->pipe_h2d) != cudaSuccess ||
+        cudaStreamWaitEvent(compute, ev[kLoaded], 0) != cudaSuccess)
       return SGEMM_ERR_CUDA;
+    st = sgemm_run(plan, alpha, product ? dA[b] : nullptr, product ? dB[b] : nullptr, beta, dC[b], compute);
+    if (st != SGEMM_OK) return st;
+    if (cudaEventRecord(ev[kComputed], compute) != cudaSuccess ||
+        cudaStreamWaitEvent(p->pipe_d2h, ev[kComputed], 0) != cudaSuccess)
+      return SGEMM_ERR_CUDA;
+    st = copy_output(p, hC[i], dC[b], p->pipe_d2h);
+    if (st != SGEMM_OK) return st;
+    if (cudaEventRecord(ev[kStored], p->pipe_d2h) != cudaSuccess) return SGEMM_ERR_CUDA;
+  }
+  // the caller's stream reaches this point once every result is in host memory
+  for (int b = 0; b < (count > 1 ? 2 : 1); ++b)
+    if (cudaStreamWaitEvent(compute, p->pipe_ev[b][kStored], 0) != cudaSuccess) return SGEMM_ERR_CUDA;
   return SGEMM_OK;
 }
 
@@ -695,6 +781,14 @@ sgemm_status_t sgemm_plan_destroy(sgemm_plan_t plan) {
   if (plan->tc_split && cudaFree(plan->tc_split) != cudaSuccess) st = SGEMM_ERR_CUDA;
   if (plan->ex_wa && cudaFree(plan->ex_wa) != cudaSuccess) st = SGEMM_ERR_CUDA;
   if (plan->ex_wb && cudaFree(plan->ex_wb) != cudaSuccess) st = SGEMM_ERR_CUDA;
+  if (plan->pipe_ready) {
+    if (cudaStreamSynchronize(plan->pipe_h2d) != cudaSuccess || cudaStreamSynchronize(plan->pipe_d2h) != cudaSuccess)
+      st = SGEMM_ERR_CUDA;
+    for (int b = 0; b < 2; ++b)
+      for (int e = 0; e < 3; ++e) cudaEventDestroy(plan->pipe_ev[b][e]);
+    cudaStreamDestroy(plan->pipe_h2d);
+    cudaStreamDestroy(plan->pipe_d2h);
+  }
   delete plan;
   return st;
 }

@@ -197,6 +197,34 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float *A, const f
 sgemm_status_t sgemm_run_host(sgemm_plan_t plan, float alpha, const float *hA, const float *hB,
                               float beta, float *hC, float *dA, float *dB, float *dC, void *stream);
 
+/*
+ * A stream of `count` products of the plan's shape from HOST memory:
+ * product i reads hA[i], hB[i] (and hC[i] when beta != 0) and writes hC[i].
+ *
+ * Buffers: dA, dB, dC each point to TWO device buffers of the plan's size,
+ * owned by the caller. Products alternate between the two sets.
+ *
+ * Overlap: while product i computes on `stream`, the inputs of product i+1
+ * copy in on one stream and the result of product i-1 copies out on
+ * another, so the copies run under the kernels. The two copy streams and
+ * six events belong to the plan, made on the first call (no device memory
+ * is allocated).
+ *
+ * Returns after enqueueing. Once `stream` reaches this point, every result
+ * is in host memory. Host memory should be pinned for the copies to be
+ * asynchronous.
+ *
+ * Concurrency: calls on one plan must not overlap in time.
+ *
+ * Errors: as sgemm_run_host. SGEMM_ERR_INVALID_ARG for count < 0 or a
+ * missing pointer.
+ *
+ * The pages time kernels only; this entry exists for end-to-end use.
+ */
+sgemm_status_t sgemm_run_host_pipelined(sgemm_plan_t plan, int count, float alpha, const float *const *hA,
+                                        const float *const *hB, float beta, float *const *hC, float *const *dA,
+                                        float *const *dB, float *const *dC, void *stream);
+
 /* Free a plan and its device workspace, if any (the device that was
  * current at sgemm_plan must be current here).  NULL is accepted. */
 sgemm_status_t sgemm_plan_destroy(sgemm_plan_t plan);

@@ -623,3 +623,24 @@ def test_c_beyond_2_31_elements(sg, oracle_mod, config, off_a):
     del dC
     Cref, S = oracle_mod.sgemm_ref(np.ascontiguousarray(A[rows]), B, None, 1.0, 0.0)
     assert_parity(Cs, Cref, S, K, f"{used} rows {rows.tolist()} of {M}x{N}")
+
+
+def test_run_host_pipelined(sg, oracle_mod):
+    """Six different products streamed from pinned host memory through two buffer sets."""
+    M, N, K = 300, 260, 196
+    plan = sg.Plan(M, N, K)
+    ins = [make_inputs(M, N, K, seed=100 + i, dist_a=("normal", 1.0), dist_b=("normal", 1.0)) for i in range(6)]
+    hA = [torch.from_numpy(a).pin_memory() for a, _, _ in ins]
+    hB = [torch.from_numpy(b).pin_memory() for _, b, _ in ins]
+    hC = [torch.from_numpy(c.copy()).pin_memory() for _, _, c in ins]
+    dA = [torch.empty(M, K, device="cuda") for _ in range(2)]
+    dB = [torch.empty(K, N, device="cuda") for _ in range(2)]
+    dC = [torch.empty(M, N, device="cuda") for _ in range(2)]
+    stream = torch.cuda.Stream()
+    plan.run_host_pipelined(0.5, hA, hB, 2.0, hC, dA, dB, dC, stream=stream)
+    stream.synchronize()
+    assert sg.device_status() == sg.SGEMM_OK
+    for i, (a, b, c) in enumerate(ins):
+        Cref, S = oracle_mod.sgemm_ref(a, b, c, 0.5, 2.0)
+        assert_parity(hC[i].numpy(), Cref, S, K, f"pipelined product {i}")
+    plan.close()
