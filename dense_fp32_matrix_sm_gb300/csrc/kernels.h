@@ -14,6 +14,7 @@ enum VariantKind : int {
   kKindSkinny = 2,   // small-M streaming kernel, needs 16-byte aligned A/B rows
   kKindCpa = 3,      // A by cp.async (transposed, any alignment), B by TMA (16-byte aligned rows)
   kKindTc = 4,       // tensor cores, operands split into two TF32 parts (any alignment; plan workspace)
+  kKindTcFused = 5,  // tensor cores, the split inside the GEMM kernel (A and B read by TMA as stored)
 };
 
 // Everything one launch needs.  Tensor maps are encoded by the caller per

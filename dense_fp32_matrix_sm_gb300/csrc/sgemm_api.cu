@@ -165,6 +165,9 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
   // The split leaves ~3 * 2^-22 |a b| per product; K >= 16 keeps that well
   // inside the acceptance bound 4 K 2^-24 |A||B|.
   if (v->kind == kKindTc) return K >= 16;
+  // the fused form reads A and B by TMA as stored: 16-byte rows (the stored
+  // leading dimensions are checked again by sgemm_plan_ex)
+  if (v->kind == kKindTcFused) return K >= 16 && lda % 4 == 0 && ldb % 4 == 0;
   if (ldb % 4 != 0) return false;  // TMA row strides must be multiples of 16 bytes
   if (v->kind == kKindCpa) return true;  // A is copied 4 bytes at a time: any lda
   if (lda % 4 != 0) return false;
@@ -464,6 +467,32 @@ sgemm_status_t encode_maps(const Variant* v, const sgemm_plan_s* p, const float*
   return SGEMM_OK;
 }
 
+// Tensor maps for the fused split-TF32 kernel over A and B as stored: a
+// K-major operand (A as M x K, B given as N x K) with the 128-byte swizzle
+// and 32 (k) x 128 (rows) boxes; an MN-major one (B as K x N, A given as
+// K x M) unswizzled with 128 (rows) x 32 (k) boxes.
+sgemm_status_t encode_maps_tcf(const Variant* v, const sgemm_plan_s* p, const float* A, const float* B,
+                               LaunchArgs* a) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return SGEMM_ERR_CUDA;
+  auto one = [&](CUtensorMap* map, const float* base, bool k_major, int64_t rows, int64_t ld, int box_rows) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k_major ? p->K : rows),
+                                static_cast<cuuint64_t>(k_major ? rows : p->K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(k_major ? v->bk : box_rows),
+                               static_cast<cuuint32_t>(k_major ? box_rows : v->bk)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, k_major ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  if (!one(&a->tmA, A, !p->ex_ta, p->M, p->ex_lda, v->bm) || !one(&a->tmB, B, p->ex_tb != 0, p->N, p->ex_ldb, v->bn))
+    return SGEMM_ERR_CUDA;
+  a->a_trans = p->ex_ta;
+  a->b_trans = p->ex_tb;
+  return SGEMM_OK;
+}
+
 // Host-to-device copies of one product's inputs (A and B when there is a
 // product, C when beta != 0) with their stored shapes, one 2-D copy per
 // matrix of a batch; and the device-to-host copy of its result.
@@ -561,11 +590,14 @@ sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64
     const char* env = getenv("SGEMM_FORCE_CONFIG");
     if (env && *env) forced = find_variant(env);
   }
-  const bool native = forced >= 0 && reg.all[forced]->kind == kKindTc;  // reads either layout itself
+  const bool native = forced >= 0 && (reg.all[forced]->kind == kKindTc ||
+                                      reg.all[forced]->kind == kKindTcFused);  // reads either layout itself
+  if (native && reg.all[forced]->kind == kKindTcFused && (lda2 % 4 != 0 || ldb2 % 4 != 0))
+    return SGEMM_ERR_UNSUPPORTED;
   // the row-major, untransposed operands the other kernels read: a
   // transposed operand goes through a plan buffer with a 16-byte row stride
-  const int64_t lda_eff = ta && !native ? std::max<int64_t>(4, (K + 3) / 4 * 4) : (ta ? std::max<int64_t>(1, K) : lda2);
-  const int64_t ldb_eff = tb && !native ? std::max<int64_t>(4, (N2 + 3) / 4 * 4) : (tb ? std::max<int64_t>(1, N2) : ldb2);
+  const int64_t lda_eff = ta && !native ? std::max<int64_t>(4, (K + 3) / 4 * 4) : (ta ? (K + 3) / 4 * 4 : lda2);
+  const int64_t ldb_eff = tb && !native ? std::max<int64_t>(4, (N2 + 3) / 4 * 4) : (tb ? (N2 + 3) / 4 * 4 : ldb2);
   sgemm_plan_t p = nullptr;
   sgemm_status_t st = make_plan(M2, N2, K, lda_eff, ldb_eff, ldc, config_id, &p);
   if (st != SGEMM_OK) return st;
@@ -575,7 +607,8 @@ sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64
   p->ex_tb = tb;
   p->ex_lda = lda2;
   p->ex_ldb = ldb2;
-  if (!native && registry().all[p->config_id]->kind != kKindTc) {
+  const int kind = registry().all[p->config_id]->kind;
+  if (!native && kind != kKindTc && kind != kKindTcFused) {
     if (ta && M2 > 0 && K > 0 && cudaMalloc(reinterpret_cast<void**>(&p->ex_wa), sizeof(float) * M2 * lda_eff) != cudaSuccess) {
       sgemm_plan_destroy(p);
       return SGEMM_ERR_CUDA;
@@ -629,7 +662,10 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   }
   int grid = p->grid;
   const bool a_needs_16 = v->kind == kKindTma || v->kind == kKindSkinny;
-  if (v->kind != kKindGeneric && v->kind != kKindTc &&
+  if (v->kind == kKindTcFused &&
+      ((reinterpret_cast<uintptr_t>(A) & 15) != 0 || (reinterpret_cast<uintptr_t>(B) & 15) != 0))
+    return SGEMM_ERR_UNSUPPORTED;  // TMA needs 16-byte aligned bases; the scalar kernel cannot read every layout
+  if (v->kind != kKindGeneric && v->kind != kKindTc && v->kind != kKindTcFused &&
       ((a_needs_16 && (reinterpret_cast<uintptr_t>(A) & 15) != 0) || (reinterpret_cast<uintptr_t>(B) & 15) != 0)) {
     v = reg.all[p->generic_id];
     grid = 0;
@@ -686,6 +722,9 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
     a.tmA2 = p->tc_maps[1];
     a.tmB = p->tc_maps[2];
     a.tmB2 = p->tc_maps[3];
+  } else if (v->kind == kKindTcFused) {
+    st = encode_maps_tcf(v, p, A, B, &a);
+    if (st != SGEMM_OK) return st;
   } else if (v->kind != kKindGeneric && v->tma_swizzle_a >= 0) {
     st = encode_maps(v, p, A, B, &a);
     if (st != SGEMM_OK) return st;
@@ -800,11 +839,11 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
            "variant=%s kind=%s tile=%dx%dx%d stages=%d ffma2=%d threads=%d smem=%d grid=%d ctas_per_sm=%d "
            "tiles=%lld sms=%d split=%d streamk=%d dp_waves=%d sk_tiles=%lld k_order=%s M=%lld N=%lld K=%lld "
            "order=%s op=%c%c batch=%lld",
-           v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : v->kind == kKindTc ? "tc" : "skinny", v->bm, v->bn,
+           v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : v->kind == kKindTc ? "tc" : v->kind == kKindTcFused ? "tcf" : "skinny", v->bm, v->bn,
            v->bk, v->stages, v->ffma2, v->threads, v->smem_bytes, plan->grid, plan->ctas_per_sm,
            static_cast<long long>(plan->tiles), plan->num_sms, plan->split, plan->sk_iters > 0 ? 1 : 0, plan->dp_waves,
            static_cast<long long>(plan->sk_iters > 0 ? plan->tiles - static_cast<int64_t>(plan->dp_waves) * plan->grid : 0),
-           v->kind == kKindTc ? "tf32x3"
+           (v->kind == kKindTc || v->kind == kKindTcFused) ? "tf32x3"
            : (plan->split > 1 || v->kind == kKindSkinny || plan->sk_iters > 0) ? "split" : "sequential",
            static_cast<long long>(plan->ex_swap ? plan->N : plan->M),
            static_cast<long long>(plan->ex_swap ? plan->M : plan->N), static_cast<long long>(plan->K),

@@ -393,9 +393,295 @@ struct TcVariant {
   }
 };
 
+// ---------------------------------------------------------------------------
+// Fused form: the split happens inside the GEMM kernel.
+//  * Warp 0 copies the raw float32 slices of A and B (32 deep, 128 rows
+//    each) by TMA into a 3-deep raw ring, hiding the copy latency.
+//  * Eight converter warps turn raw slot r into the hi and lo parts of both
+//    operands in slot h of a 2-deep split ring: K-major tiles in the layout
+//    the MMA reads (128-byte rows, 16-byte chunk q of row r at position
+//    q ^ (r % 8), the layout TMA's 128-byte swizzle gives).  A K-major
+//    source (A as stored, B given transposed) arrives with that swizzle and
+//    converts chunk by chunk; an MN-major source (B as stored, A given
+//    transposed) arrives unswizzled as [32 k][128 rows] and is transposed
+//    while converting.  They fence the async proxy, then release the raw
+//    slot and publish the split slot.
+//  * Warp 1 issues the MMAs on split slots as they are published.
+//  * The converter warps run the epilogue after the last slice.
+constexpr int kFBN = 128;
+constexpr int kFRawStages = 3;
+constexpr int kFSplitStages = 2;
+constexpr int kFThreads = 320;                    // warp 0 TMA, warp 1 MMA, warps 2-9 convert + epilogue
+constexpr int kFConv = 256;                       // converter threads
+constexpr int kFTile = BM * BK * 4;               // 16 KB: one 128-row x 32-k operand slice
+constexpr int kFRawBytes = kFRawStages * 2 * kFTile;      // raw A, raw B per slot
+constexpr int kFSplitBytes = kFSplitStages * 4 * kFTile;  // A_hi, A_lo, B_hi, B_lo per slot
+constexpr int kFSmemBytes = kFRawBytes + kFSplitBytes + kBarBytes + 1024;
+static_assert(kFSmemBytes <= 227 * 1024, "shared memory per CTA");
+constexpr uint32_t kFIdesc = TcShape<kFBN, 1>::kIdesc;
+
+// Converter thread t (0..255) takes half of one 128-row x 32-k slice:
+// raw -> hi, lo (both K-major, swizzled).  MN_MAJOR: raw is [32 k][128 rows]
+// (512-byte rows, no swizzle); else raw is already K-major and swizzled.
+template <bool MN_MAJOR>
+__device__ __forceinline__ void convert_half(const unsigned char* raw, unsigned char* hi, unsigned char* lo, int t) {
+  if constexpr (MN_MAJOR) {
+    // row t % 128, chunks q of half t / 128: 4 k values per chunk, one from
+    // each raw row (consecutive threads read consecutive words), stored as
+    // one 16-byte chunk
+    const float* r = reinterpret_cast<const float*>(raw);
+    const int row = t & 127;
+    const int q0 = 4 * (t >> 7);
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      const int q = q0 + qq;
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = r[(4 * q + j) * BM + row];
+      float h[4], l[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        h[j] = to_tf32(v[j]);
+        l[j] = to_tf32(v[j] - h[j]);
+      }
+      const int off = row * 128 + ((q ^ (row & 7)) << 4);
+      *reinterpret_cast<float4*>(hi + off) = make_float4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<float4*>(lo + off) = make_float4(l[0], l[1], l[2], l[3]);
+    }
+  } else {
+    // 1024 chunks of 16 bytes, 4 per thread; the swizzle is the same in all three tiles
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int off = (t + kFConv * i) << 4;
+      const float4 v = *reinterpret_cast<const float4*>(raw + off);
+      const float x[4] = {v.x, v.y, v.z, v.w};
+      float h[4], l[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        h[j] = to_tf32(x[j]);
+        l[j] = to_tf32(x[j] - h[j]);
+      }
+      *reinterpret_cast<float4*>(hi + off) = make_float4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<float4*>(lo + off) = make_float4(l[0], l[1], l[2], l[3]);
+    }
+  }
+}
+
+// TA: A given transposed (stored K x M); TB: B given transposed (stored N x K).
+template <bool TA, bool TB>
+__global__ void __launch_bounds__(kFThreads, 1)
+    tf32x3_fused_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const TcParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw_base = ptx::smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+  const uint32_t smem_base = ptx::smem_addr(smem);
+  // raw slot r: A at raw_off(r, 0), B at raw_off(r, 1); split slot h: part i
+  // (0 A_hi, 1 A_lo, 2 B_hi, 3 B_lo) at split_off(h, i)
+  auto raw_off = [](int r, int i) { return (2 * r + i) * kFTile; };
+  auto split_off = [](int h, int i) { return kFRawBytes + (4 * h + i) * kFTile; };
+  const uint32_t bar_base = smem_base + kFRawBytes + kFSplitBytes;
+  auto raw_full = [&](int r) { return bar_base + 8u * r; };
+  auto raw_empty = [&](int r) { return bar_base + 8u * (kFRawStages + r); };
+  auto split_full = [&](int h) { return bar_base + 8u * (2 * kFRawStages + h); };
+  auto split_empty = [&](int h) { return bar_base + 8u * (2 * kFRawStages + kFSplitStages + h); };
+  const uint32_t accum_bar = bar_base + 8u * (2 * kFRawStages + 2 * kFSplitStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kFRawBytes + kFSplitBytes +
+                                                    8 * (2 * kFRawStages + 2 * kFSplitStages + 1));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tiles_m = (p.M + BM - 1) / BM;
+  const int tiles_n = (p.N + kFBN - 1) / kFBN;
+  int tm, tn;
+  tile_coords(blockIdx.x, tiles_m, tiles_n, p.group_m, tm, tn);
+  const int KT = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int r = 0; r < kFRawStages; ++r) {
+      ptx::mbar_init(raw_full(r), 1);
+      ptx::mbar_init(raw_empty(r), kFConv);
+    }
+    for (int h = 0; h < kFSplitStages; ++h) {
+      ptx::mbar_init(split_full(h), kFConv);
+      ptx::mbar_init(split_empty(h), 1);
+    }
+    ptx::mbar_init(accum_bar, 1);
+    ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(ptx::smem_addr(tmem_slot)),
+                 "r"(static_cast<uint32_t>(kFBN))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer: raw slices of A and B ----
+    int issued = 0;
+    for (int kb = 0; kb < KT; ++kb) {
+      const int r = kb % kFRawStages;
+      if (kb >= kFRawStages && !ptx::mbar_wait(raw_empty(r), ((kb / kFRawStages) - 1) & 1, p.timeout_ns)) {
+        atomicOr(p.status, kStatusTimeoutEmpty);
+        break;
+      }
+      ptx::mbar_arrive_expect_tx(raw_full(r), 2 * kFTile);
+      if constexpr (TA) {
+        ptx::tma_load_2d(smem_base + raw_off(r, 0), &tmA, tm * BM, kb * BK, raw_full(r));
+      } else {
+        ptx::tma_load_2d(smem_base + raw_off(r, 0), &tmA, kb * BK, tm * BM, raw_full(r));
+      }
+      if constexpr (TB) {
+        ptx::tma_load_2d(smem_base + raw_off(r, 1), &tmB, kb * BK, tn * kFBN, raw_full(r));
+      } else {
+        ptx::tma_load_2d(smem_base + raw_off(r, 1), &tmB, tn * kFBN, kb * BK, raw_full(r));
+      }
+      issued = kb + 1;
+    }
+    // every copy started here has landed before the CTA can leave
+    for (int kb = issued > kFRawStages ? issued - kFRawStages : 0; kb < issued; ++kb)
+      ptx::mbar_wait(raw_full(kb % kFRawStages), (kb / kFRawStages) & 1, p.timeout_ns);
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer ----
+    for (int kb = 0; kb < KT; ++kb) {
+      const int h = kb % kFSplitStages;
+      if (!ptx::mbar_wait(split_full(h), (kb / kFSplitStages) & 1, p.timeout_ns)) {
+        atomicOr(p.status, kStatusTimeoutFull);
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < BK / 8; ++kk) {
+        const uint64_t ah = smem_desc_sw128(smem_base + split_off(h, 0) + 32 * kk);
+        const uint64_t al = smem_desc_sw128(smem_base + split_off(h, 1) + 32 * kk);
+        const uint64_t bh = smem_desc_sw128(smem_base + split_off(h, 2) + 32 * kk);
+        const uint64_t bl = smem_desc_sw128(smem_base + split_off(h, 3) + 32 * kk);
+        mma_tf32(tmem, al, bh, kFIdesc, (kb | kk) != 0 ? 1u : 0u);
+        mma_tf32(tmem, ah, bl, kFIdesc, 1u);
+        mma_tf32(tmem, ah, bh, kFIdesc, 1u);
+      }
+      mma_commit(split_empty(h));  // the split slot is free once these MMAs have read it
+    }
+    mma_commit(accum_bar);  // arrives when every MMA issued above has completed
+  } else if (warp >= 2) {
+    // ---- converters ----
+    const int t = threadIdx.x - 64;
+    bool ok = true;
+    for (int kb = 0; kb < KT; ++kb) {
+      const int r = kb % kFRawStages, h = kb % kFSplitStages;
+      if (!ptx::mbar_wait(raw_full(r), (kb / kFRawStages) & 1, p.timeout_ns) ||
+          (kb >= kFSplitStages && !ptx::mbar_wait(split_empty(h), ((kb / kFSplitStages) - 1) & 1, p.timeout_ns))) {
+        atomicOr(p.status, kStatusTimeoutFull);
+        ok = false;
+        break;
+      }
+      convert_half<TA>(smem + raw_off(r, 0), smem + split_off(h, 0), smem + split_off(h, 1), t);
+      convert_half<!TB>(smem + raw_off(r, 1), smem + split_off(h, 2), smem + split_off(h, 3), t);
+      ptx::fence_proxy_async_smem();  // the MMA reads the split tiles through the async proxy
+      ptx::mbar_arrive(split_full(h));
+      ptx::mbar_arrive(raw_empty(r));
+    }
+    // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows),
+    //      columns 64 ((w - 2) / 4) .. +63 ----
+    const bool done = ptx::mbar_wait(accum_bar, 0, p.timeout_ns);
+    if (!done) atomicOr(p.status, kStatusTimeoutFull);
+    tc_fence_after();
+    const int lane_base = 32 * (warp & 3);
+    const int col_half = (warp - 2) >> 2;
+    const int row = tm * BM + lane_base + lane;
+#pragma unroll 1
+    for (int cc = 64 * col_half; cc < 64 * col_half + 64; cc += 32) {
+      uint32_t rr[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(lane_base) << 16) + static_cast<uint32_t>(cc), rr);
+      if (!done || !ok || row >= p.M) continue;
+      float* crow = p.C + static_cast<int64_t>(row) * p.ldc;
+      const int col0 = tn * kFBN + cc;
+      if (p.vec_c && col0 + 32 <= p.N) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          float4* d = reinterpret_cast<float4*>(crow + col0 + j);
+          const float4 v = make_float4(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1]),
+                                       __uint_as_float(rr[j + 2]), __uint_as_float(rr[j + 3]));
+          if (p.beta == 0.f) {
+            *d = make_float4(p.alpha * v.x, p.alpha * v.y, p.alpha * v.z, p.alpha * v.w);
+          } else {
+            const float4 o = *d;
+            *d = make_float4(fmaf(p.alpha, v.x, p.beta * o.x), fmaf(p.alpha, v.y, p.beta * o.y),
+                             fmaf(p.alpha, v.z, p.beta * o.z), fmaf(p.alpha, v.w, p.beta * o.w));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int col = col0 + j;
+          if (col < p.N) {
+            const float v = __uint_as_float(rr[j]);
+            crow[col] = p.beta == 0.f ? p.alpha * v : fmaf(p.alpha, v, p.beta * crow[col]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(static_cast<uint32_t>(kFBN))
+                 : "memory");
+  }
+}
+
+struct TcFusedVariant {
+  static constexpr auto k00 = tf32x3_fused_kernel<false, false>;
+  static constexpr auto k01 = tf32x3_fused_kernel<false, true>;
+  static constexpr auto k10 = tf32x3_fused_kernel<true, false>;
+  static constexpr auto k11 = tf32x3_fused_kernel<true, true>;
+  static cudaError_t prepare() {
+    for (auto k : {k00, k01, k10, k11}) {
+      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmemBytes);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  static cudaError_t occupancy(int* ctas) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, k00, kFThreads, kFSmemBytes);
+  }
+  // a.tmA / a.tmB: maps over A and B as stored (see the split-TF32 fused
+  // branch of the plan code): K-major sources with the 128-byte swizzle and
+  // 32 x 128 boxes, MN-major ones unswizzled with 128 x 32 boxes
+  static cudaError_t launch(const LaunchArgs& a, cudaStream_t stream) {
+    TcParams p;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    p.group_m = 8;
+    p.vec_c = (reinterpret_cast<uintptr_t>(a.C) & 15) == 0 && a.ldc % 4 == 0;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    const auto k = a.a_trans ? (a.b_trans ? k11 : k10) : (a.b_trans ? k01 : k00);
+    k<<<a.grid, kFThreads, kFSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    return cudaGetLastError();
+  }
+  static Variant describe(const char* name) {
+    return Variant{name, kKindTcFused, BM, kFBN, BK, kFRawStages, 0, kFThreads, kFSmemBytes, 128, &prepare, &occupancy,
+                   &launch, 0, 0};
+  }
+};
+
 const Variant kVariants[] = {
     TcVariant<256, 2>::describe("tf32x3_128x256x32_s2"),
     TcVariant<128, 3>::describe("tf32x3_128x128x32_s3"),
+    TcFusedVariant::describe("tf32x3f_128x128x32_s3"),
 };
 
 }  // namespace tc

@@ -422,8 +422,10 @@ def test_stream_k_tail(sg, oracle_mod, shape):
 # ---- split-TF32 tensor-core variant (reported apart from the FFMA path) -------
 
 TC = "tf32x3_128x256x32_s2"
+TC_VARIANTS = ["tf32x3_128x256x32_s2", "tf32x3_128x128x32_s3", "tf32x3f_128x128x32_s3"]
 
 
+@pytest.mark.parametrize("tc", TC_VARIANTS)
 @pytest.mark.parametrize("case", [
     # (M, N, K, lda pad, ldb pad, ldc pad, A offset, B offset, alpha, beta, distribution)
     (1024, 1024, 1024, 0, 0, 0, 0, 0, 1.0, 0.0, "normal"),
@@ -433,18 +435,20 @@ TC = "tf32x3_128x256x32_s2"
     # all-positive inputs: partial sums grow to |A||B|, the worst case for accumulator rounding
     (512, 768, 4096, 0, 0, 0, 0, 0, 1.0, 0.0, "positive"),
 ])
-def test_split_tf32_variant(sg, oracle_mod, case):
+def test_split_tf32_variant(sg, oracle_mod, case, tc):
     M, N, K, pa, pb, pc, oa, ob, alpha, beta, dist = case
+    if tc.startswith("tf32x3f") and (pa % 4 or pb % 4 or oa % 4 or ob % 4 or K % 4 or N % 4):
+        pytest.skip("the fused form reads A and B by TMA: 16-byte rows and bases")
     d = ("uniform", 1.0) if dist == "normal" else ("uniform", 1.0)
     A, B, C0 = make_inputs(M, N, K, seed=M + N + K, dist_a=("normal", 1.0) if dist == "normal" else d, dist_b=d)
     if dist == "positive":
         A, B = np.abs(A), np.abs(B)
     Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
-    C, used = run_gpu(sg, A, B, C0, alpha, beta, config=TC, lda=K + pa, ldb=N + pb, ldc=N + pc, off_a=oa,
+    C, used = run_gpu(sg, A, B, C0, alpha, beta, config=tc, lda=K + pa, ldb=N + pb, ldc=N + pc, off_a=oa,
                       off_b=ob)
-    assert used == TC and run_gpu.last_info["k_order"] == "tf32x3"
-    assert_parity(C, Cref, S, K, f"{TC} {M}x{N}x{K} {dist}")
-    C2, _ = run_gpu(sg, A, B, C0, alpha, beta, config=TC, lda=K + pa, ldb=N + pb, ldc=N + pc, off_a=oa, off_b=ob)
+    assert used == tc and run_gpu.last_info["k_order"] == "tf32x3"
+    assert_parity(C, Cref, S, K, f"{tc} {M}x{N}x{K} {dist}")
+    C2, _ = run_gpu(sg, A, B, C0, alpha, beta, config=tc, lda=K + pa, ldb=N + pb, ldc=N + pc, off_a=oa, off_b=ob)
     assert np.array_equal(C, C2)
 
 
@@ -481,7 +485,8 @@ def _stored(X, order, trans, pad):
 @pytest.mark.parametrize("order", ["row", "col"])
 @pytest.mark.parametrize("ta,tb", [(False, False), (False, True), (True, False), (True, True)])
 @pytest.mark.parametrize("shape,config,pad", [((257, 131, 77), None, 0), ((200, 300, 100), None, 3),
-                                              ((12, 1000, 515), None, 0), ((300, 520, 96), "tf32x3_128x256x32_s2", 1)])
+                                              ((12, 1000, 515), None, 0), ((300, 520, 96), "tf32x3_128x256x32_s2", 1),
+                                              ((300, 520, 96), "tf32x3f_128x128x32_s3", 0)])
 def test_order_and_transpose(sg, oracle_mod, order, ta, tb, shape, config, pad):
     M, N, K = shape
     opA, opB, C0 = make_inputs(M, N, K, seed=M + 2 * N + 3 * K + ta + 2 * tb, dist_a=("normal", 1.0),
@@ -600,7 +605,8 @@ def test_strided_batch_argument_errors(sg):
 
 # ---- a C of more than 2^31 elements: 64-bit offsets in every epilogue ---------
 
-@pytest.mark.parametrize("config,off_a", [(None, 0), ("generic_64x64x16", 1), ("tf32x3_128x128x32_s3", 0)])
+@pytest.mark.parametrize("config,off_a", [(None, 0), ("generic_64x64x16", 1), ("tf32x3_128x128x32_s3", 0),
+                                          ("tf32x3f_128x128x32_s3", 0)])
 def test_c_beyond_2_31_elements(sg, oracle_mod, config, off_a):
     M, N, K = 65536 + 17, 32768 + 9, 40
     assert M * N > 2 ** 31
