@@ -143,6 +143,47 @@ __device__ __forceinline__ void pa_slice(const float* As, const float4* Bs4, flo
   }
 }
 
+// As pa_slice, with B given transposed (stored N x K): the stage holds
+// Bt[n][k], rows of 32 k (128 bytes) with the 128-byte swizzle (16-byte
+// chunk q of row n at position q ^ (n % 8)).  Lane l of column group g owns
+// columns n = 128 g + l + 32 j (j = 0..3): per k-quad it reads one float4
+// of 4 k from each of its 4 rows; accp[p][j] = {C[2p][n_j], C[2p+1][n_j]}.
+template <int BN, int GW>
+__device__ __forceinline__ void pa_slice_bt(const float* As, const float* Bt, float* atw, int gw, int lane, int group,
+                                            float2 (&accp)[kSBM / 2][4]) {
+#pragma unroll
+  for (int qq = 0; qq < (kSBK / 4) / GW; ++qq) {
+    const int q = gw + GW * qq;
+    {
+      const int m = lane >> 1, h = lane & 1;
+      const float2 v = *reinterpret_cast<const float2*>(As + m * kSBK + ((q ^ (m & 7)) << 2) + 2 * h);
+      atw[(2 * h) * 32 + 16 * h + m] = v.x;
+      atw[(2 * h + 1) * 32 + 16 * h + m] = v.y;
+    }
+    float4 bq[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = 128 * group + lane + 32 * j;
+      bq[j] = *reinterpret_cast<const float4*>(Bt + n * kSBK + ((q ^ (n & 7)) << 2));
+    }
+    __syncwarp();
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const float* ak = atw + kk * 32 + 16 * ((kk >> 1) & 1);
+#pragma unroll
+      for (int pp = 0; pp < kSBM / 2; ++pp) {
+        const float2 ap = *reinterpret_cast<const float2*>(ak + 2 * pp);  // rows 2pp, 2pp+1
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float b = kk == 0 ? bq[j].x : kk == 1 ? bq[j].y : kk == 2 ? bq[j].z : bq[j].w;
+          accp[pp][j] = __ffma2_rn(ap, make_float2(b, b), accp[pp][j]);
+        }
+      }
+    }
+    __syncwarp();  // the next quad overwrites atw
+  }
+}
+
 template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST, bool PAIRA>
 __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     sgemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -338,7 +379,8 @@ struct SkinnySkParams {
   unsigned int epoch;
 };
 
-template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST>
+// BT: B given transposed (stored N x K), loaded as swizzled [n][k] boxes.
+template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST, bool BT>
 __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     sgemm_skinny_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const SkinnySkParams p) {
@@ -382,10 +424,11 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     const uint32_t dst = smem_base + s * S::kStageBytes;
     ptx::mbar_arrive_expect_tx(bar_full + 8 * s, S::kStageBytes);
     ptx::tma_load_2d(dst, &tmA, kt * kSBK, 0, bar_full + 8 * s);
+    const int bx = BT ? kt * kSBK : n0, by = BT ? n0 : kt * kSBK;  // B as [k][n], or Bt as [n][k]
     if constexpr (EVICT_FIRST) {
-      ptx::tma_load_2d_hint(dst + S::kStageA, &tmB, n0, kt * kSBK, bar_full + 8 * s, ptx::l2_policy_evict_first());
+      ptx::tma_load_2d_hint(dst + S::kStageA, &tmB, bx, by, bar_full + 8 * s, ptx::l2_policy_evict_first());
     } else {
-      ptx::tma_load_2d(dst + S::kStageA, &tmB, n0, kt * kSBK, bar_full + 8 * s);
+      ptx::tma_load_2d(dst + S::kStageA, &tmB, bx, by, bar_full + 8 * s);
     }
   };
 
@@ -436,8 +479,13 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
       ready = it + 1 < total_it &&
               ptx::mbar_test_wait(bar_full + 8 * ((it + 1) % STAGES), ((it + 1) / STAGES) & 1u);
       const float* As = reinterpret_cast<const float*>(smem + s * S::kStageBytes);
-      const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + group * 32 + lane;
-      pa_slice<BN, GW>(As, Bs4, atw, gw, lane, accp);
+      if constexpr (BT) {
+        pa_slice_bt<BN, GW>(As, reinterpret_cast<const float*>(smem + s * S::kStageBytes + S::kStageA), atw, gw, lane,
+                            group, accp);
+      } else {
+        const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + group * 32 + lane;
+        pa_slice<BN, GW>(As, Bs4, atw, gw, lane, accp);
+      }
       __syncwarp();
       if (lane == 0) {
         const unsigned int before = ptx::atom_add_acq_rel_cta(&released[s], 1u);
@@ -458,12 +506,19 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
           const int pp = m >> 1;
           const float4 v = (m & 1) ? make_float4(accp[pp][0].y, accp[pp][1].y, accp[pp][2].y, accp[pp][3].y)
                                    : make_float4(accp[pp][0].x, accp[pp][1].x, accp[pp][2].x, accp[pp][3].x);
-          float4* d = part4 + m * (BN / 4) + group * 32 + lane;
-          if (w == 0) {
-            *d = v;
-          } else {
-            const float4 o = *d;
-            *d = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+          if constexpr (BT) {  // lane's columns l + 32 j of the group
+            float* d = partial + m * BN + 128 * group + lane;
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) d[32 * j] = w == 0 ? vv[j] : d[32 * j] + vv[j];
+          } else {  // lane's columns 4 l .. 4 l + 3 of the group
+            float4* d = part4 + m * (BN / 4) + group * 32 + lane;
+            if (w == 0) {
+              *d = v;
+            } else {
+              const float4 o = *d;
+              *d = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+            }
           }
         }
       }
@@ -528,9 +583,13 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
 template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST>
 struct SkinnySkVariant {
   using S = SkinnyShape<BN, GW, STAGES>;
-  static constexpr auto kernel = sgemm_skinny_sk_kernel<BN, GW, STAGES, MINB, EVICT_FIRST>;
+  static constexpr auto kernel = sgemm_skinny_sk_kernel<BN, GW, STAGES, MINB, EVICT_FIRST, false>;
+  static constexpr auto kernel_bt = sgemm_skinny_sk_kernel<BN, GW, STAGES, MINB, EVICT_FIRST, true>;
   static cudaError_t prepare() {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    return e != cudaSuccess ? e
+                            : cudaFuncSetAttribute(kernel_bt, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   S::kSmemBytes);
   }
   static cudaError_t occupancy(int* ctas) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kernel, S::kThreads, S::kSmemBytes);
@@ -549,12 +608,18 @@ struct SkinnySkVariant {
     p.ws = a.ws;
     p.flags = a.flags;
     p.epoch = a.epoch;
-    kernel<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    if (a.b_trans) {
+      kernel_bt<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    } else {
+      kernel<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    }
     return cudaGetLastError();
   }
   static Variant describe(const char* name) {
-    return Variant{name, kKindSkinny, kSBM, BN, kSBK, STAGES, 1, S::kThreads, S::kSmemBytes, 128, &prepare, &occupancy,
-                   &launch, 0, 1};
+    Variant v{name, kKindSkinny, kSBM, BN, kSBK, STAGES, 1, S::kThreads, S::kSmemBytes, 128, &prepare, &occupancy,
+              &launch, 0, 1};
+    v.b_trans_ok = 1;  // reads B given transposed (N x K) itself
+    return v;
   }
 };
 

@@ -53,6 +53,7 @@ struct sgemm_plan_s {
   int64_t ex_lda, ex_ldb;
   float* ex_wa;
   float* ex_wb;
+  int ex_native_tb;  // the variant reads B given transposed (N x K) itself: no ex_wb
   // sgemm_run_host_pipelined: copy streams (host to device, device to host)
   // and, per buffer set b, events loaded / computed / stored; made on first use
   std::mutex pipe_mutex;
@@ -300,6 +301,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->ex_ldb = ldb;
   p->ex_wa = nullptr;
   p->ex_wb = nullptr;
+  p->ex_native_tb = 0;
   p->pipe_ready = false;
   if (v->kind == kKindTma || v->kind == kKindCpa) {
     const int64_t slots = static_cast<int64_t>(sms) * ctas;
@@ -453,7 +455,16 @@ sgemm_status_t encode_maps(const Variant* v, const sgemm_plan_s* p, const float*
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
   }
-  {
+  if (a->b_trans) {  // B given transposed (N x K): K-major boxes of 32 k x bn rows, 128-byte swizzle
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->ex_ldb) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(v->bk), static_cast<cuuint32_t>(v->bn)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&a->tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
+  } else {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->N), static_cast<cuuint64_t>(p->K), nb_b};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p->ldb) * 4,
                                    static_cast<cuuint64_t>(nb_b > 1 ? p->stride_b : p->K * p->ldb) * 4};
@@ -607,13 +618,17 @@ sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64
   p->ex_tb = tb;
   p->ex_lda = lda2;
   p->ex_ldb = ldb2;
-  const int kind = registry().all[p->config_id]->kind;
+  const Variant* chosen = registry().all[p->config_id];
+  const int kind = chosen->kind;
+  // a few-row kernel reads B given transposed (N x K, K contiguous) by TMA itself
+  if (tb && !native && chosen->b_trans_ok && ldb2 % 4 == 0) p->ex_native_tb = 1;
   if (!native && kind != kKindTc && kind != kKindTcFused) {
     if (ta && M2 > 0 && K > 0 && cudaMalloc(reinterpret_cast<void**>(&p->ex_wa), sizeof(float) * M2 * lda_eff) != cudaSuccess) {
       sgemm_plan_destroy(p);
       return SGEMM_ERR_CUDA;
     }
-    if (tb && N2 > 0 && K > 0 && cudaMalloc(reinterpret_cast<void**>(&p->ex_wb), sizeof(float) * K * ldb_eff) != cudaSuccess) {
+    if (tb && !p->ex_native_tb && N2 > 0 && K > 0 &&
+        cudaMalloc(reinterpret_cast<void**>(&p->ex_wb), sizeof(float) * K * ldb_eff) != cudaSuccess) {
       sgemm_plan_destroy(p);
       return SGEMM_ERR_CUDA;
     }
@@ -665,6 +680,8 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   if (v->kind == kKindTcFused &&
       ((reinterpret_cast<uintptr_t>(A) & 15) != 0 || (reinterpret_cast<uintptr_t>(B) & 15) != 0))
     return SGEMM_ERR_UNSUPPORTED;  // TMA needs 16-byte aligned bases; the scalar kernel cannot read every layout
+  if (p->ex_native_tb && ((reinterpret_cast<uintptr_t>(B) & 15) != 0 || (reinterpret_cast<uintptr_t>(A) & 15) != 0))
+    return SGEMM_ERR_UNSUPPORTED;  // B given transposed is read by TMA; the scalar kernel cannot take it
   if (v->kind != kKindGeneric && v->kind != kKindTc && v->kind != kKindTcFused &&
       ((a_needs_16 && (reinterpret_cast<uintptr_t>(A) & 15) != 0) || (reinterpret_cast<uintptr_t>(B) & 15) != 0)) {
     v = reg.all[p->generic_id];
@@ -687,6 +704,7 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   a.grid = grid;
   a.split_k = v->kind == kKindSkinny ? p->split : 1;
   a.batch = static_cast<int>(p->batch);
+  a.b_trans = p->ex_native_tb;
   a.stride_a = p->stride_a;
   a.stride_b = p->stride_b;
   a.stride_c = p->stride_c;

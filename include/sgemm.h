@@ -166,7 +166,11 @@ enum { SGEMM_NO_TRANS = 0, SGEMM_TRANS = 1 };
  *   - The FFMA kernels read row-major operands stored untransposed. A
  *     transposed operand is first transposed on the GPU into a buffer the
  *     plan allocates (cudaMalloc), one extra kernel per run.
- *   - The split-TF32 variant reads either layout directly.
+ *   - The split-TF32 variant reads either layout directly. So does the
+ *     few-row stream-K kernel for B given transposed (stored N x K, the
+ *     usual weight layout of decode) when ldb is a multiple of 4; such a
+ *     plan needs A and B 16-byte aligned at run time, else
+ *     SGEMM_ERR_UNSUPPORTED.
  * Runs of a plan with such a buffer must not overlap in time.
  *
  * The pages cover the row-major, untransposed product only; the other
