@@ -429,6 +429,20 @@ def run_ours(args):
     out["clocks"] = {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "sm_mhz_min",
                                                  "power_w_max", "samples")}
 
+    # The FMA-only probe (after the timed steps): the FFMA pipe's achievable
+    # rate, and the SM clock read inside a kernel, beside the nominal peak.
+    p2_tflops, p2_mhz = sg.probe_ffma(True)
+    p1_tflops, _ = sg.probe_ffma(False)
+    nominal_at_probe = sms * FMA_LANES_PER_SM * 2 * p2_mhz * 1e6 / 1e12
+    out["ffma_probe"] = {"ffma2_tflops": round(p2_tflops, 2), "ffma_tflops": round(p1_tflops, 2),
+                         "sm_mhz_in_kernel": round(p2_mhz, 1),
+                         "nominal_tflops_at_that_clock": round(nominal_at_probe, 2),
+                         "ffma2_frac_of_nominal": round(p2_tflops / nominal_at_probe, 4),
+                         "call": "sgemm_probe_ffma: the FFMA kernels' accumulation pattern without loads (4 x 8 FFMA2 pairs; 8 x 8 FFMA), 2 x 256-thread CTAs per SM"}
+    if out["roofline"]["bound"] == "alu":
+        out["roofline"]["frac_of_ffma2_probe"] = round(achieved_tflops / p2_tflops, 4)
+    out["gpu_launches"] += 4
+
     if not args.kernel_only:
         # End to end from pinned host memory, every step copying its inputs in
         # and its result out.  Headline: sgemm_run_host_pipelined, where one

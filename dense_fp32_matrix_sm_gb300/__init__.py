@@ -21,6 +21,7 @@ from ._lib import (  # noqa: F401
     device_status,
     lib,
     num_configs,
+    probe_ffma,
     run_static_scratch,
     selftest_wait_timeout,
     set_wait_timeout_ns,

@@ -47,6 +47,7 @@ SIGNATURES = {
     "sgemm_run_host_pipelined": (_int, [_vp, _int, _f32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _f32,
                                         ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                         ctypes.POINTER(_vp), _vp]),
+    "sgemm_probe_ffma": (_int, [_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
     "sgemm_plan_batched": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _int,
                                   ctypes.POINTER(_vp)]),
 }
@@ -306,3 +307,11 @@ def run_static_scratch(M: int, N: int, K: int, alpha: float, A, B, beta: float, 
     ldc = int(ldc) if ldc is not None else max(1, N)
     _check(lib().sgemm_run_static_scratch(M, N, K, lda, ldb, ldc, float(alpha), _ptr(A), _ptr(B), float(beta),
                                           _ptr(C), _stream_handle(stream)), "sgemm_run_static_scratch")
+
+
+def probe_ffma(paired: bool = True):
+    """(TFLOP/s, SM MHz measured inside the kernel) of an FMA-only kernel on the current device."""
+    t = ctypes.c_double()
+    f = ctypes.c_double()
+    _check(lib().sgemm_probe_ffma(1 if paired else 0, ctypes.byref(t), ctypes.byref(f)), "sgemm_probe_ffma")
+    return t.value, f.value

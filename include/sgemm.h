@@ -344,6 +344,28 @@ sgemm_status_t sgemm_run_static_scratch(int64_t M, int64_t N, int64_t K, int64_t
                                         int64_t ldc, float alpha, const float *A, const float *B,
                                         float beta, float *C, void *stream);
 
+/*
+ * Measurement aid, not a product: the FP32 FMA pipe's achievable rate on
+ * the current device.
+ *   - Kernel: the FFMA kernels' accumulation pattern without their loads,
+ *     run by two 256-thread CTAs per SM. paired = 1: FFMA2 on 4 x 8 pair
+ *     accumulators (two A rows times one broadcast B value, the form the
+ *     FFMA kernels issue). paired = 0: scalar FFMA on an 8 x 8 outer
+ *     product. Either way each thread does 128 FLOP per step.
+ *   - *tflops: the rate measured with CUDA events over one launch, after
+ *     one warm-up launch.
+ *   - *sm_mhz: the SM clock read inside the kernel, as cycles per
+ *     nanosecond of the global timer between the start and end of its
+ *     first CTA.
+ *   - Behaviour: synchronous (about 1 ms on GB300) on a private stream.
+ *     SGEMM_ERR_INVALID_ARG for NULL outputs or paired not 0 or 1.
+ * The FFMA roofline's nominal denominator is SMs x 128 x 2 x clock; the
+ * pages report an FMA-only test reaching 96% of that rate ("Writing a Fast
+ * Matmul in CUDA, Step by Step", the measurement set-up). This gives the
+ * same figure for GB300.
+ */
+sgemm_status_t sgemm_probe_ffma(int paired, double *tflops, double *sm_mhz);
+
 #ifdef __cplusplus
 }
 #endif

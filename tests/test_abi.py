@@ -85,6 +85,12 @@ def test_plan_ex_rejects_before_cuda(lib):
     assert not h.value
 
 
+def test_probe_rejects_bad_arguments_before_cuda(lib):
+    t = ctypes.c_double()
+    assert lib.sgemm_probe_ffma(1, None, ctypes.byref(t)) == -1
+    assert lib.sgemm_probe_ffma(2, ctypes.byref(t), ctypes.byref(t)) == -1
+
+
 def test_static_scratch_rejects_before_cuda(lib):
     """sgemm_run_static_scratch checks its arguments before any CUDA call."""
     f = lib.sgemm_run_static_scratch

@@ -682,3 +682,14 @@ def test_few_row_transposed_b_is_read_natively(sg, oracle_mod):
     Cref, S = oracle_mod.sgemm_ref(x, Wt, C0, 1.0, 1.0)
     assert_parity(dC.cpu().numpy(), Cref, S, K, "few-row NT")
     plan.close()
+
+
+def test_ffma_probe(sg):
+    """The FMA-only probe: its rate is near the nominal SMs x 128 x 2 x clock, and the clock read inside the
+    kernel is a plausible SM clock."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for paired in (True, False):
+        tflops, mhz = sg.probe_ffma(paired)
+        assert 300.0 < mhz < 3500.0, mhz
+        nominal = sms * 128 * 2 * mhz * 1e6 / 1e12
+        assert 0.5 * nominal < tflops < 1.05 * nominal, (paired, tflops, nominal)
