@@ -283,17 +283,25 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
       const uint32_t s = it % STAGES;
       const float* At = at_buf + (it & 1) * (BK * BM);
       const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + (wn * 32 + 4 * c) / 4;
+      // operands of step k+1 are loaded while step k multiplies (register double buffer)
+      auto load_ops = [&](int k, float2 (&ap)[4], float4& b0, float4& b1) {
+        const int f = S::kSwz * (k / S::kKPart);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          ap[i] = *reinterpret_cast<const float2*>(At + k * BM + ((f & 15) ? a_lo8 : a_lo0) + 16 * (i ^ (f >> 4)));
+        b0 = Bs4[k * (BN / 4)];
+        b1 = Bs4[k * (BN / 4) + 4];
+      };
+      float2 apn[4];
+      float4 b0n, b1n;
+      load_ops(0, apn, b0n, b1n);
 #pragma unroll
       for (int k = 0; k < BK; ++k) {
         float2 ap[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int f = S::kSwz * (k / S::kKPart);
-          ap[i] = *reinterpret_cast<const float2*>(At + k * BM + ((f & 15) ? a_lo8 : a_lo0) + 16 * (i ^ (f >> 4)));
-        }
-        const float4 b0 = Bs4[k * (BN / 4)];
-        const float4 b1 = Bs4[k * (BN / 4) + 4];
-        const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        for (int i = 0; i < 4; ++i) ap[i] = apn[i];
+        const float bb[8] = {b0n.x, b0n.y, b0n.z, b0n.w, b1n.x, b1n.y, b1n.z, b1n.w};
+        if (k + 1 < BK) load_ops(k + 1, apn, b0n, b1n);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
