@@ -265,7 +265,7 @@ def time_steps(torch, fn, steps: int, flush, stream):
     return [s.elapsed_time(e) for s, e in evs]
 
 
-TC_VARIANT = "tf32x3_128x128x32_s3"
+TC_VARIANT = "tf32x3p_128x128x32_s3"
 TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tensor rates, TF32 over BF16
 
 

@@ -109,6 +109,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// As mbar_wait, but also gives up as soon as *abort (a flag the CTA's other
+// roles set when one of them fails) is non-zero.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                                   const volatile int* abort) {
+#pragma unroll 1
+  for (int i = 0; i < 64; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort || globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
 // 2-D tiled TMA load of the box at (x = inner coordinate, y = outer) into
 // shared memory at `dst`; completion is signalled on `bar` as transaction
 // bytes.  x * 4 bytes must be a multiple of 16 (callers pass multiples of 4).

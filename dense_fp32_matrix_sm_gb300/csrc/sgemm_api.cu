@@ -359,7 +359,9 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       p->flags = static_cast<unsigned int*>(flags);
     }
   } else if (v->kind == kKindTc) {
-    // One 128 x 256 tile per CTA.  The plan owns the split operands
+    // persistent forms: one CTA per SM walks the tiles
+    if (v->persistent) grid = std::min<int64_t>(grid, static_cast<int64_t>(sms) * ctas);
+    // One tile per CTA (or per step of a persistent CTA).  The plan owns the split operands
     // (A_hi, A_lo: M x kp; B_hi, B_lo transposed: N x kp) and encodes their
     // four tensor maps once: 32-float (128-byte, swizzled) k-slices of 128
     // rows of A and 256 rows of B.

@@ -360,10 +360,205 @@ void launch_split(const LaunchArgs& a, cudaStream_t stream) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Persistent form: one CTA per SM walks tiles (grouped order) with the same
+// split operands and ring, and two TMEM accumulators of BN columns.  The MMA
+// warp fills one accumulator while warps 2-5 drain the other: after reading
+// a chunk of it they store it, and once the whole accumulator is read they
+// release it (one arrival per warp) for the tile after next.  A role that
+// gives up sets a shared abort flag, so the others stop waiting at once.
 template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
+                             const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
+                             const TcParams p) {
+  using S = TcShape<BN, STAGES>;
+  constexpr int kTileB = S::kTileB;
+  constexpr int kStageBytes = S::kStageBytes;
+  constexpr uint32_t kCols = 2 * S::kTmemCols;  // two accumulators
+  static_assert(kCols <= 512, "TMEM holds 512 columns");
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ int s_abort;
+  const uint32_t raw_base = ptx::smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+  const uint32_t smem_base = ptx::smem_addr(smem);
+  const uint32_t bar_base = smem_base + STAGES * kStageBytes;
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto acc_full = [&](int b) { return bar_base + 8u * (2 * STAGES + b); };
+  auto acc_empty = [&](int b) { return bar_base + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t mma_done = bar_base + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + STAGES * kStageBytes + 8 * (2 * STAGES + 5));
+  const volatile int* abort_flag = &s_abort;
+  auto fail = [&](unsigned int bit) {
+    atomicOr(p.status, bit);
+    *reinterpret_cast<volatile int*>(&s_abort) = 1;
+  };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tiles_m = (p.M + BM - 1) / BM;
+  const int tiles_n = (p.N + BN - 1) / BN;
+  const int num_tiles = tiles_m * tiles_n;
+  const int G = static_cast<int>(gridDim.x);
+  const int my_tiles = static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / G + 1 : 0;
+  const int KT = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(acc_full(b), 1);
+      ptx::mbar_init(acc_empty(b), 4);  // one arrival per epilogue warp
+    }
+    ptx::mbar_init(mma_done, 1);
+    ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tmAh);
+    ptx::prefetch_tensormap(&tmAl);
+    ptx::prefetch_tensormap(&tmBh);
+    ptx::prefetch_tensormap(&tmBl);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(ptx::smem_addr(tmem_slot)),
+                 "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer: slices of every tile, one ring across tiles ----
+    uint32_t g = 0;
+    for (int i = 0; i < my_tiles && !*abort_flag; ++i) {
+      int tm, tn;
+      tile_coords(static_cast<int>(blockIdx.x) + i * G, tiles_m, tiles_n, p.group_m, tm, tn);
+      for (int kb = 0; kb < KT; ++kb, ++g) {
+        const int s = static_cast<int>(g % STAGES);
+        const uint32_t use = g / STAGES;
+        if (g >= STAGES && !ptx::mbar_wait_or_abort(empty_bar(s), (use - 1) & 1u, p.timeout_ns, abort_flag)) {
+          if (!*abort_flag) fail(kStatusTimeoutEmpty);
+          i = my_tiles;
+          break;
+        }
+        const uint32_t st = smem_base + s * kStageBytes;
+        ptx::mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+        ptx::tma_load_2d(st, &tmAh, kb * BK, tm * BM, full_bar(s));
+        ptx::tma_load_2d(st + kTileA, &tmAl, kb * BK, tm * BM, full_bar(s));
+        ptx::tma_load_2d(st + 2 * kTileA, &tmBh, kb * BK, tn * BN, full_bar(s));
+        ptx::tma_load_2d(st + 2 * kTileA + kTileB, &tmBl, kb * BK, tn * BN, full_bar(s));
+      }
+    }
+    // every copy started here has landed before the CTA can leave
+    for (uint32_t h = g > STAGES ? g - STAGES : 0; h < g; ++h)
+      ptx::mbar_wait(full_bar(static_cast<int>(h % STAGES)), (h / STAGES) & 1u, p.timeout_ns);
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer ----
+    uint32_t g = 0;
+    bool ok = true;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int b = i & 1;
+      if (i >= 2 && !ptx::mbar_wait_or_abort(acc_empty(b), ((i >> 1) - 1) & 1, p.timeout_ns, abort_flag)) {
+        if (!*abort_flag) fail(kStatusTimeoutEmpty);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + static_cast<uint32_t>(b) * S::kTmemCols;
+      for (int kb = 0; kb < KT; ++kb, ++g) {
+        const int s = static_cast<int>(g % STAGES);
+        if (!ptx::mbar_wait_or_abort(full_bar(s), (g / STAGES) & 1u, p.timeout_ns, abort_flag)) {
+          if (!*abort_flag) fail(kStatusTimeoutFull);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = smem_base + s * kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < BK / 8; ++kk) {
+          const uint64_t ah = smem_desc_sw128(st + 32 * kk);
+          const uint64_t al = smem_desc_sw128(st + kTileA + 32 * kk);
+          const uint64_t bh = smem_desc_sw128(st + 2 * kTileA + 32 * kk);
+          const uint64_t bl = smem_desc_sw128(st + 2 * kTileA + kTileB + 32 * kk);
+          mma_tf32(d, al, bh, S::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          mma_tf32(d, ah, bl, S::kIdesc, 1u);
+          mma_tf32(d, ah, bh, S::kIdesc, 1u);
+        }
+        mma_commit(empty_bar(s));
+      }
+      if (ok) mma_commit(acc_full(b));
+    }
+    mma_commit(mma_done);  // arrives when every MMA issued above has completed
+  } else if (warp >= 2) {
+    // ---- epilogue: TMEM -> registers -> alpha, beta -> C, tile after tile ----
+    const int lane_base = 32 * (warp & 3);
+    for (int i = 0; i < my_tiles; ++i) {
+      const int b = i & 1;
+      if (!ptx::mbar_wait_or_abort(acc_full(b), (i >> 1) & 1, p.timeout_ns, abort_flag)) {
+        if (!*abort_flag) fail(kStatusTimeoutFull);
+        break;
+      }
+      tc_fence_after();
+      int tm, tn;
+      tile_coords(static_cast<int>(blockIdx.x) + i * G, tiles_m, tiles_n, p.group_m, tm, tn);
+      const int row = tm * BM + lane_base + lane;
+      float* crow = p.C + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll 1
+      for (int cc = 0; cc < BN; cc += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(lane_base) << 16) + static_cast<uint32_t>(b * BN + cc), r);
+        if (row >= p.M) continue;
+        const int col0 = tn * BN + cc;
+        if (p.vec_c && col0 + 32 <= p.N) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float4* dst = reinterpret_cast<float4*>(crow + col0 + j);
+            const float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                         __uint_as_float(r[j + 3]));
+            if (p.beta == 0.f) {
+              *dst = make_float4(p.alpha * v.x, p.alpha * v.y, p.alpha * v.z, p.alpha * v.w);
+            } else {
+              const float4 o = *dst;
+              *dst = make_float4(fmaf(p.alpha, v.x, p.beta * o.x), fmaf(p.alpha, v.y, p.beta * o.y),
+                                 fmaf(p.alpha, v.z, p.beta * o.z), fmaf(p.alpha, v.w, p.beta * o.w));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = col0 + j;
+            if (col < p.N) {
+              const float v = __uint_as_float(r[j]);
+              crow[col] = p.beta == 0.f ? p.alpha * v : fmaf(p.alpha, v, p.beta * crow[col]);
+            }
+          }
+        }
+      }
+      // this warp has read its lanes of accumulator b: release it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(acc_empty(b));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0) ptx::mbar_wait(mma_done, 0, p.timeout_ns);  // no MMA may still write TMEM
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+  }
+}
+
+template <int BN, int STAGES, bool PERSIST = false>
 struct TcVariant {
   using S = TcShape<BN, STAGES>;
-  static constexpr auto kernel = tf32x3_kernel<BN, STAGES>;
+  static constexpr auto kernel = PERSIST ? tf32x3_persistent_kernel<BN, STAGES> : tf32x3_kernel<BN, STAGES>;
   static cudaError_t prepare() {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   }
@@ -389,7 +584,7 @@ struct TcVariant {
   }
   static Variant describe(const char* name) {
     return Variant{name, kKindTc, BM, BN, BK, STAGES, 0, kThreads, S::kSmemBytes, 128, &prepare, &occupancy,
-                   &launch, 0, 0};
+                   &launch, PERSIST ? 1 : 0, 0};
   }
 };
 
@@ -681,6 +876,8 @@ struct TcFusedVariant {
 const Variant kVariants[] = {
     TcVariant<256, 2>::describe("tf32x3_128x256x32_s2"),
     TcVariant<128, 3>::describe("tf32x3_128x128x32_s3"),
+    TcVariant<128, 3, true>::describe("tf32x3p_128x128x32_s3"),
+    TcVariant<256, 2, true>::describe("tf32x3p_128x256x32_s2"),
     TcFusedVariant::describe("tf32x3f_128x128x32_s3"),
 };
 

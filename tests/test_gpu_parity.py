@@ -429,7 +429,8 @@ def test_stream_k_tail(sg, oracle_mod, shape):
 # ---- split-TF32 tensor-core variant (reported apart from the FFMA path) -------
 
 TC = "tf32x3_128x256x32_s2"
-TC_VARIANTS = ["tf32x3_128x256x32_s2", "tf32x3_128x128x32_s3", "tf32x3f_128x128x32_s3"]
+TC_VARIANTS = ["tf32x3_128x256x32_s2", "tf32x3_128x128x32_s3", "tf32x3f_128x128x32_s3", "tf32x3p_128x128x32_s3",
+               "tf32x3p_128x256x32_s2"]
 
 
 @pytest.mark.parametrize("tc", TC_VARIANTS)
