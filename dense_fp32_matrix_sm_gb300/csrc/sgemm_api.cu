@@ -506,6 +506,23 @@ sgemm_status_t encode_maps_tcf(const Variant* v, const sgemm_plan_s* p, const fl
   return SGEMM_OK;
 }
 
+// Whether the address span of C, [C, C + (M-1) ldc + N + (batch-1) stride_c),
+// meets that of operand A (is_a) or B as the caller stores it.
+bool spans_overlap(const sgemm_plan_s* p, const float* C, const float* X, bool is_a) {
+  // stored shapes in row-major terms (a column-major plan holds A and B swapped)
+  const bool internal_a = p->ex_swap ? !is_a : is_a;
+  const int64_t rows = internal_a ? (p->ex_ta ? p->K : p->M) : (p->ex_tb ? p->N : p->K);
+  const int64_t cols = internal_a ? (p->ex_ta ? p->M : p->K) : (p->ex_tb ? p->K : p->N);
+  const int64_t ld = internal_a ? p->ex_lda : p->ex_ldb;
+  const int64_t nb = p->batch > 1 ? p->batch : 1;
+  const int64_t stride = internal_a ? p->stride_a : p->stride_b;
+  const uintptr_t x0 = reinterpret_cast<uintptr_t>(X);
+  const uintptr_t x1 = x0 + static_cast<uintptr_t>(((rows - 1) * ld + cols + (nb - 1) * stride) * 4);
+  const uintptr_t c0 = reinterpret_cast<uintptr_t>(C);
+  const uintptr_t c1 = c0 + static_cast<uintptr_t>(((p->M - 1) * p->ldc + p->N + (nb - 1) * p->stride_c) * 4);
+  return x0 < c1 && c0 < x1;
+}
+
 // Host-to-device copies of one product's inputs (A and B when there is a
 // product, C when beta != 0) with their stored shapes, one 2-D copy per
 // matrix of a batch; and the device-to-host copy of its result.
@@ -647,6 +664,9 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   if (!C) return SGEMM_ERR_INVALID_ARG;
   const bool product = p->K > 0 && alpha != 0.f;
   if (product && (!A || !B)) return SGEMM_ERR_INVALID_ARG;
+  // C may not share its address span with A or B (the kernels read A and B
+  // while other CTAs write C): a conservative span test, rows included
+  if (product && (spans_overlap(p, C, A, true) || spans_overlap(p, C, B, false))) return SGEMM_ERR_UNSUPPORTED;
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess) return SGEMM_ERR_CUDA;
   if (device != p->device) return SGEMM_ERR_INVALID_ARG;

@@ -38,7 +38,9 @@
  *   - M == 0 or N == 0: nothing is launched, SGEMM_OK.
  *   - K == 0 or alpha == 0: C = beta * C; A and B are not read.
  *   - beta == 0: C is not read (NaN or garbage in C does not propagate).
- *   - A, B and C must not overlap; the library does not check this.
+ *   - C must not share its address span (first to last element, rows and
+ *     padding included) with A or B: sgemm_run returns
+ *     SGEMM_ERR_UNSUPPORTED when they meet. A and B may overlap each other.
  *   - Any alignment and any leading dimension is accepted.  Fast paths
  *     need A and B 16-byte aligned with lda % 4 == 0 and ldb % 4 == 0; other
  *     inputs run a GPU kernel with scalar loads (there is no CPU path).

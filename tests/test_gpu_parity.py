@@ -694,3 +694,18 @@ def test_ffma_probe(sg):
         assert 300.0 < mhz < 3500.0, mhz
         nominal = sms * 128 * 2 * mhz * 1e6 / 1e12
         assert 0.5 * nominal < tflops < 1.05 * nominal, (paired, tflops, nominal)
+
+
+def test_c_overlapping_a_or_b_is_refused(sg):
+    M, N, K = 64, 64, 64
+    buf = torch.zeros(3 * 64 * 64, device="cuda")
+    plan = sg.Plan(M, N, K)
+    a, b, c = buf.data_ptr(), buf.data_ptr() + 4 * 64 * 64, buf.data_ptr() + 8 * 64 * 64
+    plan.run(1.0, a, b, 0.0, c)  # disjoint spans: fine
+    for cc in (a, b, b + 4 * 100):
+        with pytest.raises(sg.SgemmError) as e:
+            plan.run(1.0, a, b, 0.0, cc)
+        assert e.value.status == sg.SGEMM_ERR_UNSUPPORTED
+    plan.run(1.0, a, a, 0.0, c)  # A and B may alias each other
+    torch.cuda.synchronize()
+    plan.close()
