@@ -577,6 +577,10 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
       }
     }
     __syncthreads();  // the next piece rewrites `partial`
+    // every thread has read the contributors' partials: clear their flags, so
+    // each run (a replayed graph included, whose epoch is fixed) starts from zero
+    if (threadIdx.x == 0)
+      for (int c = c_first; c < b; ++c) *reinterpret_cast<volatile unsigned int*>(p.flags + c) = 0u;
   }
 }
 

@@ -364,6 +364,11 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
           acc[i][j2 + 1].y += v.w;
         }
       }
+      // every thread has read the partials: clear their flags, so each run
+      // (a replayed graph included, whose epoch is fixed) starts from zero
+      __syncthreads();
+      if (threadIdx.x == 0)
+        for (int c = c_first; c < b; ++c) *reinterpret_cast<volatile unsigned int*>(p.flags + c) = 0u;
     }
 
     // ---------------- epilogue ----------------

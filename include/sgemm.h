@@ -51,6 +51,10 @@
  * stream) and returns; results are ready when the stream reaches that point.
  * A plan is immutable after sgemm_plan returns and may be used from several
  * host threads.  No entry point allocates device memory inside sgemm_run.
+ * sgemm_run only encodes tensor maps on the host and launches, so it can be
+ * captured into a CUDA graph once the plan has run once outside capture.
+ * A replayed stream-K launch stays correct: the CTA that consumes a partial
+ * tile clears that tile's flag, so every run leaves the flags at zero.
  * A plan whose description says streamk=1 owns a device workspace (one
  * partial tile and one flag per CTA of its grid), allocated by sgemm_plan
  * and freed by sgemm_plan_destroy; two runs of such a plan must not overlap

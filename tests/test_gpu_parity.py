@@ -709,3 +709,38 @@ def test_c_overlapping_a_or_b_is_refused(sg):
     plan.run(1.0, a, a, 0.0, c)  # A and B may alias each other
     torch.cuda.synchronize()
     plan.close()
+
+
+@pytest.mark.parametrize("shape", [(2048, 2048, 1024), (16, 16384, 4096)])
+def test_stream_k_plan_replays_in_a_cuda_graph(sg, oracle_mod, shape):
+    """A stream-K plan captured in a CUDA graph and replayed on new inputs: the
+    finishers clear the flags they consumed, so the fixed epoch of the
+    captured launch stays valid replay after replay."""
+    M, N, K = shape
+    plan = sg.Plan(M, N, K)
+    info = plan.info()
+    assert info["streamk"] == 1, info
+    dA = torch.zeros(M, K, device="cuda")
+    dB = torch.zeros(K, N, device="cuda")
+    dC = torch.zeros(M, N, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        plan.run(1.0, dA, dB, 0.0, dC, stream=s)  # warm: kernel attributes and modules before capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        plan.run(1.0, dA, dB, 0.0, dC, stream=s)
+    rows, cols = sample_rows_cols(M, N, n_rows=min(M, 128), n_cols=128, seed=1)
+    for rep in range(3):
+        A, B, _ = make_inputs(M, N, K, seed=400 + rep, dist_a=("normal", 1.0), dist_b=("normal", 1.0), dist_c=None)
+        dA.copy_(torch.from_numpy(A))
+        dB.copy_(torch.from_numpy(B))
+        g.replay()
+        torch.cuda.synchronize()
+        assert sg.device_status() == sg.SGEMM_OK
+        Cs = dC.cpu().numpy()[np.ix_(rows, cols)]
+        Cref, S = oracle_mod.sgemm_ref(np.ascontiguousarray(A[rows]), np.ascontiguousarray(B[:, cols]), None, 1.0, 0.0)
+        assert_parity(Cs, Cref, S, K, f"graph replay {rep} of {info['variant']}")
+    plan.close()
