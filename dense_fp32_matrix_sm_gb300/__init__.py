@@ -13,8 +13,10 @@ from ._lib import (  # noqa: F401
     SGEMM_ERR_TIMEOUT,
     SGEMM_ERR_UNSUPPORTED,
     SGEMM_OK,
+    SGEMM_TUNE_TENSOR_CORES,
     Plan,
     SgemmError,
+    autotune,
     config_id,
     config_name,
     config_names,

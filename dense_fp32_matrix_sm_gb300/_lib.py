@@ -21,6 +21,7 @@ SGEMM_ERR_UNSUPPORTED = -2
 SGEMM_ERR_CUDA = -3
 SGEMM_ERR_TIMEOUT = -4
 SGEMM_ERR_NOMEM = -5
+SGEMM_TUNE_TENSOR_CORES = 1
 
 # Every function include/sgemm.h declares, with (restype, argtypes).
 _i64 = ctypes.c_int64
@@ -48,6 +49,8 @@ SIGNATURES = {
                                         ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                         ctypes.POINTER(_vp), _vp]),
     "sgemm_probe_ffma": (_int, [_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
+    "sgemm_plan_autotune": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _int, _vp,
+                                   ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_vp)]),
     "sgemm_plan_batched": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _int,
                                   ctypes.POINTER(_vp)]),
 }
@@ -315,3 +318,25 @@ def probe_ffma(paired: bool = True):
     f = ctypes.c_double()
     _check(lib().sgemm_probe_ffma(1 if paired else 0, ctypes.byref(t), ctypes.byref(f)), "sgemm_probe_ffma")
     return t.value, f.value
+
+
+def autotune(M: int, N: int, K: int, A, B, C, lda: Optional[int] = None, ldb: Optional[int] = None,
+             ldc: Optional[int] = None, tensor_cores: bool = False, stream=None, with_times: bool = False):
+    """Time every variant that takes this shape on the scratch buffers A, B, C (C is overwritten) and
+    return a Plan for the fastest; with_times also returns {variant name: ms per run}."""
+    M, N, K = int(M), int(N), int(K)
+    lda = int(lda) if lda is not None else max(1, K)
+    ldb = int(ldb) if ldb is not None else max(1, N)
+    ldc = int(ldc) if ldc is not None else max(1, N)
+    n = num_configs()
+    times = (ctypes.c_double * n)() if with_times else None
+    h = ctypes.c_void_p()
+    _check(lib().sgemm_plan_autotune(M, N, K, lda, ldb, ldc, _ptr(A), _ptr(B), _ptr(C),
+                                     SGEMM_TUNE_TENSOR_CORES if tensor_cores else 0, _stream_handle(stream),
+                                     times, ctypes.byref(h)), "sgemm_plan_autotune")
+    plan = Plan.__new__(Plan)
+    plan.M, plan.N, plan.K, plan.lda, plan.ldb, plan.ldc = M, N, K, lda, ldb, ldc
+    plan._h = h
+    if not with_times:
+        return plan
+    return plan, {config_name(i): times[i] for i in range(n) if times[i] >= 0}

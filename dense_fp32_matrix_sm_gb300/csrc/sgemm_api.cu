@@ -10,6 +10,8 @@
 
 #include <algorithm>
 #include <atomic>
+#include <map>
+#include <tuple>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -506,6 +508,20 @@ sgemm_status_t encode_maps_tcf(const Variant* v, const sgemm_plan_s* p, const fl
   return SGEMM_OK;
 }
 
+// Autotuning cache: (device, shape, leading dimensions, tensor cores
+// allowed) -> the fastest variant measured by sgemm_plan_autotune.
+struct TuneKey {
+  int device;
+  int64_t M, N, K, lda, ldb, ldc;
+  bool tensor;
+  bool operator<(const TuneKey& o) const {
+    return std::tie(device, M, N, K, lda, ldb, ldc, tensor) <
+           std::tie(o.device, o.M, o.N, o.K, o.lda, o.ldb, o.ldc, o.tensor);
+  }
+};
+std::mutex g_tune_mutex;
+std::map<TuneKey, int> g_tune_cache;
+
 // Whether the address span of C, [C, C + (M-1) ldc + N + (batch-1) stride_c),
 // meets that of operand A (is_a) or B as the caller stores it.
 bool spans_overlap(const sgemm_plan_s* p, const float* C, const float* X, bool is_a) {
@@ -577,6 +593,76 @@ sgemm_status_t sgemm_plan_with_config(int64_t M, int64_t N, int64_t K, int64_t l
                                       int config_id, sgemm_plan_t* out) {
   if (config_id < 0) return SGEMM_ERR_INVALID_ARG;
   return make_plan(M, N, K, lda, ldb, ldc, config_id, out);
+}
+
+sgemm_status_t sgemm_plan_autotune(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                   const float* A, const float* B, float* C, int flags, void* stream_,
+                                   double* times_ms, sgemm_plan_t* out) {
+  if (!out) return SGEMM_ERR_INVALID_ARG;
+  sgemm_status_t st = check_dims(M, N, K, lda, ldb, ldc);
+  if (st != SGEMM_OK) return st;
+  if ((flags & ~SGEMM_TUNE_TENSOR_CORES) != 0) return SGEMM_ERR_INVALID_ARG;
+  const Registry& reg = registry();
+  const int nv = static_cast<int>(reg.all.size());
+  if (times_ms)
+    for (int i = 0; i < nv; ++i) times_ms[i] = -1.0;
+  if (M == 0 || N == 0 || K == 0) return make_plan(M, N, K, lda, ldb, ldc, -1, out);  // nothing to time
+  if (!A || !B || !C) return SGEMM_ERR_INVALID_ARG;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return SGEMM_ERR_CUDA;
+  const bool tensor = (flags & SGEMM_TUNE_TENSOR_CORES) != 0;
+  const TuneKey key{device, M, N, K, lda, ldb, ldc, tensor};
+  {
+    std::lock_guard<std::mutex> lock(g_tune_mutex);
+    auto it = g_tune_cache.find(key);
+    if (it != g_tune_cache.end() && !times_ms) return make_plan(M, N, K, lda, ldb, ldc, it->second, out);
+  }
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    if (e0) cudaEventDestroy(e0);
+    return SGEMM_ERR_CUDA;
+  }
+  constexpr int kReps = 5;
+  int best = -1;
+  double best_ms = 0.0;
+  st = SGEMM_OK;
+  for (int id = 0; id < nv && st == SGEMM_OK; ++id) {
+    const Variant* v = reg.all[id];
+    if (!tensor && (v->kind == kKindTc || v->kind == kKindTcFused)) continue;
+    sgemm_plan_t p = nullptr;
+    if (make_plan(M, N, K, lda, ldb, ldc, id, &p) != SGEMM_OK) continue;  // this variant does not take the shape
+    // one warm run (kernel attributes, modules, TMA descriptors), then kReps timed back to back
+    if (sgemm_run(p, 1.0f, A, B, 0.0f, C, stream_) != SGEMM_OK) {
+      sgemm_plan_destroy(p);
+      continue;  // e.g. the fused form refuses unaligned buffers
+    }
+    float ms = 0.f;
+    bool ok = cudaEventRecord(e0, stream) == cudaSuccess;
+    for (int r = 0; r < kReps && ok; ++r) ok = sgemm_run(p, 1.0f, A, B, 0.0f, C, stream_) == SGEMM_OK;
+    ok = ok && cudaEventRecord(e1, stream) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess &&
+         cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess;
+    sgemm_plan_destroy(p);
+    if (!ok) {
+      st = SGEMM_ERR_CUDA;
+      break;
+    }
+    const double per = static_cast<double>(ms) / kReps;
+    if (times_ms) times_ms[id] = per;
+    if (best < 0 || per < best_ms) {
+      best = id;
+      best_ms = per;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (st != SGEMM_OK) return st;
+  if (best < 0) return SGEMM_ERR_UNSUPPORTED;
+  {
+    std::lock_guard<std::mutex> lock(g_tune_mutex);
+    g_tune_cache[key] = best;
+  }
+  return make_plan(M, N, K, lda, ldb, ldc, best, out);
 }
 
 sgemm_status_t sgemm_plan_batched(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,

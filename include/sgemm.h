@@ -113,6 +113,44 @@ sgemm_status_t sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
 sgemm_status_t sgemm_plan_with_config(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                       int64_t ldc, int config_id, sgemm_plan_t *out);
 
+/* Flags for sgemm_plan_autotune. */
+enum { SGEMM_TUNE_TENSOR_CORES = 1 };
+
+/*
+ * Autotuning: time every variant that takes this shape and return a plan
+ * for the fastest. The pages autotune the kernel's tile parameters by
+ * compiling every legal configuration, running it and keeping the winner
+ * ("How a Matmul Kernel Gets Fast", the autotuning step). Here the compiled
+ * configurations are this build's variants.
+ *
+ * Arguments:
+ *   - A, B, C: scratch device buffers of the plan's shape and leading
+ *     dimensions. C is overwritten (the timing runs use alpha = 1,
+ *     beta = 0).
+ *   - flags: SGEMM_TUNE_TENSOR_CORES also tries the split-TF32
+ *     tensor-core variants, which compute differently (see above). By
+ *     default only the FP32 FFMA variants compete.
+ *   - times_ms: if not NULL, receives sgemm_num_configs() entries, the mean
+ *     time per run of each variant (-1 where a variant was not tried).
+ *   - stream: the stream the timing runs go on.
+ *
+ * Timing: each variant gets one warm run, then 5 runs back to back timed
+ * with CUDA events on `stream`. L2 is not flushed between runs, so operands
+ * that fit in L2 stay hot.
+ *
+ * Cache: winners are cached per (device, shape, leading dimensions,
+ * flags). A later call with times_ms == NULL returns the cached choice
+ * without timing.
+ *
+ * Behaviour: synchronous (it waits for the timing runs).
+ *
+ * Errors: as sgemm_plan. SGEMM_ERR_UNSUPPORTED if no variant could run.
+ * M, N or K of 0 gives the table's plan without timing.
+ */
+sgemm_status_t sgemm_plan_autotune(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                   const float *A, const float *B, float *C, int flags, void *stream,
+                                   double *times_ms, sgemm_plan_t *out);
+
 /*
  * Plan a strided batch of `batch` independent products of one shape:
  * C_z = alpha * A_z * B_z + beta * C_z, z = 0 .. batch-1, with

@@ -85,6 +85,15 @@ def test_plan_ex_rejects_before_cuda(lib):
     assert not h.value
 
 
+def test_autotune_rejects_bad_arguments_before_cuda(lib):
+    h = ctypes.c_void_p()
+    f = lib.sgemm_plan_autotune
+    assert f(64, 64, 64, 63, 64, 64, 16, 16, 16, 0, None, None, ctypes.byref(h)) == -1   # lda < K
+    assert f(64, 64, 64, 64, 64, 64, 16, 16, 16, 4, None, None, ctypes.byref(h)) == -1   # unknown flag
+    assert f(64, 64, 64, 64, 64, 64, None, 16, 16, 0, None, None, ctypes.byref(h)) == -1  # no scratch A
+    assert f(64, 64, 64, 64, 64, 64, 16, 16, 16, 0, None, None, None) == -1              # no output
+
+
 def test_probe_rejects_bad_arguments_before_cuda(lib):
     t = ctypes.c_double()
     assert lib.sgemm_probe_ffma(1, None, ctypes.byref(t)) == -1

@@ -744,3 +744,23 @@ def test_stream_k_plan_replays_in_a_cuda_graph(sg, oracle_mod, shape):
         Cref, S = oracle_mod.sgemm_ref(np.ascontiguousarray(A[rows]), np.ascontiguousarray(B[:, cols]), None, 1.0, 0.0)
         assert_parity(Cs, Cref, S, K, f"graph replay {rep} of {info['variant']}")
     plan.close()
+
+
+def test_autotune_picks_the_fastest_and_caches_it(sg, oracle_mod):
+    M, N, K = 1000, 1100, 512
+    dA = torch.randn(M, K, device="cuda")
+    dB = torch.randn(K, N, device="cuda")
+    dC = torch.empty(M, N, device="cuda")
+    plan, times = sg.autotune(M, N, K, dA, dB, dC, with_times=True)
+    assert times and plan.config_name == min(times, key=times.get)
+    assert not any(n.startswith("tf32x3") for n in times)  # FFMA variants only by default
+    again = sg.autotune(M, N, K, dA, dB, dC)  # cached: same choice, no timing
+    assert again.config_name == plan.config_name
+    A, B, C0 = make_inputs(M, N, K, seed=9, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
+    C, used = run_gpu(sg, A, B, C0, 0.5, 2.0, config=plan.config_name)
+    Cref, S = oracle_mod.sgemm_ref(A, B, C0, 0.5, 2.0)
+    assert_parity(C, Cref, S, K, f"autotuned {used}")
+    _, with_tc = sg.autotune(M, N, K, dA, dB, dC, tensor_cores=True, with_times=True)
+    assert any(n.startswith("tf32x3") for n in with_tc)
+    plan.close()
+    again.close()
