@@ -179,28 +179,33 @@ cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaSt
 }
 
 // out (cols x rows, ld_out) = transpose of in (rows x cols, ld_in), through a
-// 32 x 33 shared tile so both the reads and the writes are coalesced.
+// 32 x 33 shared tile so both the reads and the writes are coalesced.  Block
+// row blockIdx.y takes row tiles blockIdx.y, + gridDim.y, ... (any row count).
 __global__ void transpose_kernel(const float* __restrict__ in, int64_t ld_in, int rows, int cols,
                                  float* __restrict__ out, int64_t ld_out) {
   __shared__ float t[32][33];
   const int c0 = blockIdx.x * 32;
-  const int r0 = blockIdx.y * 32;
-  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-    const int r = r0 + j, c = c0 + threadIdx.x;
-    if (r < rows && c < cols) t[j][threadIdx.x] = in[static_cast<int64_t>(r) * ld_in + c];
-  }
-  __syncthreads();
-  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-    const int c = c0 + j, r = r0 + threadIdx.x;
-    if (c < cols && r < rows) out[static_cast<int64_t>(c) * ld_out + r] = t[threadIdx.x][j];
+  const int row_tiles = (rows + 31) / 32;
+  for (int ty = blockIdx.y; ty < row_tiles; ty += gridDim.y) {
+    const int r0 = ty * 32;
+    for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+      const int r = r0 + j, c = c0 + threadIdx.x;
+      if (r < rows && c < cols) t[j][threadIdx.x] = in[static_cast<int64_t>(r) * ld_in + c];
+    }
+    __syncthreads();
+    for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+      const int c = c0 + j, r = r0 + threadIdx.x;
+      if (c < cols && r < rows) out[static_cast<int64_t>(c) * ld_out + r] = t[threadIdx.x][j];
+    }
+    __syncthreads();  // the tile is refilled by the next row tile
   }
 }
 
 cudaError_t launch_transpose(const float* in, int64_t ld_in, int rows, int cols, float* out, int64_t ld_out,
                              cudaStream_t stream) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
-  const dim3 grid((cols + 31) / 32, (rows + 31) / 32);
-  if (grid.y > 65535u) return cudaErrorInvalidValue;
+  const int row_tiles = (rows + 31) / 32;
+  const dim3 grid((cols + 31) / 32, row_tiles < 65535 ? row_tiles : 65535);
   transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(in, ld_in, rows, cols, out, ld_out);
   return cudaGetLastError();
 }

@@ -71,8 +71,6 @@ __device__ __forceinline__ unsigned int atom_add_acq_rel_cta(unsigned int* addr,
   return old;
 }
 
-// Order this thread's generic-proxy shared-memory accesses before later
-// async-proxy (TMA) accesses to the same memory.
 // Flag handshake between CTAs of one grid (stream-K partial tiles): the
 // writer releases after its data stores, the reader acquires before its loads.
 __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
@@ -85,6 +83,8 @@ __device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) 
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Order this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

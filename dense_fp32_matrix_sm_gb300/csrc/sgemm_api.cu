@@ -888,14 +888,25 @@ sgemm_status_t sgemm_run_host_pipelined(sgemm_plan_t plan, int count, float alph
   {
     std::lock_guard<std::mutex> lock(p->pipe_mutex);
     if (!p->pipe_ready) {
-      if (cudaStreamCreateWithFlags(&p->pipe_h2d, cudaStreamNonBlocking) != cudaSuccess) return SGEMM_ERR_CUDA;
-      if (cudaStreamCreateWithFlags(&p->pipe_d2h, cudaStreamNonBlocking) != cudaSuccess) {
-        cudaStreamDestroy(p->pipe_h2d);
+      // create everything or nothing: a failure destroys what was made
+      cudaStream_t s[2] = {nullptr, nullptr};
+      cudaEvent_t ev[2][3] = {{nullptr, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+      bool ok = cudaStreamCreateWithFlags(&s[0], cudaStreamNonBlocking) == cudaSuccess &&
+                cudaStreamCreateWithFlags(&s[1], cudaStreamNonBlocking) == cudaSuccess;
+      for (int b = 0; b < 2 && ok; ++b)
+        for (int e = 0; e < 3 && ok; ++e) ok = cudaEventCreateWithFlags(&ev[b][e], cudaEventDisableTiming) == cudaSuccess;
+      if (!ok) {
+        for (int b = 0; b < 2; ++b)
+          for (int e = 0; e < 3; ++e)
+            if (ev[b][e]) cudaEventDestroy(ev[b][e]);
+        for (int i = 0; i < 2; ++i)
+          if (s[i]) cudaStreamDestroy(s[i]);
         return SGEMM_ERR_CUDA;
       }
+      p->pipe_h2d = s[0];
+      p->pipe_d2h = s[1];
       for (int b = 0; b < 2; ++b)
-        for (int e = 0; e < 3; ++e)
-          if (cudaEventCreateWithFlags(&p->pipe_ev[b][e], cudaEventDisableTiming) != cudaSuccess) return SGEMM_ERR_CUDA;
+        for (int e = 0; e < 3; ++e) p->pipe_ev[b][e] = ev[b][e];
       p->pipe_ready = true;
     }
   }

@@ -132,26 +132,38 @@ void launch_split_rows(const float* X, int64_t ldx, int rows, int cols, float* h
   }
 }
 
-// X (rows x cols, ldx) -> hi, lo transposed (cols x rows, ldh).
+// X (rows x cols, ldx) -> hi, lo transposed (cols x rows, ldh).  Block row
+// blockIdx.y takes row tiles blockIdx.y, + gridDim.y, ... (any row count).
 __global__ void split_transpose_kernel(const float* __restrict__ X, int64_t ldx, int rows, int cols,
                                        float* __restrict__ hi, float* __restrict__ lo, int64_t ldh) {
   __shared__ float t[32][33];
   const int c0 = blockIdx.x * 32;
-  const int r0 = blockIdx.y * 32;
-  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-    const int r = r0 + j, c = c0 + threadIdx.x;
-    t[j][threadIdx.x] = (r < rows && c < cols) ? X[static_cast<int64_t>(r) * ldx + c] : 0.f;
-  }
-  __syncthreads();
-  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-    const int c = c0 + j, r = r0 + threadIdx.x;  // output row c, column r
-    if (c < cols && r < rows) {
-      const float x = t[threadIdx.x][j];
-      const float h = to_tf32(x);
-      hi[static_cast<int64_t>(c) * ldh + r] = h;
-      lo[static_cast<int64_t>(c) * ldh + r] = to_tf32(x - h);
+  const int row_tiles = (rows + 31) / 32;
+  for (int ty = blockIdx.y; ty < row_tiles; ty += gridDim.y) {
+    const int r0 = ty * 32;
+    for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+      const int r = r0 + j, c = c0 + threadIdx.x;
+      t[j][threadIdx.x] = (r < rows && c < cols) ? X[static_cast<int64_t>(r) * ldx + c] : 0.f;
     }
+    __syncthreads();
+    for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+      const int c = c0 + j, r = r0 + threadIdx.x;  // output row c, column r
+      if (c < cols && r < rows) {
+        const float x = t[threadIdx.x][j];
+        const float h = to_tf32(x);
+        hi[static_cast<int64_t>(c) * ldh + r] = h;
+        lo[static_cast<int64_t>(c) * ldh + r] = to_tf32(x - h);
+      }
+    }
+    __syncthreads();  // the tile is refilled by the next row tile
   }
+}
+
+void launch_split_transpose(const float* X, int64_t ldx, int rows, int cols, float* hi, float* lo, int64_t ldh,
+                            cudaStream_t stream) {
+  const int row_tiles = (rows + 31) / 32;
+  const dim3 grid((cols + 31) / 32, row_tiles < 65535 ? row_tiles : 65535);
+  split_transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(X, ldx, rows, cols, hi, lo, ldh);
 }
 
 // Shared-memory matrix descriptor: K-major operand, rows of 128 bytes with
@@ -347,16 +359,14 @@ void launch_split(const LaunchArgs& a, cudaStream_t stream) {
   float* bl = bh + static_cast<int64_t>(a.N) * kp;
   // both operands end K-major: A as M x kp, B as N x kp
   if (a.a_trans) {  // A stored K x M
-    split_transpose_kernel<<<dim3((a.M + 31) / 32, (a.K + 31) / 32), dim3(32, 8), 0, stream>>>(a.A, a.lda, a.K, a.M,
-                                                                                            ah, al, kp);
+    launch_split_transpose(a.A, a.lda, a.K, a.M, ah, al, kp, stream);
   } else {
     launch_split_rows(a.A, a.lda, a.M, a.K, ah, al, kp, stream);
   }
   if (a.b_trans) {  // B stored N x K: already K-major
     launch_split_rows(a.B, a.ldb, a.N, a.K, bh, bl, kp, stream);
   } else {
-    split_transpose_kernel<<<dim3((a.N + 31) / 32, (a.K + 31) / 32), dim3(32, 8), 0, stream>>>(a.B, a.ldb, a.K, a.N,
-                                                                                            bh, bl, kp);
+    launch_split_transpose(a.B, a.ldb, a.K, a.N, bh, bl, kp, stream);
   }
 }
 

@@ -524,6 +524,28 @@ def test_order_and_transpose(sg, oracle_mod, order, ta, tb, shape, config, pad):
     assert_parity(C, Cref, S, K, f"{order} op={info['op']} {shape} {info['variant']}")
 
 
+@pytest.mark.parametrize("config", [None, "tf32x3_128x128x32_s3"])
+def test_transposed_operand_with_more_than_65535_row_tiles(sg, oracle_mod, config):
+    """A stored K x M with K > 65535 * 32: the transposing kernels walk row
+    tiles past the grid's y limit."""
+    M, N, K = 8, 8, 2_100_000
+    opA, opB, C0 = make_inputs(M, N, K, seed=77, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
+    Cref, S = oracle_mod.sgemm_ref(opA, opB, C0, 1.0, 0.5)
+    memA, lda = _stored(opA, "row", True, 0)
+    memB, ldb = _stored(opB, "row", False, 0)
+    dA, pA, _ = _to_dev(memA, lda)
+    dB, pB, _ = _to_dev(memB, ldb)
+    dC, pC, _ = _to_dev(C0, N)
+    plan = sg.Plan(M, N, K, lda, ldb, N, config=config, transa=True)
+    plan.run(1.0, pA, pB, 0.5, pC)
+    torch.cuda.synchronize()
+    assert sg.device_status() == sg.SGEMM_OK
+    C = _from_dev(dC, M, N, N)
+    variant = plan.info()["variant"]
+    plan.close()
+    assert_parity(C, Cref, S, K, f"TN K={K} {variant}")
+
+
 def test_order_and_transpose_host_buffers(sg, oracle_mod):
     """sgemm_run_host copies each operand with its stored shape."""
     M, N, K = 150, 90, 70
