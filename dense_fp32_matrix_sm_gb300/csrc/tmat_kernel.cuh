@@ -17,19 +17,23 @@
 //  * TMA copies the A slice [BM][BK] (128-byte swizzle) and the B slice
 //    [BK][BN] into a STAGES-deep ring signalled by mbarriers, as in
 //    tma_kernel.cuh.
-//  * One slice ahead of the math, all threads transpose the A slice into a
-//    double-buffered At[BK][BM]: with T = threads/BM (1, 2 or 4) threads per
-//    row, thread t reads row t/T, k-part t%T (BK/T k, 128-bit loads) and
-//    writes At[k][m ^ (32/T)*(k / (BK/T))].  The XOR puts the T k-parts of
+//  * While the math runs on slice j, all threads transpose the A slice j+1
+//    into a double-buffered At[BK][BM]: with T = threads/BM (1, 2 or 4)
+//    threads per row, thread t reads row t/T, k-part t%T (BK/T k, 128-bit
+//    loads) and writes At[k][m ^ (32/T)*(k / (BK/T))].  The copy sits at a
+//    fixed step of the unrolled k loop (TA), or in two halves (TA, TB), so
+//    its wait and its load-to-store latency hide behind FFMA2s; placed
+//    before the loop instead it cost 3.5% at 4096^3 (measured on GB300).  The XOR puts the T k-parts of
 //    a warp's 32/T rows in different bank groups (conflict-free writes) and
 //    keeps pairs (m, m+1) adjacent.
 //    ("Learn: Optimizing GEMM", section 7, and "Writing a Fast Matmul in
 //    CUDA", Step 5: A stored transposed so the inner loop reads contiguous
 //    m -- here the transpose runs on the on-chip copy instead of on the
 //    global loads.)
-//  * One CTA barrier per slice: after it the next transposed slice is
+//  * One plain CTA barrier per slice: after it the next transposed slice is
 //    complete and the current ring stage is free; thread 0 then refills
-//    that stage with the slice STAGES ahead.
+//    that stage with the slice STAGES ahead.  A wait that runs out sets a
+//    shared flag before the barrier, so every thread leaves together.
 //  * Warps own 64 x 32 tiles; lane (g, c) owns rows 16i + 2g + e and
 //    columns 4c + 16h + j; per k: four 64-bit A-pair loads, two 128-bit B
 //    loads, 32 FFMA2.
@@ -101,14 +105,18 @@ struct Shape {
   static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * kAtBytes + STAGES * 8 + 1024;
 };
 
-template <int BM_, int BN, int STAGES, int MINB, bool BATCHED>
+// The next slice is transposed at step k == TA of the current one's k loop
+// (all of it when TB < 0, else the first half, the second at k == TB).
+template <int BM_, int BN, int STAGES, int MINB, bool BATCHED, int TA, int TB>
 __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
     sgemm_tmat_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const Params p) {
   using S = Shape<BM_, BN, STAGES>;
   constexpr int BM = S::BM;
   constexpr int BK = S::BK;
+  static_assert(TA >= 0 && TA < BK && TB < BK && (TB < 0 || TB > TA), "transpose steps inside the k loop");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ int s_fail;
   const uint32_t raw_base = ptx::smem_addr(smem_raw);
   unsigned char* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
   const uint32_t smem_base = ptx::smem_addr(smem);
@@ -215,6 +223,7 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   };
 
   if (threadIdx.x == 0) {
+    s_fail = 0;
     for (int s = 0; s < STAGES; ++s) ptx::mbar_init(bar_full + 8 * s, 1);
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tmA);
@@ -229,16 +238,17 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   const int at_col = tr ^ (S::kSwz * th);  // k / kKPart == th for every k this thread writes
   bool failed;
   // Transpose A of slice j (ring stage j % STAGES) into at_buf[j & 1].
-  auto transpose = [&](uint32_t j) -> bool {
+  // chunks [q0, q1) of this thread's part; `wait` first waits for the slice
+  auto transpose_part = [&](uint32_t j, int q0, int q1, bool wait) -> bool {
     const uint32_t s = j % STAGES;
-    if (!ptx::mbar_wait(bar_full + 8 * s, (j / STAGES) & 1u, p.timeout_ns)) {
+    if (wait && !ptx::mbar_wait(bar_full + 8 * s, (j / STAGES) & 1u, p.timeout_ns)) {
       atomicOr(p.status, kStatusTimeoutFull);
       return false;
     }
     const float* As = reinterpret_cast<const float*>(smem + s * S::kStageBytes) + tr * BK;
     float* At = at_buf + (j & 1) * (BK * BM);
 #pragma unroll
-    for (int q = 0; q < S::kKPart / 4; ++q) {
+    for (int q = q0; q < q1; ++q) {
       const int chunk = (S::kKPart / 4) * th + q;  // k = 4*chunk .. +3
       const float4 v = *reinterpret_cast<const float4*>(As + ((chunk ^ (tr & 7)) << 2));
       const float e4[4] = {v.x, v.y, v.z, v.w};
@@ -247,6 +257,7 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
     }
     return true;
   };
+  auto transpose = [&](uint32_t j) -> bool { return transpose_part(j, 0, S::kKPart / 4, true); };
 
   const int wm = warp / S::kWarpsN;
   const int wn = warp % S::kWarpsN;
@@ -278,8 +289,8 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
       for (int j = 0; j < 8; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
     for (int kt = seg_k0; kt < seg_k1; ++kt, ++it) {
-      // the next slice's A, transposed ahead (its buffer was last read one slice ago)
-      const bool bad = it + 1 < total_it && !transpose(it + 1);
+      // the next slice's A is transposed during this one (its buffer was last read one slice ago)
+      bool bad = false;
       const uint32_t s = it % STAGES;
       const float* At = at_buf + (it & 1) * (BK * BM);
       const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + (wn * 32 + 4 * c) / 4;
@@ -297,6 +308,13 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
       load_ops(0, apn, b0n, b1n);
 #pragma unroll
       for (int k = 0; k < BK; ++k) {
+        constexpr int kNq = S::kKPart / 4;
+        if constexpr (TB >= 0) {  // in two halves
+          if (k == TA) bad = it + 1 < total_it && !transpose_part(it + 1, 0, kNq / 2, true);
+          if (k == TB && it + 1 < total_it && !bad) transpose_part(it + 1, kNq / 2, kNq, false);
+        } else {
+          if (k == TA) bad = it + 1 < total_it && !transpose(it + 1);
+        }
         float2 ap[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) ap[i] = apn[i];
@@ -308,7 +326,9 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
           for (int j = 0; j < 8; ++j) acc[i][j] = __ffma2_rn(ap[i], make_float2(bb[j], bb[j]), acc[i][j]);
       }
       // every warp is done with stage s and At[it & 1]; At[(it+1) & 1] is complete
-      failed = __syncthreads_or(bad) != 0;
+      if (bad) *reinterpret_cast<volatile int*>(&s_fail) = 1;
+      __syncthreads();
+      failed = *reinterpret_cast<volatile int*>(&s_fail) != 0;
       if (failed) break;
       if (threadIdx.x == 0 && it + STAGES < total_it) {
         ptx::fence_proxy_async_smem();
@@ -411,12 +431,12 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   }
 }
 
-template <int BM_, int BN, int STAGES, int MINB>
+template <int BM_, int BN, int STAGES, int MINB, int TA, int TB = -1>
 struct Variant_ {
   using S = Shape<BM_, BN, STAGES>;
   // a single product runs the plain 2-D kernel; strided batches their own instantiation
-  static constexpr auto kernel = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, false>;
-  static constexpr auto kernel_batched = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, true>;
+  static constexpr auto kernel = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, false, TA, TB>;
+  static constexpr auto kernel_batched = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, true, TA, TB>;
   static cudaError_t prepare() {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     return e != cudaSuccess ? e

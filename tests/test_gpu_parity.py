@@ -121,7 +121,7 @@ def _shape_cases(n=40, seed=0):
     return sorted(cases)
 
 
-@pytest.mark.parametrize("variant_idx", range(40))
+@pytest.mark.parametrize("variant_idx", range(48))
 def test_shape_sweep_every_variant(sg, oracle_mod, variant_idx):
     names = _variants(sg)
     if variant_idx >= len(names):
