@@ -43,12 +43,25 @@ FMA_LANES_PER_SM = 128          # FP32 lanes per SM (4 sub-partitions x 32)
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ["tma_kernel.cuh", "cpa_kernel.cuh", "tmat_kernel.cuh", "tile_order.cuh", "kernel_skinny.cu", "kernel_generic.cu", "ptx.cuh", "kernels.h"]
+# The sources a variant family's kernel is built from: a traffic figure in
+# profiles/traffic.json stays valid while their hash is unchanged.
+KERNEL_SOURCES = {
+    "tmat_": ["tmat_kernel.cuh", "tmat_variants.cu", "tile_order.cuh", "ptx.cuh", "kernels.h"],
+    "skinny": ["kernel_skinny.cu", "ptx.cuh", "kernels.h"],
+    "tma_": ["tma_kernel.cuh", "tma_variants_a.cu", "tma_variants_b.cu", "tma_variants_c.cu", "tile_order.cuh", "ptx.cuh",
+             "kernels.h"],
+    "cpa_": ["cpa_kernel.cuh", "cpa_variants.cu", "tile_order.cuh", "ptx.cuh", "kernels.h"],
+    "tf32x3": ["tc_tf32x3.cu", "ptx.cuh", "kernels.h"],
+    "generic": ["kernel_generic.cu", "kernels.h"],
+}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(variant: str) -> str:
+    """Hash of the sources of `variant`'s kernel family (all kernel sources for an unknown family)."""
+    names = next((v for k, v in KERNEL_SOURCES.items() if variant.startswith(k)),
+                 sorted({n for v in KERNEL_SOURCES.values() for n in v}))
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in names:
         p = os.path.join(ROOT, "dense_fp32_matrix_sm_gb300", "csrc", name)
         if os.path.exists(p):
             h.update(open(p, "rb").read())
@@ -401,7 +414,7 @@ def run_ours(args):
     if os.path.exists(TRAFFIC_FILE):
         try:
             rec = json.load(open(TRAFFIC_FILE)).get(f"{info.get('variant')}|{w.name}")
-            if rec and rec.get("kernel_source_sha") == kernel_source_hash():
+            if rec and rec.get("kernel_source_sha") == kernel_source_hash(str(info.get("variant"))):
                 traffic = rec.get("dram_bytes_per_launch")
         except (ValueError, OSError):
             traffic = None
