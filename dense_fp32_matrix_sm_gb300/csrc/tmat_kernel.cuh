@@ -34,6 +34,13 @@
 //    complete and the current ring stage is free; thread 0 then refills
 //    that stage with the slice STAGES ahead.  A wait that runs out sets a
 //    shared flag before the barrier, so every thread leaves together.
+//  * Or (SPLIT) the barrier's two jobs go to two pairs of mbarriers, so
+//    warps may drift apart by most of a slice: "slice j+1 transposed"
+//    (arrived after the copy, waited before slice j+1) and "slice j done"
+//    (arrived after the k loop, waited before the copy in slice j+1, which
+//    overwrites At[j & 1]; thread 0 then refills slice j's stage).  Waits
+//    stop early once any thread has failed, and the threads agree on
+//    failure with one CTA barrier per segment.
 //  * Warps own 64 x 32 tiles; lane (g, c) owns rows 16i + 2g + e and
 //    columns 4c + 16h + j; per k: four 64-bit A-pair loads, two 128-bit B
 //    loads, 32 FFMA2.
@@ -107,7 +114,12 @@ struct Shape {
 
 // The next slice is transposed at step k == TA of the current one's k loop
 // (all of it when TB < 0, else the first half, the second at k == TB).
-template <int BM_, int BN, int STAGES, int MINB, bool BATCHED, int TA, int TB>
+// SPLIT: split-phase slice synchronisation through mbarriers instead of one
+// CTA barrier per slice: every thread arrives on at_full[(j+1) & 1] after its
+// part of slice j+1's transpose and on slice_done[j & 1] after slice j; it
+// waits on at_full[j & 1] before slice j and on slice_done[(j-1) & 1] before
+// overwriting At[(j+1) & 1], where thread 0 also refills stage (j-1) % STAGES.
+template <int BM_, int BN, int STAGES, int MINB, bool BATCHED, int TA, int TB, bool SPLIT>
 __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
     sgemm_tmat_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const Params p) {
@@ -117,6 +129,7 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   static_assert(TA >= 0 && TA < BK && TB < BK && (TB < 0 || TB > TA), "transpose steps inside the k loop");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ int s_fail;
+  __shared__ __align__(8) unsigned long long s_sync[4];  // SPLIT: at_full[2], slice_done[2]
   const uint32_t raw_base = ptx::smem_addr(smem_raw);
   unsigned char* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
   const uint32_t smem_base = ptx::smem_addr(smem);
@@ -225,6 +238,8 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   if (threadIdx.x == 0) {
     s_fail = 0;
     for (int s = 0; s < STAGES; ++s) ptx::mbar_init(bar_full + 8 * s, 1);
+    if constexpr (SPLIT)
+      for (int i = 0; i < 4; ++i) ptx::mbar_init(ptx::smem_addr(&s_sync[i]), S::kThreads);
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tmA);
     ptx::prefetch_tensormap(&tmB);
@@ -288,9 +303,27 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
+    const uint32_t at_full0 = ptx::smem_addr(&s_sync[0]);
+    const uint32_t done0 = ptx::smem_addr(&s_sync[2]);
+    // SPLIT: a bounded wait that gives up as soon as another thread failed; warp-uniform result
+    auto split_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+      const bool ok = ptx::mbar_wait_or_abort(bar, parity, p.timeout_ns, &s_fail);
+      if (!ok) {
+        atomicOr(p.status, kStatusTimeoutFull);
+        *reinterpret_cast<volatile int*>(&s_fail) = 1;
+      }
+      return __all_sync(0xffffffffu, ok);
+    };
     for (int kt = seg_k0; kt < seg_k1; ++kt, ++it) {
       // the next slice's A is transposed during this one (its buffer was last read one slice ago)
       bool bad = false;
+      if constexpr (SPLIT) {
+        // At[it & 1] is complete once every thread has transposed its part (slice 0: the prologue barrier)
+        if (it >= 1 && !split_wait(at_full0 + 8 * (it & 1), ((it - 1) >> 1) & 1u)) {
+          failed = true;
+          break;
+        }
+      }
       const uint32_t s = it % STAGES;
       const float* At = at_buf + (it & 1) * (BK * BM);
       const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + (wn * 32 + 4 * c) / 4;
@@ -309,11 +342,24 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
 #pragma unroll
       for (int k = 0; k < BK; ++k) {
         constexpr int kNq = S::kKPart / 4;
+        if constexpr (SPLIT) {
+          if (k == TA && it >= 1) {
+            // every thread is done with slice it-1: At[(it+1) & 1] and stage (it-1) % STAGES are free
+            bad = !split_wait(done0 + 8 * ((it - 1) & 1), ((it - 1) >> 1) & 1u);
+            if (!bad && threadIdx.x == 0 && it - 1 + STAGES < total_it) {
+              ptx::fence_proxy_async_smem();
+              issue(it - 1 + STAGES);
+            }
+          }
+        }
         if constexpr (TB >= 0) {  // in two halves
-          if (k == TA) bad = it + 1 < total_it && !transpose_part(it + 1, 0, kNq / 2, true);
+          if (k == TA && !bad) bad = it + 1 < total_it && !transpose_part(it + 1, 0, kNq / 2, true);
           if (k == TB && it + 1 < total_it && !bad) transpose_part(it + 1, kNq / 2, kNq, false);
         } else {
-          if (k == TA) bad = it + 1 < total_it && !transpose(it + 1);
+          if (k == TA && !bad) bad = it + 1 < total_it && !transpose(it + 1);
+        }
+        if constexpr (SPLIT) {
+          if (k == (TB >= 0 ? TB : TA) && !bad && it + 1 < total_it) ptx::mbar_arrive(at_full0 + 8 * ((it + 1) & 1));
         }
         float2 ap[4];
 #pragma unroll
@@ -325,16 +371,27 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
 #pragma unroll
           for (int j = 0; j < 8; ++j) acc[i][j] = __ffma2_rn(ap[i], make_float2(bb[j], bb[j]), acc[i][j]);
       }
-      // every warp is done with stage s and At[it & 1]; At[(it+1) & 1] is complete
-      if (bad) *reinterpret_cast<volatile int*>(&s_fail) = 1;
-      __syncthreads();
-      failed = *reinterpret_cast<volatile int*>(&s_fail) != 0;
-      if (failed) break;
-      if (threadIdx.x == 0 && it + STAGES < total_it) {
-        ptx::fence_proxy_async_smem();
-        issue(it + STAGES);
+      if constexpr (SPLIT) {
+        if (__any_sync(0xffffffffu, bad)) {
+          *reinterpret_cast<volatile int*>(&s_fail) = 1;
+          failed = true;
+          break;
+        }
+        ptx::mbar_arrive(done0 + 8 * (it & 1));  // this thread is done with slice it
+      } else {
+        // every warp is done with stage s and At[it & 1]; At[(it+1) & 1] is complete
+        if (bad) *reinterpret_cast<volatile int*>(&s_fail) = 1;
+        __syncthreads();
+        failed = *reinterpret_cast<volatile int*>(&s_fail) != 0;
+        if (failed) break;
+        if (threadIdx.x == 0 && it + STAGES < total_it) {
+          ptx::fence_proxy_async_smem();
+          issue(it + STAGES);
+        }
       }
     }
+    // SPLIT: warps leave a failed segment at different slices; agree before going on
+    if constexpr (SPLIT) failed = __syncthreads_or(failed) != 0;
     if (failed) break;
 
     // ---------------- stream-K: publish, or gather the partial tiles ----------------
@@ -431,12 +488,12 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   }
 }
 
-template <int BM_, int BN, int STAGES, int MINB, int TA, int TB = -1>
+template <int BM_, int BN, int STAGES, int MINB, int TA, int TB = -1, bool SPLIT = false>
 struct Variant_ {
   using S = Shape<BM_, BN, STAGES>;
   // a single product runs the plain 2-D kernel; strided batches their own instantiation
-  static constexpr auto kernel = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, false, TA, TB>;
-  static constexpr auto kernel_batched = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, true, TA, TB>;
+  static constexpr auto kernel = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, false, TA, TB, SPLIT>;
+  static constexpr auto kernel_batched = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, true, TA, TB, SPLIT>;
   static cudaError_t prepare() {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     return e != cudaSuccess ? e
