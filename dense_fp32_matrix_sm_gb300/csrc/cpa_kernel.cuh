@@ -153,7 +153,9 @@ __global__ void __launch_bounds__(Shape<BM, BN, STAGES, KW>::kThreads, MINB)
     }
   };
 
+  uint32_t issued = 0;  // slices this thread has issued
   auto issue = [&](uint32_t j) {
+    issued = j + 1;
     const uint32_t s = j % STAGES;
     const uint32_t a_stage = smem_base + s * S::kStageBytes;
     const int k0 = cur.kt * BK;
@@ -299,6 +301,12 @@ __global__ void __launch_bounds__(Shape<BM, BN, STAGES, KW>::kThreads, MINB)
         }
       }
     }
+  }
+  // After a failed wait: this thread's cp.async copies, and thread 0's TMA
+  // copies (bounded), land before the CTA's shared memory is released.
+  if (failed) {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (threadIdx.x == 0) ptx::drain_ring(bar_full, 8, issued, STAGES, p.timeout_ns);
   }
 }
 

@@ -350,6 +350,12 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     }
     cluster_sync();  // peers may still be reading this CTA's partial tile
   }
+  // After a failed wait, copies still in flight land before the CTA's shared
+  // memory is released.  Every warp that sees the failure drains what has been
+  // issued so far; a copy issued later is drained by the warp that issued it
+  // (or was waited on by every warp, when no warp saw the failure).
+  if (lane == 0 && *reinterpret_cast<volatile int*>(&s_failed))
+    ptx::drain_ring_released(bar_full, 8, released, S::kWarps, STAGES, total_it, p.timeout_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -582,6 +588,12 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     if (threadIdx.x == 0)
       for (int c = c_first; c < b; ++c) *reinterpret_cast<volatile unsigned int*>(p.flags + c) = 0u;
   }
+  // After a failed wait, copies still in flight land before the CTA's shared
+  // memory is released.  Every warp that sees the failure drains what has been
+  // issued so far; a copy issued later is drained by the warp that issued it
+  // (or was waited on by every warp, when no warp saw the failure).
+  if (lane == 0 && *reinterpret_cast<volatile int*>(&s_failed))
+    ptx::drain_ring_released(bar_full, 8, released, S::kWarps, STAGES, total_it, p.timeout_ns);
 }
 
 template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST>

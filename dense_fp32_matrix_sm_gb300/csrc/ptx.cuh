@@ -124,6 +124,41 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
   }
 }
 
+// After a failed wait, before the CTA exits: wait (bounded) until the
+// copies of the last `stages` slices issued into a ring have landed, so no
+// copy writes shared memory that a later CTA owns.  Slice j used stage
+// j % stages (its full barrier at bar_full + stride * stage) in phase
+// j / stages; every earlier slice was waited on before its stage was reused.
+// Each wait lasts at least 100 ms, however short the configured limit, which
+// is far above a copy's latency.
+__device__ __forceinline__ void drain_ring(uint32_t bar_full, uint32_t stride, uint32_t issued, uint32_t stages,
+                                           uint64_t timeout_ns) {
+  const uint64_t limit = timeout_ns < 100000000ull ? 100000000ull : timeout_ns;
+#pragma unroll 1
+  for (uint32_t j = issued > stages ? issued - stages : 0u; j < issued; ++j)
+    mbar_wait(bar_full + stride * (j % stages), (j / stages) & 1u, limit);
+}
+
+// drain_ring for a ring refilled by "the warp that completes a stage's
+// release set": released[s] counts the warp releases of stage s, and the
+// release set of slice j (every `warps`-th release) issued slice
+// j + stages when that is below `total`.  So stage s received one copy in
+// the prologue (s < total) plus one per completed set, up to the number of
+// slices j = s (mod stages) with j + stages < total; the last of them is the
+// only one that can be in flight.
+__device__ __forceinline__ void drain_ring_released(uint32_t bar_full, uint32_t stride, const unsigned int* released,
+                                                    uint32_t warps, uint32_t stages, uint32_t total,
+                                                    uint64_t timeout_ns) {
+  const uint64_t limit = timeout_ns < 100000000ull ? 100000000ull : timeout_ns;
+#pragma unroll 1
+  for (uint32_t s = 0; s < stages && s < total; ++s) {
+    const uint32_t sets = *reinterpret_cast<const volatile unsigned int*>(released + s) / warps;
+    const uint32_t refills = (total - 1u - s) / stages;
+    const uint32_t copies = 1u + (sets < refills ? sets : refills);
+    mbar_wait(bar_full + stride * s, (copies - 1u) & 1u, limit);
+  }
+}
+
 // 2-D tiled TMA load of the box at (x = inner coordinate, y = outer) into
 // shared memory at `dst`; completion is signalled on `bar` as transaction
 // bytes.  x * 4 bytes must be a multiple of 16 (callers pass multiples of 4).

@@ -275,8 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Before leaving, every copy this thread started has landed (bounded):
     // the last STAGES slices are the only ones possibly still in flight.
-    for (int kb = issued > STAGES ? issued - STAGES : 0; kb < issued; ++kb)
-      ptx::mbar_wait(full_bar(kb % STAGES), (kb / STAGES) & 1, p.timeout_ns);
+    ptx::drain_ring(full_bar(0), 8u, static_cast<uint32_t>(issued), STAGES, p.timeout_ns);
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
     for (int kb = 0; kb < KT; ++kb) {
@@ -465,8 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // every copy started here has landed before the CTA can leave
-    for (uint32_t h = g > STAGES ? g - STAGES : 0; h < g; ++h)
-      ptx::mbar_wait(full_bar(static_cast<int>(h % STAGES)), (h / STAGES) & 1u, p.timeout_ns);
+    ptx::drain_ring(full_bar(0), 8u, g, STAGES, p.timeout_ns);
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
     uint32_t g = 0;
@@ -750,8 +748,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       issued = kb + 1;
     }
     // every copy started here has landed before the CTA can leave
-    for (int kb = issued > kFRawStages ? issued - kFRawStages : 0; kb < issued; ++kb)
-      ptx::mbar_wait(raw_full(kb % kFRawStages), (kb / kFRawStages) & 1, p.timeout_ns);
+    ptx::drain_ring(raw_full(0), 8u, static_cast<uint32_t>(issued), kFRawStages, p.timeout_ns);
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
     for (int kb = 0; kb < KT; ++kb) {

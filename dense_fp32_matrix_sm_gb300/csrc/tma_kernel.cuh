@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(Shape<BM, BN, BK, WM, WN, STAGES>::kThreads, M
       ptx::mbar_init(bar_full + 8 * s, 1);
       released[s] = 0u;
     }
+
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tmA);
     ptx::prefetch_tensormap(&tmB);
@@ -199,6 +200,9 @@ __global__ void __launch_bounds__(Shape<BM, BN, BK, WM, WN, STAGES>::kThreads, M
       const uint32_t phase = (it / STAGES) & 1u;
       if (!ready && !ptx::mbar_wait(bar_full + 8 * s, phase, p.timeout_ns)) {
         atomicOr(p.status, kStatusTimeoutFull);
+        // copies still in flight land before this thread leaves; a copy issued
+        // later is waited on by the thread that issued it or by its consumers
+        ptx::drain_ring_released(bar_full, 8, released, S::kWarps, STAGES, total_it, p.timeout_ns);
         return;
       }
       // Probe the next slice's stage now; the answer arrives while this

@@ -214,8 +214,9 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
 
   // producer cursor (thread 0): slices are issued in schedule order
   int c_seg = 0, c_kt = 0, c_k1 = 0, c_tm = 0, c_tn = 0, c_z = 0;
+  uint32_t c_issued = 0;  // slices issued so far
   auto issue = [&](uint32_t j) {
-    (void)j;
+    c_issued = j + 1;
     if (c_kt == c_k1) {  // enter the next segment
       int tile, k0;
       segment(c_seg++, tile, k0, c_k1);
@@ -486,6 +487,8 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
       }
     }
   }
+  // after a failure, copies still in flight land before the CTA's shared memory is released
+  if (failed && threadIdx.x == 0) ptx::drain_ring(bar_full, 8, c_issued, STAGES, p.timeout_ns);
 }
 
 template <int BM_, int BN, int STAGES, int MINB, int TA, int TB = -1, bool SPLIT = false>
