@@ -185,18 +185,18 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
 // Measured on GB300 with the stream-K tail (which removes most of the
 // partial-wave loss once there is at least one full wave):
 //  * 128 x 256 tiles from one full wave of them on, with K >= 256 (eight or
-//    more k-slices per tile, the stream-K threshold): 63.7-66.6 TFLOP/s from
-//    2560^3 up, 2-4% above 128 x 128;
-//  * 128 x 128 tiles down to three quarters of a wave (1536^3: 56.5 vs 54.4
-//    for 128 x 64);
-//  * below that, 128 x 64 tiles two to an SM (1024^3: 36.1 vs 24.4);
+//    more k-slices per tile, the stream-K threshold): 66.3-69.6 TFLOP/s from
+//    2560^3 up, 1-2% above 128 x 128 (4096 x 4096 x 256: a tie);
+//  * 128 x 128 tiles down to half a wave (80 tiles: 2048 x 640 x 2048 34.0
+//    vs 31.4 for 128 x 64; 1280^3 41.0 vs 37.8; 1536^3 59.6 vs 55.2);
+//  * below that, 128 x 64 tiles two to an SM (1024^3, 64 tiles: 38.4 vs 26.0);
 //  * never a tile more than twice as wide as N: 64 x (512 x 64 x 512) ran
 //    14.5 TFLOP/s on 256-wide tiles, three quarters of each tile empty.
 const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms) {
   const int64_t wide_tiles = batch * ((M + 127) / 128) * ((N + 255) / 256);
   const int64_t square_tiles = batch * ((M + 127) / 128) * ((N + 127) / 128);
   if (N > 128 && wide_tiles >= num_sms && K >= 256) return "tmat_128x256x32_s3_b1";
-  if (N > 64 && 4 * square_tiles >= 3 * static_cast<int64_t>(num_sms)) return "tmat_128x128x32_s4_b1";
+  if (N > 64 && 2 * square_tiles >= static_cast<int64_t>(num_sms)) return "tmat_128x128x32_s4_b1";
   return "tmat_128x64x32_s3_b2";
 }
 
