@@ -132,13 +132,21 @@ void launch_split_rows(const float* X, int64_t ldx, int rows, int cols, float* h
   }
 }
 
-// X (rows x cols, ldx) -> hi, lo transposed (cols x rows, ldh).  Block row
-// blockIdx.y takes row tiles blockIdx.y, + gridDim.y, ... (any row count).
+// X (rows x cols, ldx) -> hi, lo transposed (cols x rows, ldh; ldh a
+// multiple of 4, hi and lo 16-byte aligned).  A block of 32 x 8 threads
+// moves 32 x 32 tiles through shared memory: coalesced 128-byte row reads,
+// then each thread writes one float4 of four consecutive rows to each
+// output (a warp covers four output rows; the column reads hit 32 distinct
+// banks).  Block row blockIdx.y takes row tiles blockIdx.y, + gridDim.y,
+// ... (any row count).
 __global__ void split_transpose_kernel(const float* __restrict__ X, int64_t ldx, int rows, int cols,
                                        float* __restrict__ hi, float* __restrict__ lo, int64_t ldh) {
   __shared__ float t[32][33];
   const int c0 = blockIdx.x * 32;
   const int row_tiles = (rows + 31) / 32;
+  const int tid = threadIdx.y * 32 + threadIdx.x;
+  const int oc = tid >> 3;  // output row c0 + oc
+  const int q = tid & 7;    // output columns r0 + 4q .. + 3
   for (int ty = blockIdx.y; ty < row_tiles; ty += gridDim.y) {
     const int r0 = ty * 32;
     for (int j = threadIdx.y; j < 32; j += blockDim.y) {
@@ -146,13 +154,26 @@ __global__ void split_transpose_kernel(const float* __restrict__ X, int64_t ldx,
       t[j][threadIdx.x] = (r < rows && c < cols) ? X[static_cast<int64_t>(r) * ldx + c] : 0.f;
     }
     __syncthreads();
-    for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-      const int c = c0 + j, r = r0 + threadIdx.x;  // output row c, column r
-      if (c < cols && r < rows) {
-        const float x = t[threadIdx.x][j];
-        const float h = to_tf32(x);
-        hi[static_cast<int64_t>(c) * ldh + r] = h;
-        lo[static_cast<int64_t>(c) * ldh + r] = to_tf32(x - h);
+    const int c = c0 + oc;
+    const int r = r0 + 4 * q;
+    if (c < cols && r < rows) {
+      float h[4], l[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float x = t[4 * q + i][oc];
+        h[i] = to_tf32(x);
+        l[i] = to_tf32(x - h[i]);
+      }
+      float* ho = hi + static_cast<int64_t>(c) * ldh + r;
+      float* lo_ = lo + static_cast<int64_t>(c) * ldh + r;
+      if (r + 3 < rows) {
+        *reinterpret_cast<float4*>(ho) = make_float4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<float4*>(lo_) = make_float4(l[0], l[1], l[2], l[3]);
+      } else {
+        for (int i = 0; i < 4 && r + i < rows; ++i) {
+          ho[i] = h[i];
+          lo_[i] = l[i];
+        }
       }
     }
     __syncthreads();  // the tile is refilled by the next row tile
