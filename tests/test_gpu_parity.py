@@ -526,8 +526,8 @@ def test_order_and_transpose(sg, oracle_mod, order, ta, tb, shape, config, pad):
 
 @pytest.mark.parametrize("config", [None, "tf32x3_128x128x32_s3"])
 def test_transposed_operand_with_more_than_65535_row_tiles(sg, oracle_mod, config):
-    """A stored K x M with K > 65535 * 64: the transposing kernels (32- and
-    64-row tiles) walk row tiles past the grid's y limit."""
+    """A stored K x M with K = 4.2 M, more than 65535 tiles of 32 rows: the
+    transposing kernels walk row tiles past the grid's y limit."""
     M, N, K = 8, 8, 4_200_000
     opA, opB, C0 = make_inputs(M, N, K, seed=77, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
     Cref, S = oracle_mod.sgemm_ref(opA, opB, C0, 1.0, 0.5)
