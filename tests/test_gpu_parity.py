@@ -733,7 +733,7 @@ def test_c_overlapping_a_or_b_is_refused(sg):
     plan.close()
 
 
-@pytest.mark.parametrize("shape", [(2048, 2048, 1024), (16, 16384, 4096)])
+@pytest.mark.parametrize("shape", [(2048, 2048, 1024), (4096, 4096, 1024), (16, 16384, 4096)])
 def test_stream_k_plan_replays_in_a_cuda_graph(sg, oracle_mod, shape):
     """A stream-K plan captured in a CUDA graph and replayed on new inputs: the
     finishers clear the flags they consumed, so the fixed epoch of the
