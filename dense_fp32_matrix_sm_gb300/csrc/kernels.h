@@ -73,6 +73,7 @@ struct Variant {
   int streamk;           // 1: the kernel can split its tail tiles along K (workspace per plan)
   int batched;           // 1: runs strided batches (TMA variants: 3-D tensor maps, batch outermost)
   int b_trans_ok;        // 1: reads B given transposed (stored N x K) itself, LaunchArgs::b_trans = 1
+  int a_trans_ok;        // 1: reads A given transposed (stored K x M) itself, LaunchArgs::a_trans = 1
 };
 
 // Variant tables, one per kernel translation unit.

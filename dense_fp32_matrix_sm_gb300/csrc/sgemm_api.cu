@@ -56,6 +56,7 @@ struct sgemm_plan_s {
   float* ex_wa;
   float* ex_wb;
   int ex_native_tb;  // the variant reads B given transposed (N x K) itself: no ex_wb
+  int ex_native_ta;  // the variant reads A given transposed (K x M) itself: no ex_wa
   // sgemm_run_host_pipelined: copy streams (host to device, device to host)
   // and, per buffer set b, events loaded / computed / stored; made on first use
   std::mutex pipe_mutex;
@@ -304,6 +305,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->ex_wa = nullptr;
   p->ex_wb = nullptr;
   p->ex_native_tb = 0;
+  p->ex_native_ta = 0;
   p->pipe_ready = false;
   if (v->kind == kKindTma || v->kind == kKindCpa) {
     const int64_t slots = static_cast<int64_t>(sms) * ctas;
@@ -445,7 +447,16 @@ sgemm_status_t encode_maps(const Variant* v, const sgemm_plan_s* p, const float*
   // an operand shared by every product (stride 0) is a batch of one
   const cuuint64_t nb_a = static_cast<cuuint64_t>(p->batch > 1 && p->stride_a != 0 ? p->batch : 1);
   const cuuint64_t nb_b = static_cast<cuuint64_t>(p->batch > 1 && p->stride_b != 0 ? p->batch : 1);
-  if (v->kind != kKindCpa) {  // the transposed-A kernels copy A themselves
+  if (a->a_trans) {  // A given transposed (K x M): [bk][bm] boxes, M innermost, unswizzled
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->M), static_cast<cuuint64_t>(p->K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->ex_lda) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(v->bm), static_cast<cuuint32_t>(v->bk)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&a->tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
+  } else if (v->kind != kKindCpa) {  // the transposed-A kernels copy A themselves
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->M), nb_a};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p->lda) * 4,
                                    static_cast<cuuint64_t>(nb_a > 1 ? p->stride_a : p->M * p->lda) * 4};
@@ -727,8 +738,10 @@ sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64
   const int kind = chosen->kind;
   // a few-row kernel reads B given transposed (N x K, K contiguous) by TMA itself
   if (tb && !native && chosen->b_trans_ok && ldb2 % 4 == 0) p->ex_native_tb = 1;
+  // the transposed-A kernels read A given transposed (K x M, M contiguous) by TMA themselves
+  if (ta && !native && chosen->a_trans_ok && lda2 % 4 == 0) p->ex_native_ta = 1;
   if (!native && kind != kKindTc && kind != kKindTcFused) {
-    if (ta && M2 > 0 && K > 0 && cudaMalloc(reinterpret_cast<void**>(&p->ex_wa), sizeof(float) * M2 * lda_eff) != cudaSuccess) {
+    if (ta && !p->ex_native_ta && M2 > 0 && K > 0 && cudaMalloc(reinterpret_cast<void**>(&p->ex_wa), sizeof(float) * M2 * lda_eff) != cudaSuccess) {
       sgemm_plan_destroy(p);
       return SGEMM_ERR_CUDA;
     }
@@ -790,6 +803,8 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
     return SGEMM_ERR_UNSUPPORTED;  // TMA needs 16-byte aligned bases; the scalar kernel cannot read every layout
   if (p->ex_native_tb && ((reinterpret_cast<uintptr_t>(B) & 15) != 0 || (reinterpret_cast<uintptr_t>(A) & 15) != 0))
     return SGEMM_ERR_UNSUPPORTED;  // B given transposed is read by TMA; the scalar kernel cannot take it
+  if (p->ex_native_ta && ((reinterpret_cast<uintptr_t>(A) & 15) != 0 || (reinterpret_cast<uintptr_t>(B) & 15) != 0))
+    return SGEMM_ERR_UNSUPPORTED;  // A given transposed is read by TMA; the scalar kernel cannot take it
   if (v->kind != kKindGeneric && v->kind != kKindTc && v->kind != kKindTcFused &&
       ((a_needs_16 && (reinterpret_cast<uintptr_t>(A) & 15) != 0) || (reinterpret_cast<uintptr_t>(B) & 15) != 0)) {
     v = reg.all[p->generic_id];
@@ -813,6 +828,7 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   a.split_k = v->kind == kKindSkinny ? p->split : 1;
   a.batch = static_cast<int>(p->batch);
   a.b_trans = p->ex_native_tb;
+  a.a_trans = p->ex_native_ta;
   a.stride_a = p->stride_a;
   a.stride_b = p->stride_b;
   a.stride_c = p->stride_c;

@@ -119,7 +119,11 @@ struct Shape {
 // part of slice j+1's transpose and on slice_done[j & 1] after slice j; it
 // waits on at_full[j & 1] before slice j and on slice_done[(j-1) & 1] before
 // overwriting At[(j+1) & 1], where thread 0 also refills stage (j-1) % STAGES.
-template <int BM_, int BN, int STAGES, int MINB, bool BATCHED, int TA, int TB, bool SPLIT>
+// AT: A given transposed (stored K x M, M contiguous).  TMA then copies
+// [BK][BM] boxes that already are At, and the k loop reads them from the
+// ring stage: no on-chip transpose (and, with SPLIT, no "transposed"
+// barriers; the slice's full barrier is waited on at its start).
+template <int BM_, int BN, int STAGES, int MINB, bool BATCHED, int TA, int TB, bool SPLIT, bool AT = false>
 __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
     sgemm_tmat_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const Params p) {
@@ -127,6 +131,7 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   constexpr int BM = S::BM;
   constexpr int BK = S::BK;
   static_assert(TA >= 0 && TA < BK && TB < BK && (TB < 0 || TB > TA), "transpose steps inside the k loop");
+  static_assert(!(AT && BATCHED), "A given transposed: single products only");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ int s_fail;
   __shared__ __align__(8) unsigned long long s_sync[4];  // SPLIT: at_full[2], slice_done[2]
@@ -230,7 +235,10 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
       ptx::tma_load_3d(dst, &tmA, c_kt * BK, c_tm * BM, c_z * p.a_batched, bar_full + 8 * s);
       ptx::tma_load_3d(dst + S::kStageA, &tmB, c_tn * BN, c_kt * BK, c_z * p.b_batched, bar_full + 8 * s);
     } else {
-      ptx::tma_load_2d(dst, &tmA, c_kt * BK, c_tm * BM, bar_full + 8 * s);
+      if constexpr (AT)
+        ptx::tma_load_2d(dst, &tmA, c_tm * BM, c_kt * BK, bar_full + 8 * s);
+      else
+        ptx::tma_load_2d(dst, &tmA, c_kt * BK, c_tm * BM, bar_full + 8 * s);
       ptx::tma_load_2d(dst + S::kStageA, &tmB, c_tn * BN, c_kt * BK, bar_full + 8 * s);
     }
     ++c_kt;
@@ -287,7 +295,7 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
 
   // failures are made CTA-uniform through the barrier, so every thread
   // leaves the loop at the same slice and no barrier is left waiting
-  failed = __syncthreads_or(total_it > 0 && !transpose(0)) != 0;
+  failed = __syncthreads_or(!AT && total_it > 0 && !transpose(0)) != 0;
 
   uint32_t it = 0;
   for (int seg = 0; seg < nseg && !failed; ++seg) {
@@ -318,22 +326,38 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
     for (int kt = seg_k0; kt < seg_k1; ++kt, ++it) {
       // the next slice's A is transposed during this one (its buffer was last read one slice ago)
       bool bad = false;
-      if constexpr (SPLIT) {
+      const uint32_t s = it % STAGES;
+      if constexpr (AT) {
+        // this slice's At and B are in stage s once its full barrier completes
+        if constexpr (SPLIT) {
+          if (!split_wait(bar_full + 8 * s, (it / STAGES) & 1u)) {
+            failed = true;
+            break;
+          }
+        } else {
+          bad = !ptx::mbar_wait(bar_full + 8 * s, (it / STAGES) & 1u, p.timeout_ns);
+          if (bad) atomicOr(p.status, kStatusTimeoutFull);  // the barrier below makes the failure CTA-wide
+        }
+      } else if constexpr (SPLIT) {
         // At[it & 1] is complete once every thread has transposed its part (slice 0: the prologue barrier)
         if (it >= 1 && !split_wait(at_full0 + 8 * (it & 1), ((it - 1) >> 1) & 1u)) {
           failed = true;
           break;
         }
       }
-      const uint32_t s = it % STAGES;
-      const float* At = at_buf + (it & 1) * (BK * BM);
+      const float* At = AT ? reinterpret_cast<const float*>(smem + s * S::kStageBytes)
+                           : at_buf + (it & 1) * (BK * BM);
       const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + (wn * 32 + 4 * c) / 4;
       // operands of step k+1 are loaded while step k multiplies (register double buffer)
       auto load_ops = [&](int k, float2 (&ap)[4], float4& b0, float4& b1) {
         const int f = S::kSwz * (k / S::kKPart);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          ap[i] = *reinterpret_cast<const float2*>(At + k * BM + ((f & 15) ? a_lo8 : a_lo0) + 16 * (i ^ (f >> 4)));
+        for (int i = 0; i < 4; ++i) {
+          if constexpr (AT)
+            ap[i] = *reinterpret_cast<const float2*>(At + k * BM + a_lo0 + 16 * i);
+          else
+            ap[i] = *reinterpret_cast<const float2*>(At + k * BM + ((f & 15) ? a_lo8 : a_lo0) + 16 * (i ^ (f >> 4)));
+        }
         b0 = Bs4[k * (BN / 4)];
         b1 = Bs4[k * (BN / 4) + 4];
       };
@@ -353,13 +377,14 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
             }
           }
         }
-        if constexpr (TB >= 0) {  // in two halves
+        if constexpr (AT) {
+        } else if constexpr (TB >= 0) {  // in two halves
           if (k == TA && !bad) bad = it + 1 < total_it && !transpose_part(it + 1, 0, kNq / 2, true);
           if (k == TB && it + 1 < total_it && !bad) transpose_part(it + 1, kNq / 2, kNq, false);
         } else {
           if (k == TA && !bad) bad = it + 1 < total_it && !transpose(it + 1);
         }
-        if constexpr (SPLIT) {
+        if constexpr (SPLIT && !AT) {
           if (k == (TB >= 0 ? TB : TA) && !bad && it + 1 < total_it) ptx::mbar_arrive(at_full0 + 8 * ((it + 1) & 1));
         }
         float2 ap[4];
@@ -494,11 +519,14 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
 template <int BM_, int BN, int STAGES, int MINB, int TA, int TB = -1, bool SPLIT = false>
 struct Variant_ {
   using S = Shape<BM_, BN, STAGES>;
-  // a single product runs the plain 2-D kernel; strided batches their own instantiation
+  // a single product runs the plain 2-D kernel (or, A given transposed, its
+  // AT form); strided batches their own instantiation
   static constexpr auto kernel = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, false, TA, TB, SPLIT>;
+  static constexpr auto kernel_at = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, false, TA, TB, SPLIT, true>;
   static constexpr auto kernel_batched = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, true, TA, TB, SPLIT>;
   static cudaError_t prepare() {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel_at, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     return e != cudaSuccess ? e
                             : cudaFuncSetAttribute(kernel_batched, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    S::kSmemBytes);
@@ -530,15 +558,20 @@ struct Variant_ {
     p.a_batched = a.batch > 1 && a.stride_a != 0;
     p.b_batched = a.batch > 1 && a.stride_b != 0;
     if (p.batch > 1) {
+      if (a.a_trans) return cudaErrorInvalidValue;  // A given transposed: single products only
       kernel_batched<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    } else if (a.a_trans) {
+      kernel_at<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
     } else {
       kernel<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
     }
     return cudaGetLastError();
   }
   static Variant describe(const char* name) {
-    return Variant{name, kKindTma, S::BM, BN, S::BK, STAGES, 1, S::kThreads, S::kSmemBytes, 128,
-                   &prepare, &occupancy, &launch, 0, 1, 1};
+    Variant v{name, kKindTma, S::BM, BN, S::BK, STAGES, 1, S::kThreads, S::kSmemBytes, 128,
+              &prepare, &occupancy, &launch, 0, 1, 1};
+    v.a_trans_ok = 1;  // reads A given transposed (K x M) by TMA itself, single products
+    return v;
   }
 };
 

@@ -496,7 +496,11 @@ def _stored(X, order, trans, pad):
                                               ((12, 1000, 515), None, 0), ((300, 520, 96), "tf32x3_128x256x32_s2", 1),
                                               ((300, 520, 96), "tf32x3f_128x128x32_s3", 0),
                                               ((16, 8192, 4096), None, 0),
-                                              ((7, 1000, 520), "skinny_sk_16x128x32_w4_s3_b3_ef", 0)])
+                                              ((7, 1000, 520), "skinny_sk_16x128x32_w4_s3_b3_ef", 0),
+                                              # transposed-A kernels: 128x64, 128x128, 128x256 stream-K;
+                                              # A given transposed is read natively (no transpose launch)
+                                              ((1000, 1100, 520), None, 0), ((2048, 2048, 1024), None, 0),
+                                              ((2560, 2560, 512), None, 0), ((1000, 1100, 520), None, 1)])
 def test_order_and_transpose(sg, oracle_mod, order, ta, tb, shape, config, pad):
     M, N, K = shape
     if config and config.startswith("skinny") and order == "col":
@@ -515,6 +519,15 @@ def test_order_and_transpose(sg, oracle_mod, order, ta, tb, shape, config, pad):
     info = plan.info()
     assert info["order"] == order and info["op"] == ("T" if ta else "N") + ("T" if tb else "N")
     assert info["M"] == M and info["N"] == N
+    if info["variant"].startswith("tmat"):
+        # column-major runs the row-major product of the swapped operands, so the
+        # product's A is given transposed when (row) transa or (column) transb;
+        # it is read natively when its stored row length is a multiple of 4
+        a_side_transposed = ta if order == "row" else tb
+        b_side_transposed = tb if order == "row" else ta
+        native_a = a_side_transposed and (lda if order == "row" else ldb) % 4 == 0
+        expected = 1 + (a_side_transposed and not native_a) + b_side_transposed
+        assert plan.launches == expected, (plan.launches, expected, info)
     plan.run(alpha, pA, pB, beta, pC)
     torch.cuda.synchronize()
     assert sg.device_status() == sg.SGEMM_OK
