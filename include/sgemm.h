@@ -209,12 +209,16 @@ enum { SGEMM_NO_TRANS = 0, SGEMM_TRANS = 1 };
  *     C^T = op(B)^T op(A)^T over the same memory.
  *   - The FFMA kernels read row-major operands stored untransposed. A
  *     transposed operand is first transposed on the GPU into a buffer the
- *     plan allocates (cudaMalloc), one extra kernel per run.
+ *     plan allocates (cudaMalloc), one extra kernel per run -- except in
+ *     the two native cases below.
+ *   - The transposed-A kernels (tmat_*) read the product's A given
+ *     transposed (row-major transa, or column-major transb: stored K x M)
+ *     as stored, when its leading dimension is a multiple of 4.
  *   - The split-TF32 variant reads either layout directly. So does the
  *     few-row stream-K kernel for B given transposed (stored N x K, the
- *     usual weight layout of decode) when ldb is a multiple of 4; such a
- *     plan needs A and B 16-byte aligned at run time, else
- *     SGEMM_ERR_UNSUPPORTED.
+ *     usual weight layout of decode) when ldb is a multiple of 4.
+ *   - A plan that reads a transposed operand natively needs A and B 16-byte
+ *     aligned at run time, else SGEMM_ERR_UNSUPPORTED.
  * Runs of a plan with such a buffer must not overlap in time.
  *
  * The pages cover the row-major, untransposed product only; the other
