@@ -57,6 +57,11 @@ struct sgemm_plan_s {
   float* ex_wb;
   int ex_native_tb;  // the variant reads B given transposed (N x K) itself: no ex_wb
   int ex_native_ta;  // the variant reads A given transposed (K x M) itself: no ex_wa
+  // An untransposed operand whose rows are not 16-byte multiples (lda or ldb
+  // not a multiple of 4) is copied each run into rp_a / rp_b, rows padded
+  // to lda / ldb (the kernels' view); ex_lda / ex_ldb keep the caller's.
+  float* rp_a;
+  float* rp_b;
   // sgemm_run_host_pipelined: copy streams (host to device, device to host)
   // and, per buffer set b, events loaded / computed / stored; made on first use
   std::mutex pipe_mutex;
@@ -246,12 +251,25 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return SGEMM_ERR_CUDA;
 
+  const int64_t lda_caller = lda, ldb_caller = ldb;
+  bool rp_a = false, rp_b = false;
   if (config_id < 0) {
     const char* forced = getenv("SGEMM_FORCE_CONFIG");
     if (forced && *forced) {
       config_id = find_variant(forced);
       if (config_id < 0) return SGEMM_ERR_INVALID_ARG;
     } else {
+      // TMA needs rows that are 16-byte multiples.  From 256^3 of work on, an
+      // operand without them is copied each run into a plan buffer with padded
+      // rows (one cudaMemcpy2DAsync), so the table's TMA kernels can read it:
+      // measured at 4096^3, lda = 4097 ran 54.6 TFLOP/s on the cp.async kernel
+      // and ldb = 4097 29.8 on the scalar-load kernel, against 68.8 aligned.
+      if (batch <= 1 && K > 0 && static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= 16777216.0) {
+        rp_a = lda % 4 != 0;
+        rp_b = ldb % 4 != 0;
+        if (rp_a) lda = (K + 3) / 4 * 4;
+        if (rp_b) ldb = (N + 3) / 4 * 4;
+      }
       config_id = find_variant(table_choice(M, N, K, lda, ldb, sms, batch, stride_a, stride_b));
       if (config_id < 0) config_id = reg.first_generic;
     }
@@ -300,13 +318,24 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->ex_order = SGEMM_ROW_MAJOR;
   p->ex_swap = 0;
   p->ex_ta = p->ex_tb = 0;
-  p->ex_lda = lda;
-  p->ex_ldb = ldb;
+  p->ex_lda = lda_caller;
+  p->ex_ldb = ldb_caller;
   p->ex_wa = nullptr;
   p->ex_wb = nullptr;
   p->ex_native_tb = 0;
   p->ex_native_ta = 0;
+  p->rp_a = nullptr;
+  p->rp_b = nullptr;
   p->pipe_ready = false;
+  // From here on every device buffer is stored in the plan as soon as it is
+  // allocated, and a failure frees them all through sgemm_plan_destroy.
+  auto fail = [&](sgemm_status_t e) {
+    sgemm_plan_destroy(p);
+    return e;
+  };
+  if ((rp_a && cudaMalloc(reinterpret_cast<void**>(&p->rp_a), sizeof(float) * M * lda) != cudaSuccess) ||
+      (rp_b && cudaMalloc(reinterpret_cast<void**>(&p->rp_b), sizeof(float) * K * ldb) != cudaSuccess))
+    return fail(SGEMM_ERR_CUDA);
   if (v->kind == kKindTma || v->kind == kKindCpa) {
     const int64_t slots = static_cast<int64_t>(sms) * ctas;
     if (grid > slots) grid = slots;
@@ -319,21 +348,11 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       p->dp_waves = static_cast<int>(p->tiles / slots);
       p->sk_iters = (p->tiles % slots) * KT;
       const size_t ws_bytes = static_cast<size_t>(slots) * v->bm * v->bn * sizeof(float);
-      void* ws = nullptr;
-      void* flags = nullptr;
-      if (cudaMalloc(&ws, ws_bytes) != cudaSuccess) {
-        delete p;
-        return SGEMM_ERR_CUDA;
-      }
-      if (cudaMalloc(&flags, static_cast<size_t>(slots) * sizeof(unsigned int)) != cudaSuccess ||
-          cudaMemset(flags, 0, static_cast<size_t>(slots) * sizeof(unsigned int)) != cudaSuccess) {
-        cudaFree(ws);
-        if (flags) cudaFree(flags);
-        delete p;
-        return SGEMM_ERR_CUDA;
-      }
-      p->ws = static_cast<float*>(ws);
-      p->flags = static_cast<unsigned int*>(flags);
+      if (cudaMalloc(reinterpret_cast<void**>(&p->ws), ws_bytes) != cudaSuccess ||
+          cudaMalloc(reinterpret_cast<void**>(&p->flags), static_cast<size_t>(slots) * sizeof(unsigned int)) !=
+              cudaSuccess ||
+          cudaMemset(p->flags, 0, static_cast<size_t>(slots) * sizeof(unsigned int)) != cudaSuccess)
+        return fail(SGEMM_ERR_CUDA);
     }
   } else if (v->kind == kKindSkinny && v->streamk) {
     // Stream-K few-row kernel: one resident wave over (slab, k-slice) units;
@@ -346,21 +365,11 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     if (units > 0) {
       p->sk_iters = units;
       const size_t ws_bytes = static_cast<size_t>(grid) * v->bm * v->bn * sizeof(float);
-      void* ws = nullptr;
-      void* flags = nullptr;
-      if (cudaMalloc(&ws, ws_bytes) != cudaSuccess) {
-        delete p;
-        return SGEMM_ERR_CUDA;
-      }
-      if (cudaMalloc(&flags, static_cast<size_t>(grid) * sizeof(unsigned int)) != cudaSuccess ||
-          cudaMemset(flags, 0, static_cast<size_t>(grid) * sizeof(unsigned int)) != cudaSuccess) {
-        cudaFree(ws);
-        if (flags) cudaFree(flags);
-        delete p;
-        return SGEMM_ERR_CUDA;
-      }
-      p->ws = static_cast<float*>(ws);
-      p->flags = static_cast<unsigned int*>(flags);
+      if (cudaMalloc(reinterpret_cast<void**>(&p->ws), ws_bytes) != cudaSuccess ||
+          cudaMalloc(reinterpret_cast<void**>(&p->flags), static_cast<size_t>(grid) * sizeof(unsigned int)) !=
+              cudaSuccess ||
+          cudaMemset(p->flags, 0, static_cast<size_t>(grid) * sizeof(unsigned int)) != cudaSuccess)
+        return fail(SGEMM_ERR_CUDA);
     }
   } else if (v->kind == kKindTc) {
     // persistent forms: one CTA per SM walks the tiles
@@ -372,12 +381,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     if (p->tiles > 0 && K > 0) {
       const int64_t kp = (K + 3) / 4 * 4;  // 16-byte row stride for TMA
       const size_t bytes = static_cast<size_t>(2 * (M + N) * kp) * sizeof(float);
-      void* buf = nullptr;
-      if (cudaMalloc(&buf, bytes) != cudaSuccess) {
-        delete p;
-        return SGEMM_ERR_CUDA;
-      }
-      p->tc_split = static_cast<float*>(buf);
+      if (cudaMalloc(reinterpret_cast<void**>(&p->tc_split), bytes) != cudaSuccess) return fail(SGEMM_ERR_CUDA);
       p->tc_split_ld = kp;
       float* parts[4] = {p->tc_split, p->tc_split + M * kp, p->tc_split + 2 * M * kp,
                          p->tc_split + (2 * M + N) * kp};
@@ -392,11 +396,8 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&p->tc_maps[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, parts[i], dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-          cudaFree(buf);
-          delete p;
-          return SGEMM_ERR_CUDA;
-        }
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+          return fail(SGEMM_ERR_CUDA);
       }
     }
   } else if (v->kind == kKindSkinny) {
@@ -784,6 +785,19 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   // operands; a transposed operand is first transposed into the plan's
   // buffer (the split-TF32 variants read it as stored instead)
   if (p->ex_swap) std::swap(A, B);
+  // operands whose rows are not 16-byte multiples: padded copies first
+  if (p->rp_a) {
+    if (cudaMemcpy2DAsync(p->rp_a, p->lda * sizeof(float), A, p->ex_lda * sizeof(float), p->K * sizeof(float), p->M,
+                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+      return SGEMM_ERR_CUDA;
+    A = p->rp_a;
+  }
+  if (p->rp_b) {
+    if (cudaMemcpy2DAsync(p->rp_b, p->ldb * sizeof(float), B, p->ex_ldb * sizeof(float), p->N * sizeof(float), p->K,
+                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+      return SGEMM_ERR_CUDA;
+    B = p->rp_b;
+  }
   if (p->ex_wa) {
     if (launch_transpose(A, p->ex_lda, static_cast<int>(p->K), static_cast<int>(p->M), p->ex_wa, p->lda, stream) !=
         cudaSuccess)
@@ -973,6 +987,8 @@ sgemm_status_t sgemm_plan_destroy(sgemm_plan_t plan) {
   if (plan->tc_split && cudaFree(plan->tc_split) != cudaSuccess) st = SGEMM_ERR_CUDA;
   if (plan->ex_wa && cudaFree(plan->ex_wa) != cudaSuccess) st = SGEMM_ERR_CUDA;
   if (plan->ex_wb && cudaFree(plan->ex_wb) != cudaSuccess) st = SGEMM_ERR_CUDA;
+  if (plan->rp_a && cudaFree(plan->rp_a) != cudaSuccess) st = SGEMM_ERR_CUDA;
+  if (plan->rp_b && cudaFree(plan->rp_b) != cudaSuccess) st = SGEMM_ERR_CUDA;
   if (plan->pipe_ready) {
     if (cudaStreamSynchronize(plan->pipe_h2d) != cudaSuccess || cudaStreamSynchronize(plan->pipe_d2h) != cudaSuccess)
       st = SGEMM_ERR_CUDA;
@@ -991,7 +1007,7 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
   snprintf(buf, n,
            "variant=%s kind=%s tile=%dx%dx%d stages=%d ffma2=%d threads=%d smem=%d grid=%d ctas_per_sm=%d "
            "tiles=%lld sms=%d split=%d streamk=%d dp_waves=%d sk_tiles=%lld k_order=%s M=%lld N=%lld K=%lld "
-           "order=%s op=%c%c batch=%lld",
+           "order=%s op=%c%c batch=%lld repack=%d",
            v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : v->kind == kKindTc ? "tc" : v->kind == kKindTcFused ? "tcf" : "skinny", v->bm, v->bn,
            v->bk, v->stages, v->ffma2, v->threads, v->smem_bytes, plan->grid, plan->ctas_per_sm,
            static_cast<long long>(plan->tiles), plan->num_sms, plan->split, plan->sk_iters > 0 ? 1 : 0, plan->dp_waves,
@@ -1002,7 +1018,9 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
            static_cast<long long>(plan->ex_swap ? plan->M : plan->N), static_cast<long long>(plan->K),
            plan->ex_order == SGEMM_COL_MAJOR ? "col" : "row",
            (plan->ex_swap ? plan->ex_tb : plan->ex_ta) ? 'T' : 'N', (plan->ex_swap ? plan->ex_ta : plan->ex_tb) ? 'T' : 'N',
-           static_cast<long long>(plan->batch));
+           static_cast<long long>(plan->batch),
+           // padded copies of the caller's A (1) and B (2), in the caller's terms
+           ((plan->ex_swap ? plan->rp_b : plan->rp_a) ? 1 : 0) | ((plan->ex_swap ? plan->rp_a : plan->rp_b) ? 2 : 0));
   return SGEMM_OK;
 }
 

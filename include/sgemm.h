@@ -99,8 +99,15 @@ typedef enum {
  * along K across the whole grid (stream-K; describe reports streamk=1).
  * That workspace makes the sum order along K for the tail tiles a fixed
  * split: results stay bit-identical from run to run.
+ * From M*N*K >= 2^24 on, an operand whose leading dimension is not a
+ * multiple of 4 (rows that are not 16-byte multiples, which TMA cannot
+ * read) gets a plan-owned copy with padded rows (cudaMalloc, M x K or
+ * K x N floats); each run first copies it there with one
+ * cudaMemcpy2DAsync (device to device) on the run's stream, and describe
+ * reports repack=1 (A), 2 (B) or 3.  Runs of such a plan must not overlap
+ * in time.
  * The environment variable SGEMM_FORCE_CONFIG=<variant name> overrides the
- * table choice.  *out is set only on SGEMM_OK.
+ * table choice (and then nothing is repacked).  *out is set only on SGEMM_OK.
  */
 sgemm_status_t sgemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                           sgemm_plan_t *out);

@@ -226,6 +226,35 @@ def test_misaligned_pointers(sg, oracle_mod, offs):
         assert_parity(C, Cref, S, K, f"{name} offsets {offs}")
 
 
+@pytest.mark.parametrize("pads", [(1, 0), (0, 1), (1, 3)])
+def test_unaligned_leading_dimensions_are_repacked(sg, oracle_mod, pads):
+    """From 256^3 of work on, an operand whose rows are not 16-byte multiples
+    is copied into padded rows each run, so the TMA kernels still serve it."""
+    M, N, K = 700, 600, 520
+    lda, ldb = K + pads[0], N + pads[1]
+    A, B, C0 = make_inputs(M, N, K, seed=91 + pads[1], dist_a=("normal", 1.0), dist_b=("normal", 1.0))
+    Cref, S = oracle_mod.sgemm_ref(A, B, C0, 0.75, -0.5)
+    C, used = run_gpu(sg, A, B, C0, 0.75, -0.5, lda=lda, ldb=ldb)
+    info = run_gpu.last_info
+    assert info["repack"] == (1 if lda % 4 else 0) | (2 if ldb % 4 else 0), info
+    assert used.startswith("tmat"), used
+    assert_parity(C, Cref, S, K, f"repacked lda={lda} ldb={ldb} {used}")
+    # the same storage read as column-major: C^T = B^T A^T, operands swapped
+    memA, memB = _stored(A, "col", False, 0), _stored(B, "col", False, 0)
+    dA, pA, _ = _to_dev(memA[0], M + pads[0])
+    dB, pB, _ = _to_dev(memB[0], K + pads[1])
+    memC, ldc = _stored(C0, "col", False, 0)
+    dC, pC, _ = _to_dev(memC, ldc)
+    plan = sg.Plan(M, N, K, M + pads[0], K + pads[1], ldc, order="col")
+    assert plan.info()["repack"] == (1 if (M + pads[0]) % 4 else 0) | (2 if (K + pads[1]) % 4 else 0), plan.info()
+    plan.run(0.75, pA, pB, -0.5, pC)
+    torch.cuda.synchronize()
+    assert sg.device_status() == sg.SGEMM_OK
+    Cc = _from_dev(dC, memC.shape[0], memC.shape[1], ldc).T
+    plan.close()
+    assert_parity(Cc, Cref, S, K, f"column-major repacked {pads}")
+
+
 @pytest.mark.parametrize("ldc_pad", [7, 4])
 def test_guard_bands_untouched(sg, ldc_pad):
     M, N, K = 131, 132, 76
