@@ -210,6 +210,33 @@ cudaError_t launch_transpose(const float* in, int64_t ld_in, int rows, int cols,
   return cudaGetLastError();
 }
 
+// dst (rows x cols, ldd a multiple of 4, dst 16-byte aligned) = src (rows x
+// cols, any lds and alignment): a copy that pads rows to 16-byte multiples.
+// Consecutive threads take consecutive float4 columns of a row: coalesced
+// scalar loads, one 16-byte store each (the last float4 of a row is
+// zero-padded).  Block row blockIdx.y takes rows blockIdx.y, + gridDim.y, ...
+__global__ void repack_rows_kernel(const float* __restrict__ src, int64_t lds, int rows, int cols,
+                                   float* __restrict__ dst, int64_t ldd) {
+  const int c = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (c >= cols) return;
+  for (int r = blockIdx.y; r < rows; r += gridDim.y) {
+    const float* s = src + static_cast<int64_t>(r) * lds + c;
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = c + i < cols ? s[i] : 0.f;
+    *reinterpret_cast<float4*>(dst + static_cast<int64_t>(r) * ldd + c) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+cudaError_t launch_repack(const float* src, int64_t lds, int rows, int cols, float* dst, int64_t ldd,
+                          cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const int threads = 128;
+  const dim3 grid((cols / 4 + threads) / threads, rows < 8192 ? rows : 8192);
+  repack_rows_kernel<<<grid, threads, 0, stream>>>(src, lds, rows, cols, dst, ldd);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
   return cudaGetLastError();

@@ -94,6 +94,10 @@ cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaSt
 // out (cols x rows, ld_out) = in (rows x cols, ld_in) transposed.
 cudaError_t launch_transpose(const float* in, int64_t ld_in, int rows, int cols, float* out, int64_t ld_out,
                              cudaStream_t stream);
+// dst = src with rows padded to 16-byte multiples (ldd % 4 == 0, dst 16-byte
+// aligned); src may have any leading dimension and alignment.
+cudaError_t launch_repack(const float* src, int64_t lds, int rows, int cols, float* dst, int64_t ldd,
+                          cudaStream_t stream);
 
 // One-thread kernel that waits on a barrier phase nothing completes.
 cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream);

@@ -787,14 +787,14 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   if (p->ex_swap) std::swap(A, B);
   // operands whose rows are not 16-byte multiples: padded copies first
   if (p->rp_a) {
-    if (cudaMemcpy2DAsync(p->rp_a, p->lda * sizeof(float), A, p->ex_lda * sizeof(float), p->K * sizeof(float), p->M,
-                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    if (launch_repack(A, p->ex_lda, static_cast<int>(p->M), static_cast<int>(p->K), p->rp_a, p->lda, stream) !=
+        cudaSuccess)
       return SGEMM_ERR_CUDA;
     A = p->rp_a;
   }
   if (p->rp_b) {
-    if (cudaMemcpy2DAsync(p->rp_b, p->ldb * sizeof(float), B, p->ex_ldb * sizeof(float), p->N * sizeof(float), p->K,
-                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    if (launch_repack(B, p->ex_ldb, static_cast<int>(p->K), static_cast<int>(p->N), p->rp_b, p->ldb, stream) !=
+        cudaSuccess)
       return SGEMM_ERR_CUDA;
     B = p->rp_b;
   }
@@ -1029,7 +1029,8 @@ sgemm_status_t sgemm_plan_launches(sgemm_plan_t plan, int* out) {
   // the split-TF32 variants launch two operand-split kernels before the GEMM
   const Variant* v = registry().all[plan->config_id];
   *out = (plan->M == 0 || plan->N == 0 || plan->batch == 0) ? 0 : v->kind == kKindTc && plan->K > 0 ? 3 : 1;
-  if (*out > 0 && plan->K > 0) *out += (plan->ex_wa ? 1 : 0) + (plan->ex_wb ? 1 : 0);
+  if (*out > 0 && plan->K > 0)
+    *out += (plan->ex_wa ? 1 : 0) + (plan->ex_wb ? 1 : 0) + (plan->rp_a ? 1 : 0) + (plan->rp_b ? 1 : 0);
   return SGEMM_OK;
 }
 

@@ -102,9 +102,8 @@ typedef enum {
  * From M*N*K >= 2^24 on, an operand whose leading dimension is not a
  * multiple of 4 (rows that are not 16-byte multiples, which TMA cannot
  * read) gets a plan-owned copy with padded rows (cudaMalloc, M x K or
- * K x N floats); each run first copies it there with one
- * cudaMemcpy2DAsync (device to device) on the run's stream, and describe
- * reports repack=1 (A), 2 (B) or 3.  Runs of such a plan must not overlap
+ * K x N floats); each run first copies it there with one kernel on the
+ * run's stream, and describe reports repack=1 (A), 2 (B) or 3.  Runs of such a plan must not overlap
  * in time.
  * The environment variable SGEMM_FORCE_CONFIG=<variant name> overrides the
  * table choice (and then nothing is repacked).  *out is set only on SGEMM_OK.
