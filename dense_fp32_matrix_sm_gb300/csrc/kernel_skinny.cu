@@ -383,10 +383,17 @@ struct SkinnySkParams {
   float* ws;             // kSBM x BN floats per CTA
   unsigned int* flags;   // one per CTA
   unsigned int epoch;
+  // strided batch (BATCHED): slabs are numbered product-major over all
+  // products; A and B come through 3-D tensor maps (batch = third
+  // coordinate, 0 for an operand every product shares), C is offset by stride_c
+  int batch;
+  int64_t stride_c;
+  int a_batched, b_batched;
 };
 
 // BT: B given transposed (stored N x K), loaded as swizzled [n][k] boxes.
-template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST, bool BT>
+// BATCHED: a strided batch of products, B as stored (not BT).
+template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST, bool BT, bool BATCHED = false>
 __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     sgemm_skinny_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const SkinnySkParams p) {
@@ -408,9 +415,11 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
   const int gw = warp % GW;
   const int G = static_cast<int>(gridDim.x);
   const int b = static_cast<int>(blockIdx.x);
+  static_assert(!(BT && BATCHED), "batches take B as stored");
   const int KT = (p.K + kSBK - 1) / kSBK;
-  const int nslabs = (p.N + BN - 1) / BN;
-  const int64_t U = static_cast<int64_t>(nslabs) * KT;
+  const int nslabs = (p.N + BN - 1) / BN;  // per product
+  // slabs over every product: gs = z * nslabs + slab of product z
+  const int64_t U = static_cast<int64_t>(nslabs) * (BATCHED ? p.batch : 1) * KT;
   const int64_t s0 = (static_cast<int64_t>(b) * U) / G;
   const int64_t e0 = (static_cast<int64_t>(b + 1) * U) / G;
   const uint32_t total_it = static_cast<uint32_t>(e0 - s0);
@@ -426,9 +435,21 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     const uint32_t s = j % STAGES;
     const int64_t u = unit_of(j);
     const int kt = static_cast<int>(u % KT);
-    const int n0 = static_cast<int>(u / KT) * BN;
+    const int gs = static_cast<int>(u / KT);
     const uint32_t dst = smem_base + s * S::kStageBytes;
     ptx::mbar_arrive_expect_tx(bar_full + 8 * s, S::kStageBytes);
+    if constexpr (BATCHED) {
+      const int z = gs / nslabs;
+      const int n0 = (gs - z * nslabs) * BN;
+      ptx::tma_load_3d(dst, &tmA, kt * kSBK, 0, z * p.a_batched, bar_full + 8 * s);
+      if constexpr (EVICT_FIRST)
+        ptx::tma_load_3d_hint(dst + S::kStageA, &tmB, n0, kt * kSBK, z * p.b_batched, bar_full + 8 * s,
+                              ptx::l2_policy_evict_first());
+      else
+        ptx::tma_load_3d(dst + S::kStageA, &tmB, n0, kt * kSBK, z * p.b_batched, bar_full + 8 * s);
+      return;
+    }
+    const int n0 = gs * BN;
     ptx::tma_load_2d(dst, &tmA, kt * kSBK, 0, bar_full + 8 * s);
     const int bx = BT ? kt * kSBK : n0, by = BT ? n0 : kt * kSBK;  // B as [k][n], or Bt as [n][k]
     if constexpr (EVICT_FIRST) {
@@ -466,7 +487,10 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
       k0 = static_cast<int>((s0 > lo ? s0 : lo) - lo);
       k1 = static_cast<int>((e0 < lo + KT ? e0 : lo + KT) - lo);
     }
-    const int n0 = slab * BN;
+    // slab is numbered over every product (BATCHED): product z, its column slab
+    const int z = BATCHED ? slab / nslabs : 0;
+    const int n0 = (slab - z * nslabs) * BN;
+    float* const Cz = BATCHED ? p.C + z * p.stride_c : p.C;
     float2 accp[kSBM / 2][4];
 #pragma unroll
     for (int q = 0; q < kSBM / 2; ++q)
@@ -574,7 +598,7 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
       const int m = (4 * i) / BN;
       const int n = n0 + (4 * i) % BN;
       if (m < p.M) {
-        float* crow = p.C + static_cast<int64_t>(m) * p.ldc;
+        float* crow = Cz + static_cast<int64_t>(m) * p.ldc;
         const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -601,11 +625,13 @@ struct SkinnySkVariant {
   using S = SkinnyShape<BN, GW, STAGES>;
   static constexpr auto kernel = sgemm_skinny_sk_kernel<BN, GW, STAGES, MINB, EVICT_FIRST, false>;
   static constexpr auto kernel_bt = sgemm_skinny_sk_kernel<BN, GW, STAGES, MINB, EVICT_FIRST, true>;
+  static constexpr auto kernel_batched = sgemm_skinny_sk_kernel<BN, GW, STAGES, MINB, EVICT_FIRST, false, true>;
   static cudaError_t prepare() {
-    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
-    return e != cudaSuccess ? e
-                            : cudaFuncSetAttribute(kernel_bt, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   S::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel_bt, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel_batched, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    return e;
   }
   static cudaError_t occupancy(int* ctas) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kernel, S::kThreads, S::kSmemBytes);
@@ -624,7 +650,14 @@ struct SkinnySkVariant {
     p.ws = a.ws;
     p.flags = a.flags;
     p.epoch = a.epoch;
-    if (a.b_trans) {
+    p.batch = a.batch > 1 ? a.batch : 1;
+    p.stride_c = a.stride_c;
+    p.a_batched = a.batch > 1 && a.stride_a != 0;
+    p.b_batched = a.batch > 1 && a.stride_b != 0;
+    if (p.batch > 1) {
+      if (a.b_trans) return cudaErrorInvalidValue;  // batches take B as stored
+      kernel_batched<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    } else if (a.b_trans) {
       kernel_bt<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
     } else {
       kernel<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
@@ -633,7 +666,7 @@ struct SkinnySkVariant {
   }
   static Variant describe(const char* name) {
     Variant v{name, kKindSkinny, kSBM, BN, kSBK, STAGES, 1, S::kThreads, S::kSmemBytes, 128, &prepare, &occupancy,
-              &launch, 0, 1};
+              &launch, 0, 1, 1};  // stream-K, strided batches
     v.b_trans_ok = 1;  // reads B given transposed (N x K) itself
     return v;
   }

@@ -217,6 +217,9 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     if (ldb % 4 != 0 || lda % 4 != 0 || stride_a % 4 != 0 || stride_b % 4 != 0 ||
         (stride_a != 0 && stride_a < M * lda) || (stride_b != 0 && stride_b < K * ldb))
       return "generic_64x64x16";
+    // few rows: the stream-K few-row kernel over (product, slab, k-slice)
+    // units, instead of 128-row tiles that are 7/8 empty
+    if (M <= 16) return "skinny_sk_16x128x32_w4_s3_b3_ef";
     return tmat_choice(M, N, K, batch, num_sms);
   }
   if (ldb % 4 != 0) return "generic_64x64x16";

@@ -629,6 +629,10 @@ def test_plan_ex_argument_errors(sg):
     (640, 1024, 256, 9, "tmat_128x256x32_s3_b1", False),  # 180 tiles: a stream-K tail over batches 7 and 8
     (640, 768, 256, 4, "tmat_128x128x32_s4_b1", True),  # A shared by every product (stride 0)
     (65, 33, 17, 9, "generic_64x64x16", False),
+    # few rows: the stream-K few-row kernel over (product, slab, k-slice) units
+    (16, 1024, 512, 8, None, False),
+    (7, 300, 520, 5, None, True),                       # ragged N and K, A shared
+    (1, 4096, 256, 3, None, False),
 ])
 def test_strided_batch(sg, oracle_mod, case):
     M, N, K, batch, config, shared_a = case
@@ -651,6 +655,8 @@ def test_strided_batch(sg, oracle_mod, case):
     plan = sg.Plan(M, N, K, config=config, batch=batch, stride_a=sa, stride_b=sb, stride_c=sc)
     info = plan.info()
     assert info["batch"] == batch
+    if config is None and M <= 16:
+        assert info["variant"].startswith("skinny_sk"), info
     plan.run(alpha, dA, dB, beta, dC)
     torch.cuda.synchronize()
     assert sg.device_status() == sg.SGEMM_OK
