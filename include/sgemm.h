@@ -175,10 +175,11 @@ sgemm_status_t sgemm_plan_autotune(int64_t M, int64_t N, int64_t K, int64_t lda,
  *
  * How it runs:
  *   - Every product of the batch runs in one launch.
- *   - Transposed-A kernels: 3-D tensor maps, batch outermost. They need
- *     stride_a and stride_b to be multiples of 4 that either do not overlap
- *     the matrices or are 0 (one operand shared by every product); their
- *     grid and stream-K tail span the whole batch.
+ *   - Transposed-A kernels, and for M <= 16 the stream-K few-row kernel:
+ *     3-D tensor maps, batch outermost. They need stride_a and stride_b to
+ *     be multiples of 4 that either do not overlap the matrices or are 0
+ *     (one operand shared by every product); their grid and stream-K split
+ *     span the whole batch.
  *   - Otherwise the scalar-load kernel runs, the batch on its third grid
  *     dimension.
  *
