@@ -20,12 +20,14 @@
 //  * While the math runs on slice j, all threads transpose the A slice j+1
 //    into a double-buffered At[BK][BM]: with T = threads/BM (1, 2 or 4)
 //    threads per row, thread t reads row t/T, k-part t%T (BK/T k, 128-bit
-//    loads) and writes At[k][m ^ (32/T)*(k / (BK/T))].  The copy sits at a
-//    fixed step of the unrolled k loop (TA), or in two halves (TA, TB), so
-//    its wait and its load-to-store latency hide behind FFMA2s; placed
-//    before the loop instead it cost 3.5% at 4096^3 (measured on GB300).  The XOR puts the T k-parts of
-//    a warp's 32/T rows in different bank groups (conflict-free writes) and
-//    keeps pairs (m, m+1) adjacent.
+//    loads) and writes At[k][m ^ (32/T)*(k / (BK/T))].  The XOR puts the T
+//    k-parts of a warp's 32/T rows in different bank groups (conflict-free
+//    writes) and keeps pairs (m, m+1) adjacent.  The copy sits at a fixed
+//    step of the unrolled k loop (TA), or in two halves (TA, TB), so its
+//    wait and its load-to-store latency hide behind FFMA2s; placed before
+//    the loop instead it cost 3.5% at 4096^3 (measured on GB300).
+//  * A given transposed (AT: stored K x M) needs no transpose: TMA copies
+//    [BK][BM] boxes, which the k loop reads from the ring stage directly.
 //    ("Learn: Optimizing GEMM", section 7, and "Writing a Fast Matmul in
 //    CUDA", Step 5: A stored transposed so the inner loop reads contiguous
 //    m -- here the transpose runs on the on-chip copy instead of on the
