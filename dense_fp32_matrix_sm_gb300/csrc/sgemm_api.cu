@@ -188,21 +188,26 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
 }
 
 // Tile width for the transposed-A family, over `batch` products of M x N x K.
-// Measured on GB300 with the stream-K tail (which removes most of the
-// partial-wave loss once there is at least one full wave):
+// Measured on GB300 with stream-K (which removes the partial-wave loss once
+// there is at least one full wave, and with fewer tiles than CTA slots
+// splits every tile along K once each CTA gets 8 or more k-slices):
 //  * 128 x 256 tiles from one full wave of them on, with K >= 256 (eight or
 //    more k-slices per tile, the stream-K threshold): 66.3-69.6 TFLOP/s from
 //    2560^3 up, 1-2% above 128 x 128 (4096 x 4096 x 256: a tie);
-//  * 128 x 128 tiles down to half a wave (80 tiles: 2048 x 640 x 2048 34.0
-//    vs 31.4 for 128 x 64; 1280^3 41.0 vs 37.8; 1536^3 59.6 vs 55.2);
-//  * below that, 128 x 64 tiles two to an SM (1024^3, 64 tiles: 38.4 vs 26.0);
+//  * 128 x 128 tiles down to half a wave (1536^3: 61.2 vs 56.2 for 128 x 64),
+//    or below that when every tile can be split along K: 1024^3 45.8 vs
+//    43.6, 512 x 512 x 8192 52.3 vs 49.8, 2048 x 640 x 2048 58.1 vs 53.4;
+//  * otherwise 128 x 64 tiles two to an SM (768^3: 20.3 vs 14.2);
 //  * never a tile more than twice as wide as N: 64 x (512 x 64 x 512) ran
 //    14.5 TFLOP/s on 256-wide tiles, three quarters of each tile empty.
 const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms) {
   const int64_t wide_tiles = batch * ((M + 127) / 128) * ((N + 255) / 256);
   const int64_t square_tiles = batch * ((M + 127) / 128) * ((N + 127) / 128);
+  const int64_t KT = (K + 31) / 32;
   if (N > 128 && wide_tiles >= num_sms && K >= 256) return "tmat_128x256x32_s3_b1";
-  if (N > 64 && 2 * square_tiles >= static_cast<int64_t>(num_sms)) return "tmat_128x128x32_s4_b1";
+  if (N > 64 && (2 * square_tiles >= static_cast<int64_t>(num_sms) ||
+                 (KT >= 8 && square_tiles * KT >= 8 * static_cast<int64_t>(num_sms))))
+    return "tmat_128x128x32_s4_b1";
   return "tmat_128x64x32_s3_b2";
 }
 
@@ -344,9 +349,12 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     if (grid > slots) grid = slots;
     // Stream-K tail: when the tiles do not fill the last wave, split the
     // k-slices of the leftover tiles over every CTA of a resident grid.
+    // With fewer tiles than CTA slots every tile is a "leftover" (no
+    // data-parallel wave), as long as each CTA still gets 8 or more slices.
     const int64_t KT = (K + v->bk - 1) / v->bk;
-    if (v->streamk && getenv("SGEMM_NO_STREAMK") == nullptr && p->tiles > slots && p->tiles % slots != 0 &&
-        KT >= 8) {
+    const bool tail = p->tiles > slots && p->tiles % slots != 0;
+    const bool small = p->tiles < slots && p->tiles * KT >= 8 * slots;
+    if (v->streamk && getenv("SGEMM_NO_STREAMK") == nullptr && (tail || small) && KT >= 8) {
       grid = slots;
       p->dp_waves = static_cast<int>(p->tiles / slots);
       p->sk_iters = (p->tiles % slots) * KT;

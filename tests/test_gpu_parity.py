@@ -421,11 +421,14 @@ def test_transposed_a_variants_take_any_lda(sg, oracle_mod):
             assert_parity(C, Cref, S, K, f"{name} lda={lda} off_a={off_a}")
 
 
-@pytest.mark.parametrize("shape", [(2048, 2048, 1024), (1500, 3000, 780), (2560, 1408, 256)])
+@pytest.mark.parametrize("shape", [(2048, 2048, 1024), (1500, 3000, 780), (2560, 1408, 256),
+                                   # fewer tiles than CTA slots: every tile split along K
+                                   (1024, 1024, 1024), (512, 520, 8200), (1000, 300, 3000)])
 def test_stream_k_tail(sg, oracle_mod, shape):
     """Tile counts that overshoot the resident grid: full waves run
     data-parallel and the leftover tiles are split along K across all CTAs
-    (partials through a workspace, added in CTA order)."""
+    (partials through a workspace, added in CTA order).  With fewer tiles
+    than CTA slots there is no data-parallel wave: every tile is split."""
     M, N, K = shape
     A, B, C0 = make_inputs(M, N, K, seed=M + 3 * N + K, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
     dA = torch.from_numpy(A).cuda()
@@ -447,6 +450,8 @@ def test_stream_k_tail(sg, oracle_mod, shape):
         if info["streamk"]:
             saw_streamk = True
             assert info["k_order"] == "split"
+            if info["tiles"] < info["grid"]:
+                assert info["dp_waves"] == 0, info
         rows, cols = sample_rows_cols(M, N, n_rows=192, n_cols=192, seed=7)
         Cs = outs[0][np.ix_(rows, cols)]
         Cref, S = oracle_mod.sgemm_ref(np.ascontiguousarray(A[rows]), np.ascontiguousarray(B[:, cols]),
