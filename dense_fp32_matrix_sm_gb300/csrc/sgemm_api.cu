@@ -190,14 +190,14 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
 // Tile width for the transposed-A family, over `batch` products of M x N x K.
 // Measured on GB300 with stream-K (which removes the partial-wave loss once
 // there is at least one full wave, and with fewer tiles than CTA slots
-// splits every tile along K once each CTA gets 8 or more k-slices):
+// splits every tile along K once every CTA gets a k-slice):
 //  * 128 x 256 tiles from one full wave of them on, with K >= 256 (eight or
 //    more k-slices per tile, the stream-K threshold): 66.3-69.6 TFLOP/s from
 //    2560^3 up, 1-2% above 128 x 128 (4096 x 4096 x 256: a tie);
 //  * 128 x 128 tiles down to half a wave (1536^3: 61.2 vs 56.2 for 128 x 64),
 //    or below that when every tile can be split along K: 1024^3 45.8 vs
 //    43.6, 512 x 512 x 8192 52.3 vs 49.8, 2048 x 640 x 2048 58.1 vs 53.4;
-//  * otherwise 128 x 64 tiles two to an SM (768^3: 20.3 vs 14.2);
+//  * otherwise 128 x 64 tiles two to an SM (384^3: 4.4 vs 3.1);
 //  * never a tile more than twice as wide as N: 64 x (512 x 64 x 512) ran
 //    14.5 TFLOP/s on 256-wide tiles, three quarters of each tile empty.
 const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms) {
@@ -206,7 +206,7 @@ const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_
   const int64_t KT = (K + 31) / 32;
   if (N > 128 && wide_tiles >= num_sms && K >= 256) return "tmat_128x256x32_s3_b1";
   if (N > 64 && (2 * square_tiles >= static_cast<int64_t>(num_sms) ||
-                 (KT >= 8 && square_tiles * KT >= 8 * static_cast<int64_t>(num_sms))))
+                 (KT >= 8 && square_tiles * KT >= static_cast<int64_t>(num_sms))))
     return "tmat_128x128x32_s4_b1";
   return "tmat_128x64x32_s3_b2";
 }
@@ -241,7 +241,10 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
                                                                        : "skinny_16x128x32_w4_s3_b3_ef_pa";
   }
   if (lda % 4 != 0) return "cpa_128x128x32_s3_k8_b2";  // A copied 4 bytes at a time: any lda
-  if (M * N <= 256 * 256) return "tma_128x64x32_w64x32_s3_quad_b3";
+  // tiny products: the k-contiguous kernel, unless the K loop is long enough to
+  // split every 128 x 128 tile over the grid (256 x 256 x 2048: 6.8 TFLOP/s vs 2.4)
+  if (M * N <= 256 * 256 && ((M + 127) / 128) * ((N + 127) / 128) * ((K + 31) / 32) < num_sms)
+    return "tma_128x64x32_w64x32_s3_quad_b3";
   return tmat_choice(M, N, K, 1, num_sms);
 }
 
@@ -350,10 +353,12 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     // Stream-K tail: when the tiles do not fill the last wave, split the
     // k-slices of the leftover tiles over every CTA of a resident grid.
     // With fewer tiles than CTA slots every tile is a "leftover" (no
-    // data-parallel wave), as long as each CTA still gets 8 or more slices.
+    // data-parallel wave), as long as every CTA still gets a slice
+    // (measured: 768^3 from 20.7 to 31.5 TFLOP/s, 640^3 from 13.9 to 21.2,
+    // 512^3 from 8.6 to 11.9).
     const int64_t KT = (K + v->bk - 1) / v->bk;
     const bool tail = p->tiles > slots && p->tiles % slots != 0;
-    const bool small = p->tiles < slots && p->tiles * KT >= 8 * slots;
+    const bool small = p->tiles < slots && p->tiles * KT >= slots;
     if (v->streamk && getenv("SGEMM_NO_STREAMK") == nullptr && (tail || small) && KT >= 8) {
       grid = slots;
       p->dp_waves = static_cast<int>(p->tiles / slots);

@@ -139,12 +139,15 @@ extern "C" sgemm_status_t sgemm_run_static_scratch(int64_t M, int64_t N, int64_t
 
   // The same schedule as a plan of this variant: full waves data-parallel;
   // when the last wave is partial (and K has at least 8 slices), its tiles'
-  // k-slices are split over a grid of every resident CTA.
+  // k-slices are split over a grid of every resident CTA -- and with fewer
+  // tiles than CTA slots, every tile's, as long as every CTA gets a slice.
   const int64_t slots = s->slots;
   const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
   const int64_t KT = (K + v->bk - 1) / v->bk;
   int64_t grid = tiles < slots ? tiles : slots;
-  if (tiles > slots && tiles % slots != 0 && KT >= 8) {
+  const bool tail = tiles > slots && tiles % slots != 0;
+  const bool small = tiles < slots && tiles * KT >= slots;
+  if ((tail || small) && KT >= 8) {
     if (slots > SGEMM_STATIC_SCRATCH_MAX_CTAS) return SGEMM_ERR_UNSUPPORTED;  // more partial tiles than the array holds
     grid = slots;
     a.dp_waves = static_cast<int>(tiles / slots);
