@@ -45,6 +45,8 @@ SIGNATURES = {
     "sgemm_selftest_wait_timeout": (_int, [ctypes.c_uint64, _vp]),
     "sgemm_run_static_scratch": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "sgemm_plan_ex": (_int, [_int, _int, _int, _i64, _i64, _i64, _i64, _i64, _i64, _int, ctypes.POINTER(_vp)]),
+    "sgemm_plan_ex_batched": (_int, [_int, _int, _int, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
+                                     _int, ctypes.POINTER(_vp)]),
     "sgemm_run_host_pipelined": (_int, [_vp, _int, _f32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _f32,
                                         ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                         ctypes.POINTER(_vp), _vp]),
@@ -175,11 +177,14 @@ class Plan:
         self.ldc = int(ldc) if ldc is not None else max(1, self.N if row else self.M)
         h = ctypes.c_void_p()
         if batch is not None:
-            if not row or transa or transb:
-                raise ValueError("strided batches are row-major and untransposed")
             cid = -1 if config is None else (config if isinstance(config, int) else config_id(config))
-            st = l.sgemm_plan_batched(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, int(batch), int(stride_a),
-                                      int(stride_b), int(stride_c), cid, ctypes.byref(h))
+            if not row or transa or transb:
+                st = l.sgemm_plan_ex_batched(0 if row else 1, 1 if transa else 0, 1 if transb else 0, self.M, self.N,
+                                             self.K, self.lda, self.ldb, self.ldc, int(batch), int(stride_a),
+                                             int(stride_b), int(stride_c), cid, ctypes.byref(h))
+            else:
+                st = l.sgemm_plan_batched(self.M, self.N, self.K, self.lda, self.ldb, self.ldc, int(batch),
+                                          int(stride_a), int(stride_b), int(stride_c), cid, ctypes.byref(h))
         elif not row or transa or transb:
             cid = -1 if config is None else (config if isinstance(config, int) else config_id(config))
             st = l.sgemm_plan_ex(0 if row else 1, 1 if transa else 0, 1 if transb else 0, self.M, self.N, self.K,

@@ -180,10 +180,13 @@ cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaSt
 
 // out (cols x rows, ld_out) = transpose of in (rows x cols, ld_in), through a
 // 32 x 33 shared tile so both the reads and the writes are coalesced.  Block
-// row blockIdx.y takes row tiles blockIdx.y, + gridDim.y, ... (any row count).
+// row blockIdx.y takes row tiles blockIdx.y, + gridDim.y, ... (any row count);
+// blockIdx.z is the product of a strided batch (in += z*stride_in, out += z*stride_out).
 __global__ void transpose_kernel(const float* __restrict__ in, int64_t ld_in, int rows, int cols,
-                                 float* __restrict__ out, int64_t ld_out) {
+                                 float* __restrict__ out, int64_t ld_out, int64_t stride_in, int64_t stride_out) {
   __shared__ float t[32][33];
+  in += blockIdx.z * stride_in;
+  out += blockIdx.z * stride_out;
   const int c0 = blockIdx.x * 32;
   const int row_tiles = (rows + 31) / 32;
   for (int ty = blockIdx.y; ty < row_tiles; ty += gridDim.y) {
@@ -202,11 +205,13 @@ __global__ void transpose_kernel(const float* __restrict__ in, int64_t ld_in, in
 }
 
 cudaError_t launch_transpose(const float* in, int64_t ld_in, int rows, int cols, float* out, int64_t ld_out,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, int batch, int64_t stride_in, int64_t stride_out) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
+  if (batch < 1) batch = 1;
+  if (batch > 65535) return cudaErrorInvalidConfiguration;
   const int row_tiles = (rows + 31) / 32;
-  const dim3 grid((cols + 31) / 32, row_tiles < 65535 ? row_tiles : 65535);
-  transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(in, ld_in, rows, cols, out, ld_out);
+  const dim3 grid((cols + 31) / 32, row_tiles < 65535 ? row_tiles : 65535, batch);
+  transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(in, ld_in, rows, cols, out, ld_out, stride_in, stride_out);
   return cudaGetLastError();
 }
 

@@ -392,7 +392,7 @@ struct SkinnySkParams {
 };
 
 // BT: B given transposed (stored N x K), loaded as swizzled [n][k] boxes.
-// BATCHED: a strided batch of products, B as stored (not BT).
+// BATCHED: a strided batch of products (B as stored, or given transposed).
 template <int BN, int GW, int STAGES, int MINB, bool EVICT_FIRST, bool BT, bool BATCHED = false>
 __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     sgemm_skinny_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -415,7 +415,6 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
   const int gw = warp % GW;
   const int G = static_cast<int>(gridDim.x);
   const int b = static_cast<int>(blockIdx.x);
-  static_assert(!(BT && BATCHED), "batches take B as stored");
   const int KT = (p.K + kSBK - 1) / kSBK;
   const int nslabs = (p.N + BN - 1) / BN;  // per product
   // slabs over every product: gs = z * nslabs + slab of product z
@@ -442,11 +441,12 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
       const int z = gs / nslabs;
       const int n0 = (gs - z * nslabs) * BN;
       ptx::tma_load_3d(dst, &tmA, kt * kSBK, 0, z * p.a_batched, bar_full + 8 * s);
+      const int bx = BT ? kt * kSBK : n0, by = BT ? n0 : kt * kSBK;  // B as [k][n], or Bt as [n][k]
       if constexpr (EVICT_FIRST)
-        ptx::tma_load_3d_hint(dst + S::kStageA, &tmB, n0, kt * kSBK, z * p.b_batched, bar_full + 8 * s,
+        ptx::tma_load_3d_hint(dst + S::kStageA, &tmB, bx, by, z * p.b_batched, bar_full + 8 * s,
                               ptx::l2_policy_evict_first());
       else
-        ptx::tma_load_3d(dst + S::kStageA, &tmB, n0, kt * kSBK, z * p.b_batched, bar_full + 8 * s);
+        ptx::tma_load_3d(dst + S::kStageA, &tmB, bx, by, z * p.b_batched, bar_full + 8 * s);
       return;
     }
     const int n0 = gs * BN;
@@ -626,11 +626,14 @@ struct SkinnySkVariant {
   static constexpr auto kernel = sgemm_skinny_sk_kernel<BN, GW, STAGES, MINB, EVICT_FIRST, false>;
   static constexpr auto kernel_bt = sgemm_skinny_sk_kernel<BN, GW, STAGES, MINB, EVICT_FIRST, true>;
   static constexpr auto kernel_batched = sgemm_skinny_sk_kernel<BN, GW, STAGES, MINB, EVICT_FIRST, false, true>;
+  static constexpr auto kernel_bt_batched = sgemm_skinny_sk_kernel<BN, GW, STAGES, MINB, EVICT_FIRST, true, true>;
   static cudaError_t prepare() {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel_bt, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(kernel_batched, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel_bt_batched, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     return e;
   }
   static cudaError_t occupancy(int* ctas) {
@@ -654,8 +657,9 @@ struct SkinnySkVariant {
     p.stride_c = a.stride_c;
     p.a_batched = a.batch > 1 && a.stride_a != 0;
     p.b_batched = a.batch > 1 && a.stride_b != 0;
-    if (p.batch > 1) {
-      if (a.b_trans) return cudaErrorInvalidValue;  // batches take B as stored
+    if (p.batch > 1 && a.b_trans) {
+      kernel_bt_batched<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    } else if (p.batch > 1) {
       kernel_batched<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
     } else if (a.b_trans) {
       kernel_bt<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);

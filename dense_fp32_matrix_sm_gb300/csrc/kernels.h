@@ -91,9 +91,10 @@ const Variant* tc_variants(int* count);
 cudaError_t launch_scale(float* C, int64_t ldc, int M, int N, float beta, cudaStream_t stream, int batch = 1,
                          int64_t stride_c = 0);
 
-// out (cols x rows, ld_out) = in (rows x cols, ld_in) transposed.
+// out (cols x rows, ld_out) = in (rows x cols, ld_in) transposed, for
+// `batch` products stride_in / stride_out apart.
 cudaError_t launch_transpose(const float* in, int64_t ld_in, int rows, int cols, float* out, int64_t ld_out,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int batch = 1, int64_t stride_in = 0, int64_t stride_out = 0);
 // dst = src with rows padded to 16-byte multiples (ldd % 4 == 0, dst 16-byte
 // aligned); src may have any leading dimension and alignment.
 cudaError_t launch_repack(const float* src, int64_t lds, int rows, int cols, float* dst, int64_t ldd,

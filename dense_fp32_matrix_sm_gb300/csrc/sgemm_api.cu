@@ -57,6 +57,9 @@ struct sgemm_plan_s {
   float* ex_wb;
   int ex_native_tb;  // the variant reads B given transposed (N x K) itself: no ex_wb
   int ex_native_ta;  // the variant reads A given transposed (K x M) itself: no ex_wa
+  // the caller's batch strides of the stored operands (after the swap); the
+  // kernels' own (stride_a / stride_b) differ when an operand goes through ex_wa / ex_wb
+  int64_t ex_stride_a, ex_stride_b;
   // An untransposed operand whose rows are not 16-byte multiples (lda or ldb
   // not a multiple of 4) is copied each run into rp_a / rp_b, rows padded
   // to lda / ldb (the kernels' view); ex_lda / ex_ldb keep the caller's.
@@ -158,15 +161,20 @@ sgemm_status_t check_dims(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
   return SGEMM_OK;
 }
 
+// a_span / b_span: elements one stored A / B spans (-1: M*lda / K*ldb, an
+// operand stored as the kernels read it)
 bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                      int64_t batch = 1, int64_t stride_a = 0, int64_t stride_b = 0) {
+                      int64_t batch = 1, int64_t stride_a = 0, int64_t stride_b = 0, int64_t a_span = -1,
+                      int64_t b_span = -1) {
   if (batch > 1) {
     if (!v->batched) return false;
     if (v->kind == kKindGeneric) return batch <= 65535;
     // 3-D tensor maps: 16-byte batch strides that do not overlap the matrices,
     // or 0 for an operand shared by every product
-    if (stride_a % 4 != 0 || stride_b % 4 != 0 || (stride_a != 0 && stride_a < M * lda) ||
-        (stride_b != 0 && stride_b < K * ldb))
+    if (a_span < 0) a_span = M * lda;
+    if (b_span < 0) b_span = K * ldb;
+    if (stride_a % 4 != 0 || stride_b % 4 != 0 || (stride_a != 0 && stride_a < a_span) ||
+        (stride_b != 0 && stride_b < b_span))
       return false;
   }
   if (v->kind == kKindGeneric) return true;
@@ -214,13 +222,15 @@ const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_
 // The per-shape config table.  Keys are shape classes; values are variant
 // names.  The entries come from the measured sweeps on GB300.
 const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms, int64_t batch = 1,
-                         int64_t stride_a = 0, int64_t stride_b = 0) {
+                         int64_t stride_a = 0, int64_t stride_b = 0, int64_t a_span = -1, int64_t b_span = -1) {
   if (batch > 1) {
     // Strided batches run on the batched variants only: the transposed-A
     // family when TMA can take the layout (tile counts over the whole batch),
     // else the scalar-load kernel.
+    if (a_span < 0) a_span = M * lda;
+    if (b_span < 0) b_span = K * ldb;
     if (ldb % 4 != 0 || lda % 4 != 0 || stride_a % 4 != 0 || stride_b % 4 != 0 ||
-        (stride_a != 0 && stride_a < M * lda) || (stride_b != 0 && stride_b < K * ldb))
+        (stride_a != 0 && stride_a < a_span) || (stride_b != 0 && stride_b < b_span))
       return "generic_64x64x16";
     // few rows: the stream-K few-row kernel over (product, slab, k-slice)
     // units, instead of 128-row tiles that are 7/8 empty
@@ -250,7 +260,7 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
 
 sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int config_id,
                          sgemm_plan_t* out, int64_t batch = 1, int64_t stride_a = 0, int64_t stride_b = 0,
-                         int64_t stride_c = 0) {
+                         int64_t stride_c = 0, int64_t a_span = -1, int64_t b_span = -1) {
   if (!out) return SGEMM_ERR_INVALID_ARG;
   sgemm_status_t st = check_dims(M, N, K, lda, ldb, ldc);
   if (st != SGEMM_OK) return st;
@@ -281,12 +291,13 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
         if (rp_a) lda = (K + 3) / 4 * 4;
         if (rp_b) ldb = (N + 3) / 4 * 4;
       }
-      config_id = find_variant(table_choice(M, N, K, lda, ldb, sms, batch, stride_a, stride_b));
+      config_id = find_variant(table_choice(M, N, K, lda, ldb, sms, batch, stride_a, stride_b, a_span, b_span));
       if (config_id < 0) config_id = reg.first_generic;
     }
   }
   const Variant* v = reg.all[config_id];
-  if (!variant_supports(v, M, N, K, lda, ldb, batch, stride_a, stride_b)) return SGEMM_ERR_UNSUPPORTED;
+  if (!variant_supports(v, M, N, K, lda, ldb, batch, stride_a, stride_b, a_span, b_span))
+    return SGEMM_ERR_UNSUPPORTED;
   if (v->kind != kKindGeneric && v->tma_swizzle_a >= 0 && !encode_fn()) return SGEMM_ERR_CUDA;
 
   unsigned int* status = nullptr;
@@ -310,6 +321,8 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->batch = batch;
   p->stride_a = stride_a;
   p->stride_b = stride_b;
+  p->ex_stride_a = stride_a;
+  p->ex_stride_b = stride_b;
   p->stride_c = stride_c;
   p->device = device;
   p->num_sms = sms;
@@ -465,11 +478,12 @@ sgemm_status_t encode_maps(const Variant* v, const sgemm_plan_s* p, const float*
   const cuuint64_t nb_a = static_cast<cuuint64_t>(p->batch > 1 && p->stride_a != 0 ? p->batch : 1);
   const cuuint64_t nb_b = static_cast<cuuint64_t>(p->batch > 1 && p->stride_b != 0 ? p->batch : 1);
   if (a->a_trans) {  // A given transposed (K x M): [bk][bm] boxes, M innermost, unswizzled
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->M), static_cast<cuuint64_t>(p->K)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->ex_lda) * 4};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(v->bm), static_cast<cuuint32_t>(v->bk)};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&a->tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides, box, estr,
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->M), static_cast<cuuint64_t>(p->K), nb_a};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p->ex_lda) * 4,
+                                   static_cast<cuuint64_t>(nb_a > 1 ? p->stride_a : p->K * p->ex_lda) * 4};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(v->bm), static_cast<cuuint32_t>(v->bk), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(&a->tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<float*>(A), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
@@ -488,11 +502,12 @@ sgemm_status_t encode_maps(const Variant* v, const sgemm_plan_s* p, const float*
     if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
   }
   if (a->b_trans) {  // B given transposed (N x K): K-major boxes of 32 k x bn rows, 128-byte swizzle
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->N)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->ex_ldb) * 4};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(v->bk), static_cast<cuuint32_t>(v->bn)};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&a->tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides, box, estr,
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->N), nb_b};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p->ex_ldb) * 4,
+                                   static_cast<cuuint64_t>(nb_b > 1 ? p->stride_b : p->N * p->ex_ldb) * 4};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(v->bk), static_cast<cuuint32_t>(v->bn), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(&a->tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<float*>(B), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return SGEMM_ERR_CUDA;
@@ -559,7 +574,7 @@ bool spans_overlap(const sgemm_plan_s* p, const float* C, const float* X, bool i
   const int64_t cols = internal_a ? (p->ex_ta ? p->M : p->K) : (p->ex_tb ? p->K : p->N);
   const int64_t ld = internal_a ? p->ex_lda : p->ex_ldb;
   const int64_t nb = p->batch > 1 ? p->batch : 1;
-  const int64_t stride = internal_a ? p->stride_a : p->stride_b;
+  const int64_t stride = internal_a ? p->ex_stride_a : p->ex_stride_b;
   const uintptr_t x0 = reinterpret_cast<uintptr_t>(X);
   const uintptr_t x1 = x0 + static_cast<uintptr_t>(((rows - 1) * ld + cols + (nb - 1) * stride) * 4);
   const uintptr_t c0 = reinterpret_cast<uintptr_t>(C);
@@ -581,10 +596,11 @@ sgemm_status_t copy_inputs(const sgemm_plan_s* p, bool product, float beta, cons
     const int64_t ra_u = p->ex_swap ? rb : ra, ca_u = p->ex_swap ? cb : ca, lda_u = p->ex_swap ? p->ex_ldb : p->ex_lda;
     const int64_t rb_u = p->ex_swap ? ra : rb, cb_u = p->ex_swap ? ca : cb, ldb_u = p->ex_swap ? p->ex_lda : p->ex_ldb;
     for (int64_t z = 0; z < nb; ++z) {
-      if (cudaMemcpy2DAsync(dA + z * p->stride_a, lda_u * fs, hA + z * p->stride_a, lda_u * fs, ca_u * fs, ra_u,
+      const int64_t sa_u = p->ex_swap ? p->ex_stride_b : p->ex_stride_a, sb_u = p->ex_swap ? p->ex_stride_a : p->ex_stride_b;
+      if (cudaMemcpy2DAsync(dA + z * sa_u, lda_u * fs, hA + z * sa_u, lda_u * fs, ca_u * fs, ra_u,
                             cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return SGEMM_ERR_CUDA;
-      if (cudaMemcpy2DAsync(dB + z * p->stride_b, ldb_u * fs, hB + z * p->stride_b, ldb_u * fs, cb_u * fs, rb_u,
+      if (cudaMemcpy2DAsync(dB + z * sb_u, ldb_u * fs, hB + z * sb_u, ldb_u * fs, cb_u * fs, rb_u,
                             cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return SGEMM_ERR_CUDA;
     }
@@ -605,6 +621,120 @@ sgemm_status_t copy_output(const sgemm_plan_s* p, float* hC, const float* dC, cu
     if (cudaMemcpy2DAsync(hC + z * p->stride_c, p->ldc * fs, dC + z * p->stride_c, p->ldc * fs, p->N * fs, p->M,
                           cudaMemcpyDeviceToHost, stream) != cudaSuccess)
       return SGEMM_ERR_CUDA;
+  return SGEMM_OK;
+}
+
+// sgemm_plan_ex and sgemm_plan_ex_batched: storage order and transposed
+// operands, for one product (batch 1) or a strided batch.
+sgemm_status_t make_plan_ex(int order, int transa, int transb, int64_t M, int64_t N, int64_t K, int64_t lda,
+                            int64_t ldb, int64_t ldc, int config_id, sgemm_plan_t* out, int64_t batch = 1,
+                            int64_t stride_a = 0, int64_t stride_b = 0, int64_t stride_c = 0) {
+  if (!out) return SGEMM_ERR_INVALID_ARG;
+  if ((order != SGEMM_ROW_MAJOR && order != SGEMM_COL_MAJOR) || (transa != SGEMM_NO_TRANS && transa != SGEMM_TRANS) ||
+      (transb != SGEMM_NO_TRANS && transb != SGEMM_TRANS))
+    return SGEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+  // leading dimensions of the stored matrices, in the given order
+  const int64_t a_rows = transa ? K : M, a_cols = transa ? M : K;
+  const int64_t b_rows = transb ? N : K, b_cols = transb ? K : N;
+  const bool row = order == SGEMM_ROW_MAJOR;
+  if (lda < std::max<int64_t>(1, row ? a_cols : a_rows) || ldb < std::max<int64_t>(1, row ? b_cols : b_rows) ||
+      ldc < std::max<int64_t>(1, row ? N : M))
+    return SGEMM_ERR_INVALID_ARG;
+  // Column-major C = op(A) op(B) is the row-major C^T = op(B)^T op(A)^T over
+  // the same memory: swap the operands, their transpose flags and strides.
+  const int swap = row ? 0 : 1;
+  const int64_t M2 = swap ? N : M, N2 = swap ? M : N;
+  const int ta = swap ? transb : transa, tb = swap ? transa : transb;
+  const int64_t lda2 = swap ? ldb : lda, ldb2 = swap ? lda : ldb;
+  const int64_t sa2 = swap ? stride_b : stride_a, sb2 = swap ? stride_a : stride_b;
+  if (M2 > 0x7fffffff || N2 > 0x7fffffff || K > 0x7fffffff) return SGEMM_ERR_UNSUPPORTED;
+  const bool batched = batch > 1;
+
+  const Registry& reg = registry();
+  if (config_id >= static_cast<int>(reg.all.size())) return SGEMM_ERR_INVALID_ARG;
+  int forced = config_id;
+  if (forced < 0) {
+    const char* env = getenv("SGEMM_FORCE_CONFIG");
+    if (env && *env) forced = find_variant(env);
+  }
+  const bool native = forced >= 0 && (reg.all[forced]->kind == kKindTc ||
+                                      reg.all[forced]->kind == kKindTcFused);  // reads either layout itself
+  if (native && reg.all[forced]->kind == kKindTcFused && (lda2 % 4 != 0 || ldb2 % 4 != 0))
+    return SGEMM_ERR_UNSUPPORTED;
+  // the row-major, untransposed operands the other kernels read: a
+  // transposed operand goes through a plan buffer with a 16-byte row stride
+  const int64_t lda_eff = ta && !native ? std::max<int64_t>(4, (K + 3) / 4 * 4) : (ta ? (K + 3) / 4 * 4 : lda2);
+  const int64_t ldb_eff = tb && !native ? std::max<int64_t>(4, (N2 + 3) / 4 * 4) : (tb ? (N2 + 3) / 4 * 4 : ldb2);
+  // A batch decides up front which transposed operand the kernel reads as
+  // stored (its batch stride and extent are then the caller's), using the
+  // table's rule: few rows read B given transposed, the transposed-A kernels
+  // A given transposed; a forced variant says for itself.  If the plan then
+  // gets a kernel that cannot (the table fell back to the scalar-load
+  // kernel, say), it is made again with both operands through buffers.
+  bool nat_a = false, nat_b = false;
+  if (batched) {
+    nat_a = ta && lda2 % 4 == 0 && (forced >= 0 ? reg.all[forced]->a_trans_ok != 0 : M2 > 16);
+    nat_b = tb && ldb2 % 4 == 0 && (forced >= 0 ? reg.all[forced]->b_trans_ok != 0 : M2 <= 16);
+  }
+  sgemm_plan_t p = nullptr;
+  sgemm_status_t st = SGEMM_OK;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    // the kernels' batch strides and the extent of one stored operand
+    const int64_t ka_stride = ta && !nat_a ? (sa2 == 0 ? 0 : M2 * lda_eff) : sa2;
+    const int64_t kb_stride = tb && !nat_b ? (sb2 == 0 ? 0 : K * ldb_eff) : sb2;
+    const int64_t a_span = nat_a ? K * lda2 : -1;
+    const int64_t b_span = nat_b ? N2 * ldb2 : -1;
+    st = batched ? make_plan(M2, N2, K, lda_eff, ldb_eff, ldc, config_id, &p, batch, ka_stride, kb_stride, stride_c,
+                             a_span, b_span)
+                 : make_plan(M2, N2, K, lda_eff, ldb_eff, ldc, config_id, &p);
+    if (!batched || (!nat_a && !nat_b)) break;
+    const Variant* got = st == SGEMM_OK ? registry().all[p->config_id] : nullptr;
+    if (got && (!nat_a || got->a_trans_ok) && (!nat_b || got->b_trans_ok)) break;
+    if (st == SGEMM_OK) sgemm_plan_destroy(p);
+    p = nullptr;
+    nat_a = nat_b = false;
+  }
+  if (st != SGEMM_OK) return st;
+  p->ex_order = order;
+  p->ex_swap = swap;
+  p->ex_ta = ta;
+  p->ex_tb = tb;
+  p->ex_lda = lda2;
+  p->ex_ldb = ldb2;
+  p->ex_stride_a = batched ? sa2 : 0;
+  p->ex_stride_b = batched ? sb2 : 0;
+  const Variant* chosen = registry().all[p->config_id];
+  const int kind = chosen->kind;
+  if (batched) {
+    if (kind == kKindTc || kind == kKindTcFused) {  // not batched (make_plan refuses them too)
+      sgemm_plan_destroy(p);
+      return SGEMM_ERR_UNSUPPORTED;
+    }
+    p->ex_native_ta = nat_a ? 1 : 0;
+    p->ex_native_tb = nat_b ? 1 : 0;
+  } else {
+    // a few-row kernel reads B given transposed (N x K, K contiguous) by TMA itself
+    if (tb && !native && chosen->b_trans_ok && ldb2 % 4 == 0) p->ex_native_tb = 1;
+    // the transposed-A kernels read A given transposed (K x M, M contiguous) by TMA themselves
+    if (ta && !native && chosen->a_trans_ok && lda2 % 4 == 0) p->ex_native_ta = 1;
+  }
+  if (!native && kind != kKindTc && kind != kKindTcFused) {
+    // transposed operands the kernel does not read as stored: plan buffers,
+    // one per product of a batch (one for a shared operand)
+    const int64_t nba = batched && sa2 != 0 ? batch : 1, nbb = batched && sb2 != 0 ? batch : 1;
+    if (ta && !p->ex_native_ta && M2 > 0 && K > 0 &&
+        cudaMalloc(reinterpret_cast<void**>(&p->ex_wa), sizeof(float) * nba * M2 * lda_eff) != cudaSuccess) {
+      sgemm_plan_destroy(p);
+      return SGEMM_ERR_CUDA;
+    }
+    if (tb && !p->ex_native_tb && N2 > 0 && K > 0 &&
+        cudaMalloc(reinterpret_cast<void**>(&p->ex_wb), sizeof(float) * nbb * K * ldb_eff) != cudaSuccess) {
+      sgemm_plan_destroy(p);
+      return SGEMM_ERR_CUDA;
+    }
+  }
+  *out = p;
   return SGEMM_OK;
 }
 
@@ -707,69 +837,21 @@ sgemm_status_t sgemm_plan_batched(int64_t M, int64_t N, int64_t K, int64_t lda, 
 
 sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64_t N, int64_t K, int64_t lda,
                              int64_t ldb, int64_t ldc, int config_id, sgemm_plan_t* out) {
-  if (!out) return SGEMM_ERR_INVALID_ARG;
-  if ((order != SGEMM_ROW_MAJOR && order != SGEMM_COL_MAJOR) || (transa != SGEMM_NO_TRANS && transa != SGEMM_TRANS) ||
-      (transb != SGEMM_NO_TRANS && transb != SGEMM_TRANS))
-    return SGEMM_ERR_INVALID_ARG;
-  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
-  // leading dimensions of the stored matrices, in the given order
-  const int64_t a_rows = transa ? K : M, a_cols = transa ? M : K;
-  const int64_t b_rows = transb ? N : K, b_cols = transb ? K : N;
-  const bool row = order == SGEMM_ROW_MAJOR;
-  if (lda < std::max<int64_t>(1, row ? a_cols : a_rows) || ldb < std::max<int64_t>(1, row ? b_cols : b_rows) ||
-      ldc < std::max<int64_t>(1, row ? N : M))
-    return SGEMM_ERR_INVALID_ARG;
-  // Column-major C = op(A) op(B) is the row-major C^T = op(B)^T op(A)^T over
-  // the same memory: swap the operands and their transpose flags.
-  const int swap = row ? 0 : 1;
-  const int64_t M2 = swap ? N : M, N2 = swap ? M : N;
-  const int ta = swap ? transb : transa, tb = swap ? transa : transb;
-  const int64_t lda2 = swap ? ldb : lda, ldb2 = swap ? lda : ldb;
-  if (M2 > 0x7fffffff || N2 > 0x7fffffff || K > 0x7fffffff) return SGEMM_ERR_UNSUPPORTED;
+  return make_plan_ex(order, transa, transb, M, N, K, lda, ldb, ldc, config_id, out);
+}
 
-  const Registry& reg = registry();
-  if (config_id >= static_cast<int>(reg.all.size())) return SGEMM_ERR_INVALID_ARG;
-  int forced = config_id;
-  if (forced < 0) {
-    const char* env = getenv("SGEMM_FORCE_CONFIG");
-    if (env && *env) forced = find_variant(env);
-  }
-  const bool native = forced >= 0 && (reg.all[forced]->kind == kKindTc ||
-                                      reg.all[forced]->kind == kKindTcFused);  // reads either layout itself
-  if (native && reg.all[forced]->kind == kKindTcFused && (lda2 % 4 != 0 || ldb2 % 4 != 0))
-    return SGEMM_ERR_UNSUPPORTED;
-  // the row-major, untransposed operands the other kernels read: a
-  // transposed operand goes through a plan buffer with a 16-byte row stride
-  const int64_t lda_eff = ta && !native ? std::max<int64_t>(4, (K + 3) / 4 * 4) : (ta ? (K + 3) / 4 * 4 : lda2);
-  const int64_t ldb_eff = tb && !native ? std::max<int64_t>(4, (N2 + 3) / 4 * 4) : (tb ? (N2 + 3) / 4 * 4 : ldb2);
-  sgemm_plan_t p = nullptr;
-  sgemm_status_t st = make_plan(M2, N2, K, lda_eff, ldb_eff, ldc, config_id, &p);
-  if (st != SGEMM_OK) return st;
-  p->ex_order = order;
-  p->ex_swap = swap;
-  p->ex_ta = ta;
-  p->ex_tb = tb;
-  p->ex_lda = lda2;
-  p->ex_ldb = ldb2;
-  const Variant* chosen = registry().all[p->config_id];
-  const int kind = chosen->kind;
-  // a few-row kernel reads B given transposed (N x K, K contiguous) by TMA itself
-  if (tb && !native && chosen->b_trans_ok && ldb2 % 4 == 0) p->ex_native_tb = 1;
-  // the transposed-A kernels read A given transposed (K x M, M contiguous) by TMA themselves
-  if (ta && !native && chosen->a_trans_ok && lda2 % 4 == 0) p->ex_native_ta = 1;
-  if (!native && kind != kKindTc && kind != kKindTcFused) {
-    if (ta && !p->ex_native_ta && M2 > 0 && K > 0 && cudaMalloc(reinterpret_cast<void**>(&p->ex_wa), sizeof(float) * M2 * lda_eff) != cudaSuccess) {
-      sgemm_plan_destroy(p);
-      return SGEMM_ERR_CUDA;
-    }
-    if (tb && !p->ex_native_tb && N2 > 0 && K > 0 &&
-        cudaMalloc(reinterpret_cast<void**>(&p->ex_wb), sizeof(float) * K * ldb_eff) != cudaSuccess) {
-      sgemm_plan_destroy(p);
-      return SGEMM_ERR_CUDA;
-    }
-  }
-  *out = p;
-  return SGEMM_OK;
+sgemm_status_t sgemm_plan_ex_batched(int order, int transa, int transb, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                     int64_t ldb, int64_t ldc, int64_t batch, int64_t stride_a, int64_t stride_b,
+                                     int64_t stride_c, int config_id, sgemm_plan_t* out) {
+  if (!out) return SGEMM_ERR_INVALID_ARG;
+  if (batch < 0 || stride_a < 0 || stride_b < 0 || stride_c < 0 || config_id < -1) return SGEMM_ERR_INVALID_ARG;
+  // the products' C matrices must not overlap (A and B may be shared: stride 0)
+  const bool row = order == SGEMM_ROW_MAJOR;
+  if (batch > 1 && M > 0 && N > 0 && stride_c < (row ? (M - 1) * ldc + N : (N - 1) * ldc + M))
+    return SGEMM_ERR_INVALID_ARG;
+  if (batch > 65535) return SGEMM_ERR_UNSUPPORTED;
+  return make_plan_ex(order, transa, transb, M, N, K, lda, ldb, ldc, config_id, out, batch, stride_a, stride_b,
+                      stride_c);
 }
 
 sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const float* B, float beta, float* C,
@@ -814,15 +896,18 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
       return SGEMM_ERR_CUDA;
     B = p->rp_b;
   }
+  // (a strided batch transposes every product's operand; a shared one once)
   if (p->ex_wa) {
-    if (launch_transpose(A, p->ex_lda, static_cast<int>(p->K), static_cast<int>(p->M), p->ex_wa, p->lda, stream) !=
-        cudaSuccess)
+    const int nb = p->batch > 1 && p->ex_stride_a != 0 ? static_cast<int>(p->batch) : 1;
+    if (launch_transpose(A, p->ex_lda, static_cast<int>(p->K), static_cast<int>(p->M), p->ex_wa, p->lda, stream, nb,
+                         p->ex_stride_a, p->stride_a) != cudaSuccess)
       return SGEMM_ERR_CUDA;
     A = p->ex_wa;
   }
   if (p->ex_wb) {
-    if (launch_transpose(B, p->ex_ldb, static_cast<int>(p->N), static_cast<int>(p->K), p->ex_wb, p->ldb, stream) !=
-        cudaSuccess)
+    const int nb = p->batch > 1 && p->ex_stride_b != 0 ? static_cast<int>(p->batch) : 1;
+    if (launch_transpose(B, p->ex_ldb, static_cast<int>(p->N), static_cast<int>(p->K), p->ex_wb, p->ldb, stream, nb,
+                         p->ex_stride_b, p->stride_b) != cudaSuccess)
       return SGEMM_ERR_CUDA;
     B = p->ex_wb;
   }

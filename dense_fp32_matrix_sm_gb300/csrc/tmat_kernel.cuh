@@ -133,7 +133,6 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
   constexpr int BM = S::BM;
   constexpr int BK = S::BK;
   static_assert(TA >= 0 && TA < BK && TB < BK && (TB < 0 || TB > TA), "transpose steps inside the k loop");
-  static_assert(!(AT && BATCHED), "A given transposed: single products only");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ int s_fail;
   __shared__ __align__(8) unsigned long long s_sync[4];  // SPLIT: at_full[2], slice_done[2]
@@ -234,7 +233,10 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
     const uint32_t dst = smem_base + s * S::kStageBytes;
     ptx::mbar_arrive_expect_tx(bar_full + 8 * s, S::kStageBytes);
     if constexpr (BATCHED) {
-      ptx::tma_load_3d(dst, &tmA, c_kt * BK, c_tm * BM, c_z * p.a_batched, bar_full + 8 * s);
+      if constexpr (AT)
+        ptx::tma_load_3d(dst, &tmA, c_tm * BM, c_kt * BK, c_z * p.a_batched, bar_full + 8 * s);
+      else
+        ptx::tma_load_3d(dst, &tmA, c_kt * BK, c_tm * BM, c_z * p.a_batched, bar_full + 8 * s);
       ptx::tma_load_3d(dst + S::kStageA, &tmB, c_tn * BN, c_kt * BK, c_z * p.b_batched, bar_full + 8 * s);
     } else {
       if constexpr (AT)
@@ -522,13 +524,16 @@ template <int BM_, int BN, int STAGES, int MINB, int TA, int TB = -1, bool SPLIT
 struct Variant_ {
   using S = Shape<BM_, BN, STAGES>;
   // a single product runs the plain 2-D kernel (or, A given transposed, its
-  // AT form); strided batches their own instantiation
+  // AT form); strided batches their own instantiations
   static constexpr auto kernel = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, false, TA, TB, SPLIT>;
   static constexpr auto kernel_at = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, false, TA, TB, SPLIT, true>;
   static constexpr auto kernel_batched = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, true, TA, TB, SPLIT>;
+  static constexpr auto kernel_at_batched = sgemm_tmat_kernel<BM_, BN, STAGES, MINB, true, TA, TB, SPLIT, true>;
   static cudaError_t prepare() {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel_at, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel_at_batched, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     return e != cudaSuccess ? e
                             : cudaFuncSetAttribute(kernel_batched, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    S::kSmemBytes);
@@ -559,8 +564,9 @@ struct Variant_ {
     p.stride_c = a.stride_c;
     p.a_batched = a.batch > 1 && a.stride_a != 0;
     p.b_batched = a.batch > 1 && a.stride_b != 0;
-    if (p.batch > 1) {
-      if (a.a_trans) return cudaErrorInvalidValue;  // A given transposed: single products only
+    if (p.batch > 1 && a.a_trans) {
+      kernel_at_batched<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
+    } else if (p.batch > 1) {
       kernel_batched<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
     } else if (a.a_trans) {
       kernel_at<<<a.grid, S::kThreads, S::kSmemBytes, stream>>>(a.tmA, a.tmB, p);
@@ -572,7 +578,7 @@ struct Variant_ {
   static Variant describe(const char* name) {
     Variant v{name, kKindTma, S::BM, BN, S::BK, STAGES, 1, S::kThreads, S::kSmemBytes, 128,
               &prepare, &occupancy, &launch, 0, 1, 1};
-    v.a_trans_ok = 1;  // reads A given transposed (K x M) by TMA itself, single products
+    v.a_trans_ok = 1;  // reads A given transposed (K x M) by TMA itself
     return v;
   }
 };

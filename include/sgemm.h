@@ -236,6 +236,31 @@ sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64
                              int64_t ldb, int64_t ldc, int config_id, sgemm_plan_t *out);
 
 /*
+ * sgemm_plan_ex for a strided batch: C_z = alpha * op(A_z) * op(B_z) + beta * C_z,
+ * z = 0 .. batch-1, every operand stored in `order` (with transa / transb as
+ * in sgemm_plan_ex) and the products stride_a / stride_b / stride_c floats
+ * apart (0: one A or B shared by every product).  Run it with sgemm_run on
+ * the base pointers.
+ *
+ * Argument rules: those of sgemm_plan_ex and sgemm_plan_batched; the C
+ * matrices must not overlap (stride_c at least one stored C, else
+ * SGEMM_ERR_INVALID_ARG).
+ *
+ * How it runs: as sgemm_plan_ex over the whole batch in one launch
+ * (column-major swaps the operands and their strides).  A transposed
+ * operand is read as stored where a kernel can (the product's A by the
+ * transposed-A kernels when the product has more than 16 rows, the
+ * product's B by the few-row kernel otherwise; leading dimension a multiple
+ * of 4); otherwise every product's operand is transposed first into a plan
+ * buffer (batch times the operand; one for a shared operand).  The
+ * split-TF32 variants do not run batches.  Runs of a plan must not overlap
+ * in time.
+ */
+sgemm_status_t sgemm_plan_ex_batched(int order, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                                     int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t stride_a,
+                                     int64_t stride_b, int64_t stride_c, int config_id, sgemm_plan_t *out);
+
+/*
  * Enqueue C = alpha*A*B + beta*C on `stream` (a cudaStream_t, may be NULL).
  * A, B, C are device pointers with the plan's shape and leading dimensions.
  * A and B may be NULL only when K == 0 or alpha == 0; C may be NULL only

@@ -70,6 +70,22 @@ def test_invalid_arguments_rejected_without_gpu(lib):
     assert lib.sgemm_plan_destroy(None) == 0
 
 
+def test_plan_ex_batched_rejects_before_cuda(lib):
+    """sgemm_plan_ex_batched checks the batch, strides and order before any CUDA call."""
+    h = ctypes.c_void_p()
+    f = lib.sgemm_plan_ex_batched
+    ok = (0, 0, 0, 64, 32, 16, 16, 32, 32)
+    assert f(*ok, -1, 0, 0, 0, -1, ctypes.byref(h)) == -1                 # negative batch
+    assert f(*ok, 4, -4, 0, 2048, -1, ctypes.byref(h)) == -1              # negative stride
+    assert f(*ok, 4, 0, 0, 2047, -1, ctypes.byref(h)) == -1               # row-major C overlap: needs 63*32+32
+    assert f(1, 0, 0, 64, 32, 16, 64, 16, 64, 4, 0, 0, 2047, -1, ctypes.byref(h)) == -1  # column-major: 31*64+64
+    assert f(*ok, 65536, 0, 0, 2048, -1, ctypes.byref(h)) == -2           # more products than a grid dimension
+    assert f(*ok, 4, 0, 0, 2048, -2, ctypes.byref(h)) == -1               # bad config id
+    assert f(2, 0, 0, 64, 32, 16, 16, 32, 32, 4, 0, 0, 2048, -1, ctypes.byref(h)) == -1  # bad order
+    assert f(*ok, 4, 0, 0, 2048, -1, None) == -1                          # no output
+    assert not h.value
+
+
 def test_plan_ex_rejects_before_cuda(lib):
     """sgemm_plan_ex checks order, flags and stored leading dimensions before any CUDA call."""
     h = ctypes.c_void_p()

@@ -676,6 +676,58 @@ def test_strided_batch(sg, oracle_mod, case):
     plan.close()
 
 
+@pytest.mark.parametrize("order", ["row", "col"])
+@pytest.mark.parametrize("ta,tb", [(False, False), (False, True), (True, False), (True, True)])
+@pytest.mark.parametrize("case", [
+    # (M, N, K, batch, shared A?): more than 16 rows (the transposed-A kernels read
+    # A given transposed), few rows (the few-row kernel reads B given transposed)
+    (300, 260, 96, 3, False), (16, 520, 264, 4, False), (7, 300, 100, 3, True), (200, 136, 64, 2, True)])
+def test_batched_order_and_transpose(sg, oracle_mod, order, ta, tb, case):
+    """sgemm_plan_ex_batched: every order x transpose combination of a strided
+    batch, against the oracle product by product."""
+    M, N, K, batch, shared_a = case
+    rng = np.random.default_rng(M + N + K + batch + 2 * ta + tb)
+    opA = rng.standard_normal((batch, M, K), dtype=np.float32)
+    if shared_a:
+        opA[1:] = opA[0]
+    opB = rng.standard_normal((batch, K, N), dtype=np.float32)
+    C0 = rng.uniform(-1, 1, (batch, M, N)).astype(np.float32)
+    alpha, beta = 0.5, -1.25
+    mems_a = [_stored(opA[z], order, ta, 0) for z in range(batch)]
+    mems_b = [_stored(opB[z], order, tb, 0) for z in range(batch)]
+    mems_c = [_stored(C0[z], order, False, 0) for z in range(batch)]
+    lda, ldb, ldc = mems_a[0][1], mems_b[0][1], mems_c[0][1]
+
+    def pack(mems, shared=False):
+        size = mems[0][0].size
+        stride = 0 if shared else (size + 3) // 4 * 4 + 4  # 16-byte multiples, padding between products
+        buf = torch.zeros(max(1, (0 if shared else len(mems) - 1) * stride + size), device="cuda")
+        for z, (m, _) in enumerate(mems[:1] if shared else mems):
+            buf[z * stride: z * stride + size] = torch.from_numpy(m.ravel())
+        return buf, stride
+
+    dA, sa = pack(mems_a, shared_a)
+    dB, sb = pack(mems_b)
+    dC, sc = pack(mems_c)
+    plan = sg.Plan(M, N, K, lda, ldb, ldc, order=order, transa=ta, transb=tb, batch=batch, stride_a=sa,
+                   stride_b=sb, stride_c=sc)
+    info = plan.info()
+    assert info["batch"] == batch and info["order"] == order
+    plan.run(alpha, dA, dB, beta, dC)
+    torch.cuda.synchronize()
+    assert sg.device_status() == sg.SGEMM_OK
+    out = dC.cpu().numpy()
+    size_c = mems_c[0][0].size
+    for z in range(batch):
+        Cref, S = oracle_mod.sgemm_ref(opA[z], opB[z], C0[z], alpha, beta)
+        mem = out[z * sc: z * sc + size_c].reshape(mems_c[0][0].shape)
+        Cz = mem if order == "row" else mem.T
+        assert_parity(Cz, Cref, S, K, f"batch {z}/{batch} {order} op={info['op']} {info['variant']} {case}")
+        if z + 1 < batch:
+            assert np.all(out[z * sc + size_c: (z + 1) * sc] == 0.0)
+    plan.close()
+
+
 def test_strided_batch_argument_errors(sg):
     l = sg.lib()
     h = ctypes.c_void_p()
