@@ -95,8 +95,9 @@ typedef enum {
  * dimensions, picks a kernel variant from the per-shape config table
  * (measured on GB300) and prepares it.  Allocates host memory, plus a
  * device workspace of grid * tile_m * tile_n floats and grid flags
- * (cudaMalloc) when the choice splits the last, partial wave of tiles
- * along K across the whole grid (stream-K; describe reports streamk=1).
+ * (cudaMalloc) when the choice splits the last, partial wave of tiles --
+ * or, with fewer tiles than CTA slots, every tile -- along K across the
+ * whole grid (stream-K; describe reports streamk=1).
  * That workspace makes the sum order along K for the tail tiles a fixed
  * split: results stay bit-identical from run to run.
  * From M*N*K >= 2^24 on, an operand whose leading dimension is not a
