@@ -6,7 +6,6 @@ in the process does the per-device set-up).  Each case runs two calls in a
 row on different inputs and compares each, bit for bit, with sgemm_run of
 a plan made with the same kernel variant (same schedule, same sum order),
 and with the fp64 oracle within the acceptance bound."""
-import ctypes
 
 import numpy as np
 import pytest
