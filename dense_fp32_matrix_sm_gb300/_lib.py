@@ -154,6 +154,16 @@ def _ptr(x) -> Optional[int]:
     return x.data_ptr() or None
 
 
+def _dev_ptr(x, name: str) -> Optional[int]:
+    """A device address for sgemm_run: raw integers pass through; a tensor must
+    be float32 and on a CUDA device (a host or half-precision buffer handed to
+    the kernels would be read as device float32)."""
+    if x is not None and not isinstance(x, int):
+        if getattr(x, "is_cuda", False) is not True or str(getattr(x, "dtype", "")) != "torch.float32":
+            raise TypeError(f"{name} must be a float32 CUDA tensor or a device address")
+    return _ptr(x)
+
+
 class Plan:
     """A plan for one (M, N, K, lda, ldb, ldc) on the current CUDA device.
 
@@ -204,8 +214,8 @@ class Plan:
 
     def run(self, alpha: float, A, B, beta: float, C, stream=None) -> None:
         """Enqueue C = alpha*A*B + beta*C.  A, B, C: CUDA tensors (or raw device addresses)."""
-        _check(lib().sgemm_run(self._h, float(alpha), _ptr(A), _ptr(B), float(beta), _ptr(C),
-                               _stream_handle(stream)), "sgemm_run")
+        _check(lib().sgemm_run(self._h, float(alpha), _dev_ptr(A, "A"), _dev_ptr(B, "B"), float(beta),
+                               _dev_ptr(C, "C"), _stream_handle(stream)), "sgemm_run")
 
     def run_host(self, alpha: float, hA, hB, beta: float, hC, dA, dB, dC, stream=None) -> None:
         """Host buffers in, host result out: H2D copies, the kernel, D2H copy, all on `stream`."""

@@ -319,6 +319,12 @@ def test_argument_errors_on_gpu(sg):
     with pytest.raises(sg.SgemmError) as e:
         plan.run(1.0, None, None, 0.0, None)
     assert e.value.status == sg.SGEMM_ERR_INVALID_ARG
+    # the binding refuses host and non-float32 tensors before the library sees them
+    dev = torch.zeros(8, 8, device="cuda")
+    with pytest.raises(TypeError):
+        plan.run(1.0, torch.zeros(8, 8), dev, 0.0, dev)
+    with pytest.raises(TypeError):
+        plan.run(1.0, dev, dev.half(), 0.0, dev)
     plan.close()
     with pytest.raises(sg.SgemmError) as e:
         sg.Plan(64, 64, 64, lda=65, config=next(n for n in sg.config_names() if n.startswith("tma_")))
