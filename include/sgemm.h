@@ -256,6 +256,12 @@ sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64
  * buffer (batch times the operand; one for a shared operand).  The
  * split-TF32 variants do not run batches.  Runs of a plan must not overlap
  * in time.
+ *
+ * The pages neither batch nor transpose; this combines the BLAS SGEMM
+ * conventions of sgemm_plan_ex with the strided batch of sgemm_plan_batched.
+ * Attention (one product per head, S = Q K^T then O = P V) is the motivating
+ * case in "How a Matmul Kernel Gets Fast", "What this means for real
+ * workloads".
  */
 sgemm_status_t sgemm_plan_ex_batched(int order, int transa, int transb, int64_t M, int64_t N, int64_t K,
                                      int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t stride_a,
