@@ -1,8 +1,9 @@
 // tc_tf32x3.cu -- C = alpha*A*B + beta*C in float32 on the 5th-generation
 // tensor cores, with each operand split into two TF32 parts ("3xTF32").
 //
-// The pages name tensor cores as the way past the FP32 FMA pipe ("How a
-// Matmul Kernel Gets Fast", "Beyond tiling"; "Writing a Fast Matmul in
+// The pages name tensor cores as the way past the FP32 FMA pipe ("CUDA
+// Matrix Multiplication Optimization: From Naive to Near-cuBLAS", "Beyond
+// Tiling: Async, Tensor Cores, and Scheduling"; "Writing a Fast Matmul in
 // CUDA", "What cuBLAS and CUTLASS add") but compute nothing with them; the
 // FP32 result here comes from the split, not from the pages.  This path is
 // reported on its own, never as the FFMA figure.

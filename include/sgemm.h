@@ -184,9 +184,11 @@ sgemm_status_t sgemm_plan_autotune(int64_t M, int64_t N, int64_t K, int64_t lda,
  *   - Otherwise the scalar-load kernel runs, the batch on its third grid
  *     dimension.
  *
- * The pages do not batch; this is the BLAS-style strided batch. Many small
- * products, one per attention head for instance, are the motivating case in
- * "How a Matmul Kernel Gets Fast", "What this means for real workloads".
+ * The pages do not batch; this is the BLAS-style strided batch. Many
+ * products of one shape, two per attention head (Q K^T, then the scores
+ * times V), are the motivating case in "CUDA Matrix Multiplication
+ * Optimization: From Naive to Near-cuBLAS", "What This Means for Deep
+ * Learning".
  */
 sgemm_status_t sgemm_plan_batched(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                                   int64_t batch, int64_t stride_a, int64_t stride_b, int64_t stride_c, int config_id,
@@ -259,9 +261,9 @@ sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64
  *
  * The pages neither batch nor transpose; this combines the BLAS SGEMM
  * conventions of sgemm_plan_ex with the strided batch of sgemm_plan_batched.
- * Attention (one product per head, S = Q K^T then O = P V) is the motivating
- * case in "How a Matmul Kernel Gets Fast", "What this means for real
- * workloads".
+ * Attention (two products per head, S = Q K^T then O = P V) is the
+ * motivating case in "CUDA Matrix Multiplication Optimization: From Naive
+ * to Near-cuBLAS", "What This Means for Deep Learning".
  */
 sgemm_status_t sgemm_plan_ex_batched(int order, int transa, int transb, int64_t M, int64_t N, int64_t K,
                                      int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t stride_a,
