@@ -53,6 +53,7 @@ KERNEL_SOURCES = {
     "cpa_": ["cpa_kernel.cuh", "cpa_variants.cu", "tile_order.cuh", "ptx.cuh", "kernels.h"],
     "tf32x3": ["tc_tf32x3.cu", "ptx.cuh", "kernels.h"],
     "generic": ["kernel_generic.cu", "kernels.h"],
+    "gemv": ["kernel_gemv.cu", "kernel_gemv.h", "kernels.h"],
 }
 
 

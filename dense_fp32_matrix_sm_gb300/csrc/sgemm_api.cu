@@ -17,6 +17,7 @@
 #include <vector>
 
 #include "api_internal.h"
+#include "kernel_gemv.h"
 #include "kernels.h"
 #include "sgemm.h"
 
@@ -106,6 +107,8 @@ struct Registry {
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
     v = tc_variants(&n);
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
+    v = gemv_variants(&n);
+    for (int i = 0; i < n; ++i) all.push_back(&v[i]);
   }
 };
 
@@ -161,11 +164,19 @@ sgemm_status_t check_dims(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
   return SGEMM_OK;
 }
 
+// Products the M <= 4 kernels take: one to four rows (any alignment, any
+// leading dimension or batch stride), K in at most 65535 chunks of 1024, and
+// column indexes with room to spare in 32 bits.
+bool gemv_shape(int64_t M, int64_t N, int64_t K, int64_t batch) {
+  return M <= 4 && N <= (int64_t(1) << 30) && K <= int64_t(65535) * 1024 && batch <= 65535;
+}
+
 // a_span / b_span: elements one stored A / B spans (-1: M*lda / K*ldb, an
 // operand stored as the kernels read it)
 bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                       int64_t batch = 1, int64_t stride_a = 0, int64_t stride_b = 0, int64_t a_span = -1,
                       int64_t b_span = -1) {
+  if (v->kind == kKindGemv) return gemv_shape(M, N, K, batch);
   if (batch > 1) {
     if (!v->batched) return false;
     if (v->kind == kKindGeneric) return batch <= 65535;
@@ -223,6 +234,8 @@ const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_
 // names.  The entries come from the measured sweeps on GB300.
 const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms, int64_t batch = 1,
                          int64_t stride_a = 0, int64_t stride_b = 0, int64_t a_span = -1, int64_t b_span = -1) {
+  // one to four rows: B streamed once by plain loads, any layout
+  if (gemv_shape(M, N, K, batch)) return "gemv_4x512";
   if (batch > 1) {
     // Strided batches run on the batched variants only: the transposed-A
     // family when TMA can take the layout (tile counts over the whole batch),
@@ -285,7 +298,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       // rows (one cudaMemcpy2DAsync), so the table's TMA kernels can read it:
       // measured at 4096^3, lda = 4097 ran 54.6 TFLOP/s on the cp.async kernel
       // and ldb = 4097 29.8 on the scalar-load kernel, against 68.8 aligned.
-      if (batch <= 1 && K > 0 && static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= 16777216.0) {
+      if (batch <= 1 && K > 0 && !gemv_shape(M, N, K, batch) && static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= 16777216.0) {
         rp_a = lda % 4 != 0;
         rp_b = ldb % 4 != 0;
         if (rp_a) lda = (K + 3) / 4 * 4;
@@ -399,6 +412,19 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
               cudaSuccess ||
           cudaMemset(p->flags, 0, static_cast<size_t>(grid) * sizeof(unsigned int)) != cudaSuccess)
         return fail(SGEMM_ERR_CUDA);
+    }
+  } else if (v->kind == kKindGemv) {
+    // The kernels cut K into chunks that fill whole waves of resident CTAs
+    // (more chunks when there are few column blocks); the workspace holds
+    // the partial sums of the larger count of the two forms (B as stored,
+    // B given transposed).  One chunk needs none.
+    const int64_t slots = static_cast<int64_t>(sms) * ctas;
+    grid = slots;
+    p->split = std::max(gemv_chunks(N, K, batch, 0, slots), gemv_chunks(N, K, batch, 1, slots));
+    if (p->split > 1 && M > 0 && N > 0 && K > 0) {
+      const size_t ws_bytes =
+          static_cast<size_t>(std::max<int64_t>(batch, 1)) * p->split * M * ((N + 3) / 4 * 4) * sizeof(float);
+      if (cudaMalloc(reinterpret_cast<void**>(&p->ws), ws_bytes) != cudaSuccess) return fail(SGEMM_ERR_CUDA);
     }
   } else if (v->kind == kKindTc) {
     // persistent forms: one CTA per SM walks the tiles
@@ -675,7 +701,9 @@ sgemm_status_t make_plan_ex(int order, int transa, int transb, int64_t M, int64_
   bool nat_a = false, nat_b = false;
   if (batched) {
     nat_a = ta && lda2 % 4 == 0 && (forced >= 0 ? reg.all[forced]->a_trans_ok != 0 : M2 > 16);
-    nat_b = tb && ldb2 % 4 == 0 && (forced >= 0 ? reg.all[forced]->b_trans_ok != 0 : M2 <= 16);
+    // (the M <= 4 kernels read B^T with plain loads: any row stride)
+    const bool any_ldb = forced >= 0 ? reg.all[forced]->kind == kKindGemv : gemv_shape(M2, N2, K, batch);
+    nat_b = tb && (ldb2 % 4 == 0 || any_ldb) && (forced >= 0 ? reg.all[forced]->b_trans_ok != 0 : M2 <= 16);
   }
   sgemm_plan_t p = nullptr;
   sgemm_status_t st = SGEMM_OK;
@@ -715,7 +743,7 @@ sgemm_status_t make_plan_ex(int order, int transa, int transb, int64_t M, int64_
     p->ex_native_tb = nat_b ? 1 : 0;
   } else {
     // a few-row kernel reads B given transposed (N x K, K contiguous) by TMA itself
-    if (tb && !native && chosen->b_trans_ok && ldb2 % 4 == 0) p->ex_native_tb = 1;
+    if (tb && !native && chosen->b_trans_ok && (ldb2 % 4 == 0 || kind == kKindGemv)) p->ex_native_tb = 1;
     // the transposed-A kernels read A given transposed (K x M, M contiguous) by TMA themselves
     if (ta && !native && chosen->a_trans_ok && lda2 % 4 == 0) p->ex_native_ta = 1;
   }
@@ -916,11 +944,12 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   if (v->kind == kKindTcFused &&
       ((reinterpret_cast<uintptr_t>(A) & 15) != 0 || (reinterpret_cast<uintptr_t>(B) & 15) != 0))
     return SGEMM_ERR_UNSUPPORTED;  // TMA needs 16-byte aligned bases; the scalar kernel cannot read every layout
-  if (p->ex_native_tb && ((reinterpret_cast<uintptr_t>(B) & 15) != 0 || (reinterpret_cast<uintptr_t>(A) & 15) != 0))
+  if (p->ex_native_tb && v->kind != kKindGemv &&
+      ((reinterpret_cast<uintptr_t>(B) & 15) != 0 || (reinterpret_cast<uintptr_t>(A) & 15) != 0))
     return SGEMM_ERR_UNSUPPORTED;  // B given transposed is read by TMA; the scalar kernel cannot take it
   if (p->ex_native_ta && ((reinterpret_cast<uintptr_t>(A) & 15) != 0 || (reinterpret_cast<uintptr_t>(B) & 15) != 0))
     return SGEMM_ERR_UNSUPPORTED;  // A given transposed is read by TMA; the scalar kernel cannot take it
-  if (v->kind != kKindGeneric && v->kind != kKindTc && v->kind != kKindTcFused &&
+  if (v->kind != kKindGeneric && v->kind != kKindTc && v->kind != kKindTcFused && v->kind != kKindGemv &&
       ((a_needs_16 && (reinterpret_cast<uintptr_t>(A) & 15) != 0) || (reinterpret_cast<uintptr_t>(B) & 15) != 0)) {
     v = reg.all[p->generic_id];
     grid = 0;
@@ -940,13 +969,17 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   a.alpha = alpha;
   a.beta = beta;
   a.grid = grid;
-  a.split_k = v->kind == kKindSkinny ? p->split : 1;
+  a.split_k = v->kind == kKindSkinny || v->kind == kKindGemv ? p->split : 1;
   a.batch = static_cast<int>(p->batch);
   a.b_trans = p->ex_native_tb;
   a.a_trans = p->ex_native_ta;
   a.stride_a = p->stride_a;
   a.stride_b = p->stride_b;
   a.stride_c = p->stride_c;
+  if (v->kind == kKindGemv) {
+    a.ws = p->ws;
+    if (p->ex_native_tb) a.ldb = p->ex_ldb;  // read as stored (N x K)
+  }
   if (v == reg.all[p->config_id] && p->sk_iters > 0) {
     a.dp_waves = p->dp_waves;
     a.sk_iters = p->sk_iters;
@@ -1109,7 +1142,7 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
            "variant=%s kind=%s tile=%dx%dx%d stages=%d ffma2=%d threads=%d smem=%d grid=%d ctas_per_sm=%d "
            "tiles=%lld sms=%d split=%d streamk=%d dp_waves=%d sk_tiles=%lld k_order=%s M=%lld N=%lld K=%lld "
            "order=%s op=%c%c batch=%lld repack=%d",
-           v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : v->kind == kKindTc ? "tc" : v->kind == kKindTcFused ? "tcf" : "skinny", v->bm, v->bn,
+           v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : v->kind == kKindTc ? "tc" : v->kind == kKindTcFused ? "tcf" : v->kind == kKindGemv ? "gemv" : "skinny", v->bm, v->bn,
            v->bk, v->stages, v->ffma2, v->threads, v->smem_bytes, plan->grid, plan->ctas_per_sm,
            static_cast<long long>(plan->tiles), plan->num_sms, plan->split, plan->sk_iters > 0 ? 1 : 0, plan->dp_waves,
            static_cast<long long>(plan->sk_iters > 0 ? plan->tiles - static_cast<int64_t>(plan->dp_waves) * plan->grid : 0),
@@ -1130,6 +1163,10 @@ sgemm_status_t sgemm_plan_launches(sgemm_plan_t plan, int* out) {
   // the split-TF32 variants launch two operand-split kernels before the GEMM
   const Variant* v = registry().all[plan->config_id];
   *out = (plan->M == 0 || plan->N == 0 || plan->batch == 0) ? 0 : v->kind == kKindTc && plan->K > 0 ? 3 : 1;
+  // the M <= 4 kernels add their chunks' partial sums in a second kernel
+  if (*out > 0 && v->kind == kKindGemv && plan->K > 0 &&
+      gemv_chunks(plan->N, plan->K, plan->batch, plan->ex_native_tb, plan->grid) > 1)
+    *out = 2;
   if (*out > 0 && plan->K > 0)
     *out += (plan->ex_wa ? 1 : 0) + (plan->ex_wb ? 1 : 0) + (plan->rp_a ? 1 : 0) + (plan->rp_b ? 1 : 0);
   return SGEMM_OK;

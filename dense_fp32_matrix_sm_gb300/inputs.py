@@ -68,6 +68,8 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("mlp", 8192, 14336, 4096, ("normal", 1.0), ("normal", 0.02), None, 3, 1.0, 0.0),
         Workload("decode16", 16, 16384, 8192, ("normal", 1.0), ("normal", 0.02), ("uniform", 1.0), 4,
                  1.0, 1.0),
+        Workload("decode1", 1, 16384, 8192, ("normal", 1.0), ("normal", 0.02), ("uniform", 1.0), 5,
+                 1.0, 1.0),
     )
 }
 

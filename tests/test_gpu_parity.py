@@ -100,10 +100,12 @@ def assert_parity(C, Cref, S, K, what=""):
 
 
 def _variants(sg, M=None):
-    """Variant names, without the few-row kernels when M is above their limit."""
+    """Variant names, without the few-row kernels when M is above their limits."""
     names = sg.config_names()
     if M is not None and M > 16:
         names = [n for n in names if not n.startswith("skinny")]
+    if M is not None and M > 4:
+        names = [n for n in names if not n.startswith("gemv")]
     return names
 
 
@@ -179,7 +181,7 @@ def test_skinny_variants(sg, oracle_mod, shape):
                     break  # this few-row variant does not take this shape
                 raise
             info = run_gpu.last_info
-            assert name is not None or used.startswith("skinny"), used
+            assert name is not None or used.startswith("gemv" if M <= 4 else "skinny"), used
             Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
             assert_parity(C, Cref, S, K, f"{used} {shape} split={info['split']} a={alpha} b={beta}")
             # a fixed reduction order: the same inputs give the same bits again
@@ -667,7 +669,7 @@ def test_strided_batch(sg, oracle_mod, case):
     info = plan.info()
     assert info["batch"] == batch
     if config is None and M <= 16:
-        assert info["variant"].startswith("skinny_sk"), info
+        assert info["variant"].startswith("gemv" if M <= 4 else "skinny_sk"), info
     plan.run(alpha, dA, dB, beta, dC)
     torch.cuda.synchronize()
     assert sg.device_status() == sg.SGEMM_OK
@@ -687,7 +689,9 @@ def test_strided_batch(sg, oracle_mod, case):
 @pytest.mark.parametrize("case", [
     # (M, N, K, batch, shared A?): more than 16 rows (the transposed-A kernels read
     # A given transposed), few rows (the few-row kernel reads B given transposed)
-    (300, 260, 96, 3, False), (16, 520, 264, 4, False), (7, 300, 100, 3, True), (200, 136, 64, 2, True)])
+    (300, 260, 96, 3, False), (16, 520, 264, 4, False), (7, 300, 100, 3, True), (200, 136, 64, 2, True),
+    # one to four rows (K in two chunks, partial sums added by a second kernel)
+    (2, 300, 1100, 3, False)])
 def test_batched_order_and_transpose(sg, oracle_mod, order, ta, tb, case):
     """sgemm_plan_ex_batched: every order x transpose combination of a strided
     batch, against the oracle product by product."""
@@ -817,6 +821,64 @@ def test_few_row_transposed_b_is_read_natively(sg, oracle_mod):
     Cref, S = oracle_mod.sgemm_ref(x, Wt, C0, 1.0, 1.0)
     assert_parity(dC.cpu().numpy(), Cref, S, K, "few-row NT")
     plan.close()
+
+
+# ---- one to four rows: the matrix-vector kernels -----------------------------
+
+GEMV_CASES = [(1, 1, 1), (1, 511, 1000), (2, 513, 1023), (3, 4097, 1025), (4, 1000, 3000), (1, 77, 5000),
+              (4, 8, 64), (1, 3, 70000), (2, 16384, 8192)]
+
+
+@pytest.mark.parametrize("shape", GEMV_CASES)
+@pytest.mark.parametrize("layout", ["nn", "nn_odd", "nt", "nt_odd"])
+def test_gemv_rows(sg, oracle_mod, shape, layout):
+    """M <= 4 through the table: B as stored (K x N) or given transposed
+    (N x K), 16-byte and 4-byte loads (odd row strides, B one float off a
+    16-byte boundary), one or several K chunks; bit-identical on a rerun; C
+    with NaN ignored at beta = 0; the padding of C untouched."""
+    M, N, K = shape
+    tb = layout.startswith("nt")
+    odd = layout.endswith("odd")
+    A, B, C0 = make_inputs(M, N, K, seed=M * 5 + N + K + len(layout), dist_a=("normal", 1.0),
+                           dist_b=("normal", 0.05))
+    stored_b = np.ascontiguousarray(B.T) if tb else B
+    lda = K + (3 if odd else 0)
+    ldb = stored_b.shape[1] + (1 if odd else 0)
+    ldc = N + 5
+    dA, pA, _ = _to_dev(A, lda, 1 if odd else 0)
+    dB, pB, _ = _to_dev(stored_b, ldb, 1 if odd else 0)
+    for alpha, beta in ((1.0, 0.0), (-0.5, 2.0)):
+        dC, pC, _ = _to_dev(np.full((M, N), np.nan, np.float32) if beta == 0.0 else C0, ldc, 0, fill=7.0)
+        plan = sg.Plan(M, N, K, lda, ldb, ldc, transb=tb)
+        info = plan.info()
+        assert info["variant"] == "gemv_4x512" and info["op"] == ("NT" if tb else "NN"), info
+        assert plan.launches in (1, 2) and (info["split"] > 1 or plan.launches == 1), (plan.launches, info)
+        outs = []
+        for _ in range(2):
+            if beta != 0.0:
+                dC.copy_(_to_dev(C0, ldc, 0, fill=7.0)[0])
+            plan.run(alpha, pA, pB, beta, pC)
+            torch.cuda.synchronize()
+            assert sg.device_status() == sg.SGEMM_OK
+            outs.append(dC.cpu().numpy().copy())
+        plan.close()
+        assert np.array_equal(outs[0], outs[1], equal_nan=True), "not reproducible"
+        host = outs[0]
+        C = np.stack([host[m * ldc: m * ldc + N] for m in range(M)])
+        for m in range(M):
+            assert np.all(host[m * ldc + N: (m + 1) * ldc if m + 1 < M else host.size] == 7.0), "padding written"
+        Cref, S = oracle_mod.sgemm_ref(A, B, C0 if beta != 0.0 else None, alpha, beta)
+        assert_parity(C, Cref, S, K, f"gemv {layout} {shape} split={info['split']} a={alpha} b={beta}")
+        if not tb and alpha == 1.0 and beta == 0.0 and info["k_order"] == "sequential":
+            ii, jj = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+            chain = oracle_mod.fp32_chain_entries(A, B, ii.ravel(), jj.ravel()).reshape(M, N)
+            assert np.array_equal(C, chain), f"{shape}: not the ascending-k fp32 chain"
+
+
+def test_gemv_refuses_more_than_four_rows(sg):
+    with pytest.raises(sg.SgemmError) as e:
+        sg.Plan(5, 256, 256, config="gemv_4x512")
+    assert e.value.status == sg.SGEMM_ERR_UNSUPPORTED
 
 
 def test_ffma_probe(sg):
