@@ -57,7 +57,8 @@
  * tile clears that tile's flag, so every run leaves the flags at zero.
  * A plan whose description says streamk=1 owns a device workspace (one
  * partial tile and one flag per CTA of its grid), allocated by sgemm_plan
- * and freed by sgemm_plan_destroy; two runs of such a plan must not overlap
+ * and freed by sgemm_plan_destroy; so does an M <= 4 plan (kind=gemv) with
+ * split > 1 (its partial sums).  Two runs of such a plan must not overlap
  * in time (same stream, or streams ordered by events), since both would
  * write the same workspace.  Every other plan may run on several streams
  * at once.
@@ -100,6 +101,15 @@ typedef enum {
  * whole grid (stream-K; describe reports streamk=1).
  * That workspace makes the sum order along K for the tail tiles a fixed
  * split: results stay bit-identical from run to run.
+ * For M <= 4 the table picks the matrix-vector kernels (kind=gemv): B is
+ * streamed once, K is cut into chunks that fill whole waves of the GPU,
+ * and with more than one chunk (split > 1) the plan owns a workspace of
+ * batch x split x M x N floats (N rounded up to 4) whose partial sums a
+ * second kernel adds in an order fixed by the shape (bit-identical runs).
+ * These kernels take any alignment and leading dimension, so such plans are
+ * never repacked ("Writing a Fast Matmul in CUDA", "Why decode doesn't
+ * care": a matrix-vector product uses each weight once and is bound by
+ * memory bandwidth).
  * From M*N*K >= 2^24 on, an operand whose leading dimension is not a
  * multiple of 4 (rows that are not 16-byte multiples, which TMA cannot
  * read) gets a plan-owned copy with padded rows (cudaMalloc, M x K or
@@ -176,7 +186,9 @@ sgemm_status_t sgemm_plan_autotune(int64_t M, int64_t N, int64_t K, int64_t lda,
  *
  * How it runs:
  *   - Every product of the batch runs in one launch.
- *   - Transposed-A kernels, and for M <= 16 the stream-K few-row kernel:
+ *   - For M <= 4 the matrix-vector kernels, the batch on their third grid
+ *     dimension; they take any strides.
+ *   - Transposed-A kernels, and for 4 < M <= 16 the stream-K few-row kernel:
  *     3-D tensor maps, batch outermost. They need stride_a and stride_b to
  *     be multiples of 4 that either do not overlap the matrices or are 0
  *     (one operand shared by every product); their grid and stream-K split
@@ -226,9 +238,11 @@ enum { SGEMM_NO_TRANS = 0, SGEMM_TRANS = 1 };
  *     as stored, when its leading dimension is a multiple of 4.
  *   - The split-TF32 variant reads either layout directly. So does the
  *     few-row stream-K kernel for B given transposed (stored N x K, the
- *     usual weight layout of decode) when ldb is a multiple of 4.
+ *     usual weight layout of decode) when ldb is a multiple of 4, and the
+ *     M <= 4 kernels for any ldb.
  *   - A plan that reads a transposed operand natively needs A and B 16-byte
- *     aligned at run time, else SGEMM_ERR_UNSUPPORTED.
+ *     aligned at run time, else SGEMM_ERR_UNSUPPORTED (the M <= 4 kernels
+ *     excepted: they take any alignment).
  * Runs of a plan with such a buffer must not overlap in time.
  *
  * The pages cover the row-major, untransposed product only; the other
@@ -253,11 +267,11 @@ sgemm_status_t sgemm_plan_ex(int order, int transa, int transb, int64_t M, int64
  * (column-major swaps the operands and their strides).  A transposed
  * operand is read as stored where a kernel can (the product's A by the
  * transposed-A kernels when the product has more than 16 rows, the
- * product's B by the few-row kernel otherwise; leading dimension a multiple
- * of 4); otherwise every product's operand is transposed first into a plan
- * buffer (batch times the operand; one for a shared operand).  The
- * split-TF32 variants do not run batches.  Runs of a plan must not overlap
- * in time.
+ * product's B by the few-row kernels otherwise; leading dimension a multiple
+ * of 4, or any for M <= 4); otherwise every product's operand is
+ * transposed first into a plan buffer (batch times the operand; one for a
+ * shared operand).  The split-TF32 variants do not run batches.  Runs of a
+ * plan must not overlap in time.
  *
  * The pages neither batch nor transpose; this combines the BLAS SGEMM
  * conventions of sgemm_plan_ex with the strided batch of sgemm_plan_batched.
