@@ -154,6 +154,20 @@ sgemm_status_t status_addr(int device, unsigned int** out) {
   return SGEMM_OK;
 }
 
+// Elements from the first to the last element of a stored matrix of `outer`
+// lines of `inner` elements, `ld` apart (0 when it is empty).  Computed in
+// double so that no argument overflows it.
+double span_elems(int64_t outer, int64_t inner, int64_t ld) {
+  return outer > 0 && inner > 0 ? static_cast<double>(outer - 1) * static_cast<double>(ld) + static_cast<double>(inner)
+                                : 0.0;
+}
+
+// The largest span a stored matrix (or a strided batch of them) may cover:
+// 2^40 elements, 4 TiB of floats, beyond any device memory.  Larger
+// arguments cannot describe real buffers; refusing them keeps every element
+// offset, workspace size and address computed from them far inside int64.
+constexpr double kMaxSpan = 1099511627776.0;
+
 sgemm_status_t check_dims(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc) {
   if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
   if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1)) return SGEMM_ERR_INVALID_ARG;
@@ -161,7 +175,14 @@ sgemm_status_t check_dims(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t 
   if (M > lim || N > lim || K > lim) return SGEMM_ERR_UNSUPPORTED;
   // element offsets must fit in int64 with room to spare
   if (lda > (int64_t(1) << 40) || ldb > (int64_t(1) << 40) || ldc > (int64_t(1) << 40)) return SGEMM_ERR_UNSUPPORTED;
+  if (span_elems(M, K, lda) > kMaxSpan || span_elems(K, N, ldb) > kMaxSpan || span_elems(M, N, ldc) > kMaxSpan)
+    return SGEMM_ERR_UNSUPPORTED;
   return SGEMM_OK;
+}
+
+// A strided batch of `batch` matrices of span `one`, `stride` apart.
+double batch_span(int64_t batch, int64_t stride, double one) {
+  return batch > 1 ? static_cast<double>(batch - 1) * static_cast<double>(stride) + one : one;
 }
 
 // Products the M <= 4 kernels take: one to four rows (any alignment, any
@@ -422,6 +443,8 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     grid = slots;
     p->split = std::max(gemv_chunks(N, K, batch, 0, slots), gemv_chunks(N, K, batch, 1, slots));
     if (p->split > 1 && M > 0 && N > 0 && K > 0) {
+      const double floats = static_cast<double>(std::max<int64_t>(batch, 1)) * p->split * M * ((N + 3) / 4 * 4);
+      if (floats > kMaxSpan) return fail(SGEMM_ERR_UNSUPPORTED);
       const size_t ws_bytes =
           static_cast<size_t>(std::max<int64_t>(batch, 1)) * p->split * M * ((N + 3) / 4 * 4) * sizeof(float);
       if (cudaMalloc(reinterpret_cast<void**>(&p->ws), ws_bytes) != cudaSuccess) return fail(SGEMM_ERR_CUDA);
@@ -667,6 +690,12 @@ sgemm_status_t make_plan_ex(int order, int transa, int transb, int64_t M, int64_
   if (lda < std::max<int64_t>(1, row ? a_cols : a_rows) || ldb < std::max<int64_t>(1, row ? b_cols : b_rows) ||
       ldc < std::max<int64_t>(1, row ? N : M))
     return SGEMM_ERR_INVALID_ARG;
+  // the stored matrices (one product, or the whole strided batch)
+  const int64_t nb = batch > 1 ? batch : 1;
+  if (batch_span(nb, stride_a, row ? span_elems(a_rows, a_cols, lda) : span_elems(a_cols, a_rows, lda)) > kMaxSpan ||
+      batch_span(nb, stride_b, row ? span_elems(b_rows, b_cols, ldb) : span_elems(b_cols, b_rows, ldb)) > kMaxSpan ||
+      batch_span(nb, stride_c, row ? span_elems(M, N, ldc) : span_elems(N, M, ldc)) > kMaxSpan)
+    return SGEMM_ERR_UNSUPPORTED;
   // Column-major C = op(A) op(B) is the row-major C^T = op(B)^T op(A)^T over
   // the same memory: swap the operands, their transpose flags and strides.
   const int swap = row ? 0 : 1;
@@ -856,8 +885,12 @@ sgemm_status_t sgemm_plan_batched(int64_t M, int64_t N, int64_t K, int64_t lda, 
                                   sgemm_plan_t* out) {
   if (!out) return SGEMM_ERR_INVALID_ARG;
   if (batch < 0 || stride_a < 0 || stride_b < 0 || stride_c < 0) return SGEMM_ERR_INVALID_ARG;
+  if (batch_span(batch, stride_a, span_elems(M, K, lda)) > kMaxSpan ||
+      batch_span(batch, stride_b, span_elems(K, N, ldb)) > kMaxSpan ||
+      batch_span(batch, stride_c, span_elems(M, N, ldc)) > kMaxSpan)
+    return SGEMM_ERR_UNSUPPORTED;
   // the products' C matrices must not overlap (A and B may be shared: stride 0)
-  if (batch > 1 && M > 0 && N > 0 && stride_c < (M - 1) * ldc + N) return SGEMM_ERR_INVALID_ARG;
+  if (batch > 1 && static_cast<double>(stride_c) < span_elems(M, N, ldc)) return SGEMM_ERR_INVALID_ARG;
   if (batch > 65535) return SGEMM_ERR_UNSUPPORTED;
   if (config_id < -1) return SGEMM_ERR_INVALID_ARG;
   return make_plan(M, N, K, lda, ldb, ldc, config_id, out, batch, stride_a, stride_b, stride_c);
@@ -875,7 +908,9 @@ sgemm_status_t sgemm_plan_ex_batched(int order, int transa, int transb, int64_t 
   if (batch < 0 || stride_a < 0 || stride_b < 0 || stride_c < 0 || config_id < -1) return SGEMM_ERR_INVALID_ARG;
   // the products' C matrices must not overlap (A and B may be shared: stride 0)
   const bool row = order == SGEMM_ROW_MAJOR;
-  if (batch > 1 && M > 0 && N > 0 && stride_c < (row ? (M - 1) * ldc + N : (N - 1) * ldc + M))
+  if (batch_span(batch, stride_c, row ? span_elems(M, N, ldc) : span_elems(N, M, ldc)) > kMaxSpan)
+    return SGEMM_ERR_UNSUPPORTED;
+  if (batch > 1 && static_cast<double>(stride_c) < (row ? span_elems(M, N, ldc) : span_elems(N, M, ldc)))
     return SGEMM_ERR_INVALID_ARG;
   if (batch > 65535) return SGEMM_ERR_UNSUPPORTED;
   return make_plan_ex(order, transa, transb, M, N, K, lda, ldb, ldc, config_id, out, batch, stride_a, stride_b,

@@ -101,6 +101,27 @@ def test_plan_ex_rejects_before_cuda(lib):
     assert not h.value
 
 
+def test_spans_beyond_any_memory_are_refused_before_cuda(lib):
+    """A stored matrix, or a strided batch of them, spanning more than 2^40
+    elements (4 TiB of floats) cannot describe a real buffer: every plan
+    entry refuses it with SGEMM_ERR_UNSUPPORTED before any CUDA call."""
+    h = ctypes.c_void_p()
+    big = 2 ** 20
+    # row-major A, B, C in turn spanning (rows - 1) * ld + cols = 2^40 + 2^20
+    assert lib.sgemm_plan(big + 1, 4, big, big, 4, 4, ctypes.byref(h)) == -2
+    assert lib.sgemm_plan(4, big, big + 1, big + 1, big, big, ctypes.byref(h)) == -2
+    assert lib.sgemm_plan(big + 1, big, 4, 4, big, big, ctypes.byref(h)) == -2
+    # a strided batch: A 2^41 floats apart
+    assert lib.sgemm_plan_batched(64, 64, 64, 64, 64, 64, 2, 2 ** 41, 4096, 4096, -1, ctypes.byref(h)) == -2
+    # column-major A given transposed: M columns of K, lda apart
+    assert lib.sgemm_plan_ex(1, 1, 0, big + 1, 4, big, big, big, big + 1, -1, ctypes.byref(h)) == -2
+    # a strided batch of row-major C matrices 2^41 floats apart
+    assert lib.sgemm_plan_ex_batched(0, 0, 0, 64, 32, 16, 16, 32, 32, 2, 0, 0, 2 ** 41, -1, ctypes.byref(h)) == -2
+    assert not h.value
+    dummy = 4096  # never dereferenced
+    assert lib.sgemm_run_static_scratch(big + 1, 8, big, big, 8, 8, 1.0, dummy, dummy, 0.0, dummy, None) == -2
+
+
 def test_autotune_rejects_bad_arguments_before_cuda(lib):
     h = ctypes.c_void_p()
     f = lib.sgemm_plan_autotune
