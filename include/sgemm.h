@@ -33,8 +33,10 @@
  *
  * Conventions (BLAS readings where the pages are silent):
  *   - lda >= max(1, K), ldb >= max(1, N), ldc >= max(1, N), else
- *     SGEMM_ERR_INVALID_ARG.  Dimensions above 2^31 - 1 give
- *     SGEMM_ERR_UNSUPPORTED.
+ *     SGEMM_ERR_INVALID_ARG.  Dimensions above 2^31 - 1, leading
+ *     dimensions above 2^40, and a stored matrix (or strided batch of them)
+ *     spanning more than 2^40 elements from its first to its last element
+ *     give SGEMM_ERR_UNSUPPORTED: no device holds such a buffer.
  *   - M == 0 or N == 0: nothing is launched, SGEMM_OK.
  *   - K == 0 or alpha == 0: C = beta * C; A and B are not read.
  *   - beta == 0: C is not read (NaN or garbage in C does not propagate).
