@@ -19,12 +19,23 @@ TF32 off (context), the SM clock sampled with nvidia-smi during the timed
 steps, the FFMA-peak fraction at that clock, and the CPU oracle timed on a
 bounded sample on this host's cores.
 
+"sustained": the headline workload run back to back for seconds, three
+rounds, each reported as the median of its last three quarters with its SM
+clock samples binned by MHz ("Writing a Fast Matmul in CUDA, Step by Step",
+Step 1: warm up, time launches for seconds, keep the median, sample the
+clock).  "workloads": every other workload (128^3, 4092^3 with alpha 0.5
+and beta 3, the MLP shape, the 16- and 1-row decode shapes) through the
+table's plan, each with its kernel time, roofline, ncu traffic, plan,
+cuBLAS on the same inputs and the CPU oracle (in full, or the MLP shape's
+first 1024 rows, extrapolated).
+
 --impl reference times the fp64 CPU oracle (the reference arm) on the same
 workload, one bounded row-band per step.
 """
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -78,7 +89,7 @@ def host_cores() -> int:
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
 
-    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
@@ -116,19 +127,29 @@ class ClockSampler:
         if self._t:
             self._t.join(timeout=2)
 
-    def summary(self, min_load_mhz: float = 0.0):
-        rows = []
-        for ln in self.lines:
+    def rows(self):
+        """Parsed samples: host wall-clock time t (seconds), SM and max MHz, power, reasons."""
+        out = []
+        for ln in list(self.lines):
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) != len(self.FIELDS):
                 continue
             try:
-                rows.append({"sm": float(parts[0]), "max": float(parts[1]),
-                             "power": float(parts[2]) if parts[2] not in ("[N/A]", "N/A") else None,
-                             "active": parts[3], "hw": parts[4], "hwt": parts[5], "swt": parts[6],
-                             "swp": parts[7]})
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                out.append({"t": t, "sm": float(parts[1]), "max": float(parts[2]),
+                            "power": float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
+                            "active": parts[4], "hw": parts[5], "hwt": parts[6], "swt": parts[7],
+                            "swp": parts[8]})
             except ValueError:
                 continue
+        return out
+
+    def summary(self, window=None):
+        """Median SM clock and throttle reasons over every sample, or over the
+        samples inside window = (t0, t1) (host wall-clock seconds)."""
+        rows = self.rows()
+        if window is not None:
+            rows = [r for r in rows if window[0] <= r["t"] <= window[1]]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
         reasons = set()
@@ -139,9 +160,12 @@ class ClockSampler:
                     reasons.add(name)
         sm = [r["sm"] for r in rows]
         powers = [r["power"] for r in rows if r["power"] is not None]
+        bins = {}
+        for v in sm:
+            bins[str(int(v))] = bins.get(str(int(v)), 0) + 1
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r["max"] for r in rows),
                 "sm_mhz_min": min(sm), "power_w_max": max(powers) if powers else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "samples": len(rows), "sm_mhz_bins": bins}
 
 
 def gpu_id_for(torch, dev: int) -> str:
@@ -190,6 +214,10 @@ def parse():
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the library kernel (no e2e, cuBLAS or CPU legs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="size of the CPU-baseline sample")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the record of the other workloads (kernel time, roofline, cuBLAS, CPU oracle)")
+    ap.add_argument("--sustained-seconds", type=float, default=2.0,
+                    help="length of each round of the back-to-back leg (0: skip it)")
     return ap.parse_args()
 
 
@@ -277,6 +305,183 @@ def time_steps(torch, fn, steps: int, flush, stream):
         evs.append((s, e))
     torch.cuda.synchronize()
     return [s.elapsed_time(e) for s, e in evs]
+
+
+def traffic_for(variant, workload: str):
+    """DRAM bytes per launch of `variant` on `workload` from profiles/traffic.json,
+    or None when there is no capture or the kernel's sources changed since."""
+    if not variant or not os.path.exists(TRAFFIC_FILE):
+        return None
+    try:
+        rec = json.load(open(TRAFFIC_FILE)).get(f"{variant}|{workload}")
+    except (ValueError, OSError):
+        return None
+    if rec and rec.get("kernel_source_sha") == kernel_source_hash(str(variant)):
+        return rec.get("dram_bytes_per_launch")
+    return None
+
+
+def roofline_for(w, ms: float, sms: int, sm_mhz: float, peaks: dict, traffic):
+    """The roofline of one workload's step time `ms`.  The bound follows the
+    arithmetic intensity: below the ridge (FFMA peak at sm_mhz over the
+    measured HBM copy bandwidth) the kernel is bound by HBM, above it by the
+    FP32 FFMA pipe (SMs x 128 lanes x 2 FLOP x clock)."""
+    peak_tflops = sms * FMA_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    hbm_gbs = peaks.get("hbm_gbs") or FALLBACK_HBM_GBS
+    hbm_basis = ("MEASURED_PEAKS.json hbm_gbs, STREAM-style copy, burst (of measured)" if peaks.get("hbm_gbs")
+                 else "fallback 6.8 TB/s (of fallback)")
+    intensity = w.flops / w.algorithmic_bytes()
+    ridge = peak_tflops * 1e12 / (hbm_gbs * 1e9)
+    if intensity < ridge:
+        achieved_gbs = w.algorithmic_bytes() / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm_gbs, 4), "traffic": traffic, "peak_basis": hbm_basis,
+                "algorithmic_bytes": w.algorithmic_bytes(),
+                "intensity_flop_per_byte": round(intensity, 2), "ridge_flop_per_byte": round(ridge, 2)}
+    achieved_tflops = w.flops / (ms * 1e-3) / 1e12
+    return {"bound": "alu", "achieved": round(achieved_tflops, 3), "peak": round(peak_tflops, 3),
+            "unit": "TFLOP/s", "frac": round(achieved_tflops / peak_tflops, 4), "traffic": traffic,
+            "peak_basis": "SMs x 128 FP32 lanes x 2 FLOP x median SM clock sampled during the timed steps "
+                          "(FFMA pipe; not a tensor-core path)",
+            "algorithmic_bytes": w.algorithmic_bytes(),
+            "intensity_flop_per_byte": round(intensity, 2), "ridge_flop_per_byte": round(ridge, 2)}
+
+
+def median_last_three_quarters(times):
+    """Median of the last three quarters of a run of step times (the first
+    quarter is the warming part of a back-to-back run)."""
+    n = len(times)
+    return statistics.median(times[n // 4:] if n >= 4 else times)
+
+
+def cublas_step_fn(torch, w, dA, dB, dC0, out):
+    """torch.matmul / addmm in FP32 with TF32 off: cuBLAS SGEMM, context only."""
+    torch.backends.cuda.matmul.allow_tf32 = False
+    torch.backends.cudnn.allow_tf32 = False
+    if w.beta == 0.0:
+        return lambda: torch.matmul(dA, dB, out=out)
+    return lambda: torch.addmm(dC0, dA, dB, beta=w.beta, alpha=w.alpha, out=out)
+
+
+# The pages' own sizes for the oracle on the host cores: the 128^3, 4092^3
+# and few-row problems in full; the MLP shape (962 GFLOP) on its first 1024
+# rows, scaled to the whole product.
+CPU_ROWS = {"mlp": 1024}
+
+
+def workloads_leg(torch, sg, names, stream, flush, warmup, steps, sms, peaks, sampler, cpu: bool, threads: int,
+                  min_seconds: float = 0.5):
+    """Every other workload through the table's plan, timed like the headline
+    (L2 flushed before each step, CUDA events on the launching stream), with
+    its roofline, its ncu traffic, its plan, cuBLAS on the same inputs and the
+    oracle on the host cores.  Returns (records, kernel launches)."""
+    from dense_fp32_matrix_sm_gb300.inputs import WORKLOADS, workload_inputs
+
+    recs = {}
+    launches = 0
+    for name in names:
+        w = WORKLOADS[name]
+        A, B, C0 = workload_inputs(w)
+        dA = torch.from_numpy(A).cuda()
+        dB = torch.from_numpy(B).cuda()
+        dC0 = torch.from_numpy(C0).cuda()
+        dC = dC0.clone()
+        plan = sg.Plan(w.M, w.N, w.K)
+        info = plan.info()
+
+        def step():
+            plan.run(w.alpha, dA, dB, w.beta, dC, stream)
+
+        for _ in range(warmup):
+            flush()
+            step()
+        torch.cuda.synchronize()
+        # at least `steps` steps and at least min_seconds of them, so that the
+        # 100 ms clock samples cover every workload's timed region
+        t0 = time.time()
+        times = []
+        while len(times) < steps or time.time() - t0 < min_seconds:
+            times += time_steps(torch, step, steps, flush, stream)
+        t1 = time.time()
+        if sg.device_status() != sg.SGEMM_OK:
+            raise SystemExit(f"kernel status word set during the {name} steps (a wait timed out)")
+        launches += plan.launches * (len(times) + warmup)
+        ms = statistics.fmean(times)
+        clk = sampler.summary(window=(t0 - 0.05, t1 + 0.05)) if sampler else {}
+        mhz = clk.get("sm_mhz") or peaks.get("sm_max_mhz") or 2070.0
+        rec = {"workload": f"{w.name}: {w.describe()}", "ms_per_step": round(ms, 5),
+               "ms_median": round(statistics.median(times), 5), "ms_min": round(min(times), 5),
+               "steps": len(times), "timed_seconds": round(t1 - t0, 2),
+               "gflops": round(w.flops / (ms * 1e-3) / 1e9, 1),
+               "roofline": roofline_for(w, ms, sms, mhz, peaks, traffic_for(info.get("variant"), w.name)),
+               "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+               "plan": plan.describe(), "gpu_launches_per_step": plan.launches}
+        plan.close()
+        # cuBLAS on the same inputs (context)
+        out = torch.empty_like(dC)
+        cb = cublas_step_fn(torch, w, dA, dB, dC0, out)
+        for _ in range(warmup):
+            cb()
+        cb_ms = statistics.fmean(time_steps(torch, cb, steps, flush, stream))
+        rec["cublas_context"] = {"gflops": round(w.flops / (cb_ms * 1e-3) / 1e9, 1), "ms": round(cb_ms, 5),
+                                 "call": "torch.matmul/addmm fp32, allow_tf32=False"}
+        del dA, dB, dC0, dC, out
+        torch.cuda.empty_cache()
+        if cpu:
+            import oracle
+
+            rows = min(w.M, CPU_ROWS.get(name, w.M))
+            t = time_oracle_rows(A, B, C0, w, rows, threads)
+            rec["cpu_baseline"] = {
+                "value": round(2.0 * rows * w.N * w.K / t / 1e9, 3), "unit": "GFLOP/s", "cores": threads,
+                "kind": "oracle",
+                "sample": (f"all {w.M} rows, fp64 with the |A||B| bound, {t:.2f} s" if rows == w.M else
+                           f"rows 0..{rows - 1} of {w.M} (all {w.N} columns, K={w.K}), fp64 with the |A||B| "
+                           f"bound, {t:.2f} s; extrapolated to the whole product: "
+                           f"{t * w.M / rows:.1f} s")}
+        recs[name] = rec
+    return recs, launches
+
+
+def sustained_leg(torch, step, flush, stream, w, seconds: float, rounds: int, sms, sampler):
+    """The pages' timing protocol on the headline workload: back-to-back steps
+    for `seconds` (L2 flushed before each, per-step CUDA events), the median of
+    the last three quarters, `rounds` times; the SM clock samples of each
+    round binned by MHz, so the rate can be read against the clock."""
+    out = []
+    for _ in range(rounds):
+        evs = []
+        t0 = time.time()
+        while time.time() - t0 < seconds:
+            for _ in range(50):
+                flush()
+                s = torch.cuda.Event(enable_timing=True)
+                e = torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                step()
+                e.record(stream)
+                evs.append((s, e))
+            evs[-1][1].synchronize()
+        torch.cuda.synchronize()
+        t1 = time.time()
+        times = [s.elapsed_time(e) for s, e in evs]
+        med = median_last_three_quarters(times)
+        clk = sampler.summary(window=(t0, t1)) if sampler else {}
+        mhz = clk.get("sm_mhz")
+        rec = {"steps": len(times), "seconds": round(t1 - t0, 2), "ms_median_last_3q": round(med, 5),
+               "gflops": round(w.flops / (med * 1e-3) / 1e9, 1),
+               "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_mhz_min", "reasons", "samples", "sm_mhz_bins",
+                                                  "power_w_max")}}
+        if mhz:
+            rec["pct_ffma_peak_at_round_clock"] = round(
+                100.0 * w.flops / (med * 1e-3) / (sms * FMA_LANES_PER_SM * 2 * mhz * 1e6), 2)
+        out.append(rec)
+    meds = [r["ms_median_last_3q"] for r in out]
+    return {"rounds": out, "ms_median_of_rounds": round(statistics.median(meds), 5),
+            "spread_pct": round(100.0 * (max(meds) - min(meds)) / statistics.median(meds), 2),
+            "gflops": round(w.flops / (statistics.median(meds) * 1e-3) / 1e9, 1),
+            "protocol": f"{rounds} rounds of >= {seconds:g} s of back-to-back steps, L2 flushed before each, "
+                        "per-step CUDA events, median of the last three quarters of each round"}
 
 
 TC_VARIANT = "tf32x3p_128x128x32_s3"
@@ -411,35 +616,7 @@ def run_ours(args):
         "gpu_launches": launches_per_step * steps,
     }
 
-    traffic = None
-    if os.path.exists(TRAFFIC_FILE):
-        try:
-            rec = json.load(open(TRAFFIC_FILE)).get(f"{info.get('variant')}|{w.name}")
-            if rec and rec.get("kernel_source_sha") == kernel_source_hash(str(info.get("variant"))):
-                traffic = rec.get("dram_bytes_per_launch")
-        except (ValueError, OSError):
-            traffic = None
-    # The bound follows the workload's arithmetic intensity: below the ridge
-    # (FFMA peak / measured HBM copy bandwidth) the kernel is bound by HBM.
-    hbm_gbs = peaks.get("hbm_gbs") or FALLBACK_HBM_GBS
-    hbm_basis = ("MEASURED_PEAKS.json hbm_gbs, STREAM-style copy, burst (of measured)" if peaks.get("hbm_gbs")
-                 else "fallback 6.8 TB/s (of fallback)")
-    intensity = w.flops / w.algorithmic_bytes()
-    ridge = peak_tflops * 1e12 / (hbm_gbs * 1e9)
-    if intensity < ridge:
-        achieved_gbs = w.algorithmic_bytes() / (ms * 1e-3) / 1e9
-        out["roofline"] = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
-                           "frac": round(achieved_gbs / hbm_gbs, 4), "traffic": traffic, "peak_basis": hbm_basis,
-                           "algorithmic_bytes": w.algorithmic_bytes(),
-                           "intensity_flop_per_byte": round(intensity, 2), "ridge_flop_per_byte": round(ridge, 2)}
-    else:
-        out["roofline"] = {"bound": "alu", "achieved": round(achieved_tflops, 3),
-                           "peak": round(peak_tflops, 3), "unit": "TFLOP/s",
-                           "frac": round(achieved_tflops / peak_tflops, 4), "traffic": traffic,
-                           "peak_basis": "SMs x 128 FP32 lanes x 2 FLOP x median SM clock sampled during the "
-                                         "timed steps (FFMA pipe; not a tensor-core path)",
-                           "algorithmic_bytes": w.algorithmic_bytes(),
-                           "intensity_flop_per_byte": round(intensity, 2), "ridge_flop_per_byte": round(ridge, 2)}
+    out["roofline"] = roofline_for(w, ms, sms, sm_mhz or sm_max, peaks, traffic_for(info.get("variant"), w.name))
     out["clocks"] = {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "sm_mhz_min",
                                                  "power_w_max", "samples")}
 
@@ -456,6 +633,15 @@ def run_ours(args):
     if out["roofline"]["bound"] == "alu":
         out["roofline"]["frac_of_ffma2_probe"] = round(achieved_tflops / p2_tflops, 4)
     out["gpu_launches"] += 4
+
+    if args.sustained_seconds > 0 and rank == 0 and sampler is not None:
+        sampler2 = ClockSampler(gpu_id_for(torch, dev))
+        sampler2.start()
+        out["sustained"] = sustained_leg(torch, step, flush, stream, w, args.sustained_seconds, 3, sms, sampler2)
+        sampler2.stop()
+        out["gpu_launches"] += launches_per_step * sum(r["steps"] for r in out["sustained"]["rounds"])
+        if sg.device_status() != sg.SGEMM_OK:
+            raise SystemExit("kernel status word set during the sustained steps")
 
     if not args.kernel_only:
         # End to end from pinned host memory, every step copying its inputs in
@@ -508,16 +694,8 @@ def run_ours(args):
         out["gpu_launches"] += launches_per_step * e2e_steps
 
         # cuBLAS SGEMM as context (TF32 off: plain FP32 results)
-        torch.backends.cuda.matmul.allow_tf32 = False
-        torch.backends.cudnn.allow_tf32 = False
-        tA, tB = dA, dB
         tC = torch.empty_like(dC)
-        if w.beta == 0.0:
-            def cublas_step():
-                torch.matmul(tA, tB, out=tC)
-        else:
-            def cublas_step():
-                torch.addmm(dC0, tA, tB, beta=w.beta, alpha=w.alpha, out=tC)
+        cublas_step = cublas_step_fn(torch, w, dA, dB, dC0, tC)
         for _ in range(warmup):
             cublas_step()
         cb = time_steps(torch, cublas_step, min(steps, 100), flush, stream)
@@ -530,6 +708,22 @@ def run_ours(args):
         # its own: never the FFMA figure above.
         if TC_VARIANT in sg.config_names() and w.K >= 16:
             out["tf32x3"] = tc_leg(torch, sg, w, dA, dB, dC0, stream, flush, warmup, min(steps, 100), dist, peaks)
+
+        if not args.no_workloads and rank == 0:
+            from dense_fp32_matrix_sm_gb300.inputs import WORKLOADS
+
+            names = [n for n in WORKLOADS if n != w.name]
+            if world == 1:
+                import oracle
+
+                oracle.build()
+            sampler3 = ClockSampler(gpu_id_for(torch, dev))
+            sampler3.start()
+            recs, n_launch = workloads_leg(torch, sg, names, stream, flush, warmup, max(20, min(steps, 50)), sms,
+                                           peaks, sampler3, world == 1, host_cores())
+            sampler3.stop()
+            out["workloads"] = recs
+            out["gpu_launches"] += n_launch
 
         if rank == 0 and world == 1:
             import oracle

@@ -17,12 +17,14 @@ from ._lib import (  # noqa: F401
     Plan,
     SgemmError,
     autotune,
+    clear_plan_cache,
     config_id,
     config_name,
     config_names,
     device_status,
     lib,
     num_configs,
+    plan_cache_size,
     probe_ffma,
     run_static_scratch,
     selftest_wait_timeout,

@@ -285,11 +285,57 @@ def _ld(t) -> int:
     return max(1, t.stride(0), t.shape[1]) if t.shape[0] > 1 else max(1, t.shape[1])
 
 
+# Plans made by sgemm(), kept for reuse: (device, M, N, K, lda, ldb, ldc,
+# config, stream handle) -> Plan, least recently used first.  A plan's
+# stream-K workspace must not be shared by runs that overlap in time, so a
+# plan serves one stream only: runs on one stream are ordered.
+_PLAN_CACHE_MAX = 64
+_plan_cache = {}
+_plan_cache_lock = threading.Lock()
+
+
+def _cached_plan(key, make):
+    with _plan_cache_lock:
+        plan = _plan_cache.pop(key, None)
+        if plan is None:
+            plan = make()
+        _plan_cache[key] = plan  # most recently used last
+        evicted = []
+        while len(_plan_cache) > _PLAN_CACHE_MAX:
+            evicted.append(_plan_cache.pop(next(iter(_plan_cache))))
+    for p in evicted:
+        p.close()
+    return plan
+
+
+def clear_plan_cache() -> None:
+    """Destroy every plan sgemm() keeps (frees their device workspaces; the
+    frees synchronise the device)."""
+    with _plan_cache_lock:
+        plans = list(_plan_cache.values())
+        _plan_cache.clear()
+    for p in plans:
+        p.close()
+
+
+def plan_cache_size() -> int:
+    with _plan_cache_lock:
+        return len(_plan_cache)
+
+
 def sgemm(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, stream=None, config=None):
     """C = alpha*A*B + beta*C for row-major float32 CUDA tensors; returns C.
 
     C is allocated (and beta must be 0) when not given.  Runs on the current
-    stream unless `stream` is given; does not synchronise.
+    stream unless `stream` is given.
+
+    Plans are cached per (device, shape, leading dimensions, config, stream):
+    the first call for a key makes a plan, which may allocate its device
+    workspace (cudaMalloc); later calls reuse it and allocate nothing of the
+    library's, so they only enqueue work and do not synchronise.  At most 64
+    plans are kept; the least recently used one is destroyed beyond that,
+    and destroying a plan with a workspace frees it (cudaFree synchronises
+    the device).  clear_plan_cache() drops them all.
     """
     import torch
 
@@ -306,11 +352,12 @@ def sgemm(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, stream=None, conf
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     if C.dtype != torch.float32 or not C.is_cuda or tuple(C.shape) != (M, N):
         raise TypeError("C must be an M x N float32 CUDA tensor")
-    plan = Plan(M, N, K, _ld(A) if K > 0 else 1, _ld(B), _ld(C), config=config)
-    try:
+    lda, ldb, ldc = _ld(A) if K > 0 else 1, _ld(B), _ld(C)
+    key = (A.device.index if A.device.index is not None else torch.cuda.current_device(), M, N, K, lda, ldb, ldc,
+           config, _stream_handle(stream))
+    with torch.cuda.device(A.device):
+        plan = _cached_plan(key, lambda: Plan(M, N, K, lda, ldb, ldc, config=config))
         plan.run(alpha, A, B, beta, C, stream)
-    finally:
-        plan.close()
     return C
 
 

@@ -24,5 +24,10 @@ sgemm_status_t api_encode_maps(const Variant* v, int64_t M, int64_t N, int64_t K
                                const float* A, const float* B, LaunchArgs* a);
 // The current limit for in-kernel waits.
 uint64_t api_wait_timeout_ns();
+// Whether C (M x N, ldc) shares its address span with A (M x K, lda) or
+// B (K x N, ldb), all row-major and untransposed: the conservative span
+// test sgemm_run applies before it launches.
+bool api_c_overlaps_operands(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                             const float* A, const float* B, const float* C);
 
 }  // namespace sgemm

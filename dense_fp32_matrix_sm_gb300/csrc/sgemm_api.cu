@@ -1302,4 +1302,20 @@ sgemm_status_t api_encode_maps(const Variant* v, int64_t M, int64_t N, int64_t K
 
 uint64_t api_wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 
+bool api_c_overlaps_operands(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                             const float* A, const float* B, const float* C) {
+  sgemm_plan_s shape;  // only the shape fields spans_overlap reads
+  shape.M = M;
+  shape.N = N;
+  shape.K = K;
+  shape.ldc = ldc;
+  shape.ex_lda = lda;
+  shape.ex_ldb = ldb;
+  shape.ex_swap = 0;
+  shape.ex_ta = shape.ex_tb = 0;
+  shape.batch = 1;
+  shape.ex_stride_a = shape.ex_stride_b = shape.stride_c = 0;
+  return spans_overlap(&shape, C, A, true) || spans_overlap(&shape, C, B, false);
+}
+
 }  // namespace sgemm

@@ -8,6 +8,7 @@
 // uses, handed this array instead of a plan's cudaMalloc'd workspace.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
@@ -111,6 +112,9 @@ extern "C" sgemm_status_t sgemm_run_static_scratch(int64_t M, int64_t N, int64_t
   if (lda % 4 != 0 || ldb % 4 != 0 || (reinterpret_cast<uintptr_t>(A) & 15) != 0 ||
       (reinterpret_cast<uintptr_t>(B) & 15) != 0)
     return SGEMM_ERR_UNSUPPORTED;
+  // C may not share its address span with A or B: the kernel reads A and B
+  // by TMA while other CTAs write C (the same span test as sgemm_run)
+  if (api_c_overlaps_operands(M, N, K, lda, ldb, ldc, A, B, C)) return SGEMM_ERR_UNSUPPORTED;
 
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess) return SGEMM_ERR_CUDA;
@@ -147,7 +151,9 @@ extern "C" sgemm_status_t sgemm_run_static_scratch(int64_t M, int64_t N, int64_t
   int64_t grid = tiles < slots ? tiles : slots;
   const bool tail = tiles > slots && tiles % slots != 0;
   const bool small = tiles < slots && tiles * KT >= slots;
-  if ((tail || small) && KT >= 8) {
+  // SGEMM_NO_STREAMK turns the split off here as it does for plans, so the
+  // results stay bit-identical to a plan of the same variant
+  if ((tail || small) && KT >= 8 && getenv("SGEMM_NO_STREAMK") == nullptr) {
     if (slots > SGEMM_STATIC_SCRATCH_MAX_CTAS) return SGEMM_ERR_UNSUPPORTED;  // more partial tiles than the array holds
     grid = slots;
     a.dp_waves = static_cast<int>(tiles / slots);

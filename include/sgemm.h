@@ -409,7 +409,9 @@ sgemm_status_t sgemm_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
  * sgemm_run's arguments, with the same meaning, layout and ownership; A, B,
  * C are device pointers on the current device.  Enqueues on `stream` and
  * returns.  Results are bit-identical to sgemm_run of a plan made with the
- * variant "tmat_128x256x32_s3_b1" (k_order=split when the tail is split).
+ * variant "tmat_128x256x32_s3_b1" (k_order=split when the tail is split);
+ * like plans, it honours the SGEMM_NO_STREAMK environment variable, which
+ * turns the split off.
  *
  * Scratch: the stream-K workspace and its flags sit in one file-scope
  * __device__ array of SGEMM_STATIC_SCRATCH_BYTES (see above).  Only the
@@ -438,6 +440,9 @@ sgemm_status_t sgemm_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
  *   - SGEMM_ERR_UNSUPPORTED when this kernel cannot take the layout: lda or
  *     ldb not a multiple of 4, or A or B not 16-byte aligned.  These need
  *     sgemm_plan and sgemm_run.
+ *   - SGEMM_ERR_UNSUPPORTED when C shares its address span with A or B
+ *     (the conservative span test of sgemm_run): the kernel reads A and B
+ *     while other CTAs write C.  A and B may alias each other.
  *   - SGEMM_ERR_UNSUPPORTED also when the call would need more scratch than
  *     the array holds: a stream-K grid of more than
  *     SGEMM_STATIC_SCRATCH_MAX_CTAS CTAs, on a device with more SMs than

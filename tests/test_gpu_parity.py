@@ -12,17 +12,16 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 from dense_fp32_matrix_sm_gb300.inputs import (WORKLOADS, make_inputs, sample_rows_cols,
                                                workload_inputs)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-BOUND_ABS = 1e-6
-
-
-def _bound(K, S):
-    return 4.0 * K * 2.0 ** -24 * S + BOUND_ABS
+# The bar has one definition, oracle.acceptance_bound, pinned by a
+# hand-computed value in test_oracle_pins.py.
+_bound = oracle.acceptance_bound
 
 
 @pytest.fixture(scope="module")
@@ -960,3 +959,41 @@ def test_autotune_picks_the_fastest_and_caches_it(sg, oracle_mod):
     assert any(n.startswith("tf32x3") for n in with_tc)
     plan.close()
     again.close()
+
+
+def test_sgemm_helper_reuses_its_plan(sg, oracle_mod):
+    """sgemm() keeps its plan per (device, shape, layout, config, stream): at a
+    stream-K shape the first call allocates the plan's workspace, later calls
+    allocate no device memory, and every result is within the bound."""
+    M, N, K = 2048, 4096, 1024
+    sg.clear_plan_cache()
+    A, B, C0 = make_inputs(M, N, K, seed=77, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.from_numpy(C0).cuda()
+    assert sg.Plan(M, N, K).info()["streamk"] == 1  # the table's plan has a workspace at this shape
+    sg.sgemm(dA, dB, dC, alpha=1.0, beta=0.0)
+    torch.cuda.synchronize()
+    assert sg.plan_cache_size() == 1
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        sg.sgemm(dA, dB, dC, alpha=0.5, beta=0.0)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"device memory changed across calls: {free0} -> {free1}"
+    assert sg.plan_cache_size() == 1
+    assert sg.device_status() == sg.SGEMM_OK
+    rows, cols = sample_rows_cols(M, N, n_rows=128, n_cols=128, seed=3)
+    Cref, S = oracle_mod.sgemm_ref(np.ascontiguousarray(A[rows]), np.ascontiguousarray(B[:, cols]), None, 0.5, 0.0)
+    got = dC.cpu().numpy()[np.ix_(rows, cols)].astype(np.float64)
+    assert np.all(np.abs(got - Cref) <= _bound(K, S))
+    # another stream gets its own plan (runs on two streams may overlap)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        sg.sgemm(dA, dB, dC, alpha=1.0, beta=0.0, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert sg.plan_cache_size() == 2
+    sg.clear_plan_cache()
+    assert sg.plan_cache_size() == 0

@@ -107,6 +107,20 @@ def test_flop_count():
     assert abs(WORKLOADS["square4092"].flops - 137e9) < 0.5e9
 
 
+def test_acceptance_bound_hand_values(oracle_mod):
+    # The bar is |C - C_ref| <= 4*K*2^-24*S + 1e-6, elementwise.  Worked by
+    # hand: K = 4096, S = 100 gives 4 * 4096 * 100 / 16777216 = 1638400 /
+    # 16777216 = 0.09765625, plus 1e-6.  K = 1, S = 0 leaves the absolute
+    # term alone; K = 2^22, S = 1 gives 4 * 2^22 / 2^24 = 1, plus 1e-6.
+    assert oracle_mod.acceptance_bound(4096, 100.0) == 0.09765625 + 1e-6
+    assert oracle_mod.acceptance_bound(1, 0.0) == 1e-6
+    assert oracle_mod.acceptance_bound(2 ** 22, 1.0) == 1.0 + 1e-6
+    # elementwise over an array of S, and linear in S and in K
+    got = oracle_mod.acceptance_bound(4096, np.array([[0.0, 100.0], [200.0, 50.0]]))
+    want = np.array([[1e-6, 0.09765625 + 1e-6], [0.1953125 + 1e-6, 0.048828125 + 1e-6]])
+    assert got.shape == (2, 2) and np.array_equal(got, want)
+
+
 @pytest.mark.parametrize("shape", [(3, 4, 5), (17, 1, 9), (1, 1, 1), (8, 8, 0)])
 def test_instrumented_fma_count(oracle_mod, shape):
     M, N, K = shape
