@@ -586,23 +586,95 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
       if (__syncthreads_or(timed_out)) c_first = b;  // give up on the partials; the status word says why
     }
     // own partial, then the contributors' in CTA order; then the epilogue
-    for (int i = threadIdx.x; i < kTile4; i += S::kThreads) {
-      float4 v = part4[i];
-      for (int c = c_first; c < b; ++c) {
-        const float4 o = __ldcg(&ws4[static_cast<int64_t>(c) * kTile4 + i]);
-        v.x += o.x;
-        v.y += o.y;
-        v.z += o.z;
-        v.w += o.w;
+    if constexpr (BT || BATCHED) {
+      // one output float4 at a time: holding every output's reads at once
+      // spills registers in these forms and measured slower
+      for (int i = threadIdx.x; i < kTile4; i += S::kThreads) {
+        float4 v = part4[i];
+        for (int c = c_first; c < b; ++c) {
+          const float4 o = __ldcg(&ws4[static_cast<int64_t>(c) * kTile4 + i]);
+          v.x += o.x;
+          v.y += o.y;
+          v.z += o.z;
+          v.w += o.w;
+        }
+        const int m = (4 * i) / BN;
+        const int n = n0 + (4 * i) % BN;
+        if (m < p.M) {
+          float* crow = Cz + static_cast<int64_t>(m) * p.ldc;
+          const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (n + j < p.N) crow[n + j] = p.beta == 0.f ? p.alpha * vv[j] : fmaf(p.alpha, vv[j], p.beta * crow[n + j]);
+          }
+        }
       }
+      __syncthreads();  // the next piece rewrites `partial`
+      if (threadIdx.x == 0)
+        for (int c = c_first; c < b; ++c) *reinterpret_cast<volatile unsigned int*>(p.flags + c) = 0u;
+      continue;
+    }
+    // Every global read (a contributor's partials, then C) is issued for all
+    // of this thread's outputs before any is used or C is written, so the
+    // fixup costs one round trip per contributor and one for C (measured at
+    // 16 x 16384 x 8192, beta 1: 0.1071 ms against 0.1092).
+    constexpr int kIt = kTile4 / S::kThreads;
+    static_assert(kTile4 % S::kThreads == 0, "whole float4s per thread");
+    float4 v[kIt];
+#pragma unroll
+    for (int t = 0; t < kIt; ++t) v[t] = part4[threadIdx.x + t * S::kThreads];
+    for (int c = c_first; c < b; ++c) {
+      float4 o[kIt];
+#pragma unroll
+      for (int t = 0; t < kIt; ++t) o[t] = __ldcg(&ws4[static_cast<int64_t>(c) * kTile4 + threadIdx.x + t * S::kThreads]);
+#pragma unroll
+      for (int t = 0; t < kIt; ++t) {
+        v[t].x += o[t].x;
+        v[t].y += o[t].y;
+        v[t].z += o[t].z;
+        v[t].w += o[t].w;
+      }
+    }
+    const bool vec_c = (reinterpret_cast<uintptr_t>(Cz) & 15) == 0 && (p.ldc & 3) == 0;
+    float4 old[kIt];
+    if (p.beta != 0.f) {
+#pragma unroll
+      for (int t = 0; t < kIt; ++t) {
+        const int i = threadIdx.x + t * S::kThreads;
+        const int m = (4 * i) / BN;
+        const int n = n0 + (4 * i) % BN;
+        old[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m < p.M) {
+          const float* crow = Cz + static_cast<int64_t>(m) * p.ldc + n;
+          if (vec_c && n + 3 < p.N) {
+            old[t] = *reinterpret_cast<const float4*>(crow);
+          } else {
+            if (n < p.N) old[t].x = crow[0];
+            if (n + 1 < p.N) old[t].y = crow[1];
+            if (n + 2 < p.N) old[t].z = crow[2];
+            if (n + 3 < p.N) old[t].w = crow[3];
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kIt; ++t) {
+      const int i = threadIdx.x + t * S::kThreads;
       const int m = (4 * i) / BN;
       const int n = n0 + (4 * i) % BN;
       if (m < p.M) {
-        float* crow = Cz + static_cast<int64_t>(m) * p.ldc;
-        const float vv[4] = {v.x, v.y, v.z, v.w};
+        float* crow = Cz + static_cast<int64_t>(m) * p.ldc + n;
+        const float vv[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+        const float oo[4] = {old[t].x, old[t].y, old[t].z, old[t].w};
+        float r[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (n + j < p.N) crow[n + j] = p.beta == 0.f ? p.alpha * vv[j] : fmaf(p.alpha, vv[j], p.beta * crow[n + j]);
+        for (int j = 0; j < 4; ++j) r[j] = p.beta == 0.f ? p.alpha * vv[j] : fmaf(p.alpha, vv[j], p.beta * oo[j]);
+        if (vec_c && n + 3 < p.N) {
+          *reinterpret_cast<float4*>(crow) = make_float4(r[0], r[1], r[2], r[3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (n + j < p.N) crow[j] = r[j];
         }
       }
     }

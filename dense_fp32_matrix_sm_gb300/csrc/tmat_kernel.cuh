@@ -479,37 +479,79 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
     }
 
     // ---------------- epilogue ----------------
+    if (p.beta == 0.f) {  // C is not read
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 4; ++i) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int row = tm * BM + wm * 64 + 16 * i + 2 * g + e;
-        if (row >= p.M) continue;
-        float* crow = Cz + static_cast<int64_t>(row) * p.ldc;
+        for (int e = 0; e < 2; ++e) {
+          const int row = tm * BM + wm * 64 + 16 * i + 2 * g + e;
+          if (row >= p.M) continue;
+          float* crow = Cz + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int col = tn * BN + wn * 32 + 4 * c + 16 * h;
-          float v[4];
+          for (int h = 0; h < 2; ++h) {
+            const int col = tn * BN + wn * 32 + 4 * c + 16 * h;
+            float v[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) v[q] = e ? acc[i][4 * h + q].y : acc[i][4 * h + q].x;
-          if (p.vec_c && col + 3 < p.N) {
-            float4* dst = reinterpret_cast<float4*>(crow + col);
-            float4 o;
-            if (p.beta == 0.f) {
-              o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
+            for (int q = 0; q < 4; ++q) v[q] = e ? acc[i][4 * h + q].y : acc[i][4 * h + q].x;
+            if (p.vec_c && col + 3 < p.N) {
+              *reinterpret_cast<float4*>(crow + col) =
+                  make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
             } else {
-              const float4 old = *dst;
-              o = make_float4(fmaf(p.alpha, v[0], p.beta * old.x), fmaf(p.alpha, v[1], p.beta * old.y),
-                              fmaf(p.alpha, v[2], p.beta * old.z), fmaf(p.alpha, v[3], p.beta * old.w));
-            }
-            *dst = o;
-          } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (col + q < p.N) {
-                float* d = crow + col + q;
-                *d = p.beta == 0.f ? p.alpha * v[q] : fmaf(p.alpha, v[q], p.beta * *d);
-              }
+              for (int q = 0; q < 4; ++q)
+                if (col + q < p.N) crow[col + q] = p.alpha * v[q];
+            }
+          }
+        }
+      }
+    } else {
+      // The four C reads of a row pair (i) are all issued before any of its
+      // writes: the compiler cannot move a read of C above a write to
+      // another row of C, so in the plain order each read waited out the
+      // previous write's round trip.
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float4 old[2][2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int row = tm * BM + wm * 64 + 16 * i + 2 * g + e;
+          const float* crow = Cz + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = tn * BN + wn * 32 + 4 * c + 16 * h;
+            old[e][h] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row >= p.M) continue;
+            if (p.vec_c && col + 3 < p.N) {
+              old[e][h] = *reinterpret_cast<const float4*>(crow + col);
+            } else {
+              if (col < p.N) old[e][h].x = crow[col];
+              if (col + 1 < p.N) old[e][h].y = crow[col + 1];
+              if (col + 2 < p.N) old[e][h].z = crow[col + 2];
+              if (col + 3 < p.N) old[e][h].w = crow[col + 3];
+            }
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int row = tm * BM + wm * 64 + 16 * i + 2 * g + e;
+          if (row >= p.M) continue;
+          float* crow = Cz + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = tn * BN + wn * 32 + 4 * c + 16 * h;
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = e ? acc[i][4 * h + q].y : acc[i][4 * h + q].x;
+            const float oo[4] = {old[e][h].x, old[e][h].y, old[e][h].z, old[e][h].w};
+            float r[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) r[q] = fmaf(p.alpha, v[q], p.beta * oo[q]);
+            if (p.vec_c && col + 3 < p.N) {
+              *reinterpret_cast<float4*>(crow + col) = make_float4(r[0], r[1], r[2], r[3]);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (col + q < p.N) crow[col + q] = r[q];
             }
           }
         }
