@@ -24,6 +24,17 @@ sgemm_status_t api_encode_maps(const Variant* v, int64_t M, int64_t N, int64_t K
                                const float* A, const float* B, LaunchArgs* a);
 // The current limit for in-kernel waits.
 uint64_t api_wait_timeout_ns();
+// The persistent grid of a transposed-A plan over `tiles` C tiles of KT
+// k-slices, SMs x CTAs per SM resident: full waves data-parallel and, when
+// stream-K is allowed, the last partial wave split along K (dp_waves full
+// waves, then sk_iters k-slices shared by the grid).  Pure host arithmetic.
+struct StreamKSchedule {
+  int64_t grid;
+  int dp_waves;
+  int64_t sk_iters;
+};
+StreamKSchedule api_streamk_schedule(int64_t tiles, int64_t KT, int sms, int ctas_per_sm, bool allowed);
+
 // Whether C (M x N, ldc) shares its address span with A (M x K, lda) or
 // B (K x N, ldb), all row-major and untransposed: the conservative span
 // test sgemm_run applies before it launches.

@@ -15,6 +15,8 @@ enum VariantKind : int {
   kKindCpa = 3,      // A by cp.async (transposed, any alignment), B by TMA (16-byte aligned rows)
   kKindTc = 4,       // tensor cores, operands split into two TF32 parts (any alignment; plan workspace)
   kKindTcFused = 5,  // tensor cores, the split inside the GEMM kernel (A and B read by TMA as stored)
+  // 6 is kKindGemv, the M <= 4 kernels (kernel_gemv.h)
+  kKindTiny = 7,     // small C tiles, whole K-panels in shared memory (any alignment; K <= bk)
 };
 
 // Everything one launch needs.  Tensor maps are encoded by the caller per
@@ -85,6 +87,7 @@ const Variant* skinny_variants(int* count);
 const Variant* cpa_variants(int* count);
 const Variant* tmat_variants(int* count);
 const Variant* tc_variants(int* count);
+const Variant* tiny_variants(int* count);
 
 // C = beta * C (K == 0 or alpha == 0), any leading dimension; `batch`
 // matrices stride_c apart.

@@ -9,6 +9,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <map>
 #include <tuple>
@@ -22,6 +23,10 @@
 #include "sgemm.h"
 
 using namespace sgemm;
+
+static_assert(kKindGemv != kKindGeneric && kKindGemv != kKindTma && kKindGemv != kKindSkinny &&
+                  kKindGemv != kKindCpa && kKindGemv != kKindTc && kKindGemv != kKindTcFused && kKindGemv != kKindTiny,
+              "every variant kind is distinct");
 
 struct sgemm_plan_s {
   int64_t M, N, K, lda, ldb, ldc;
@@ -109,6 +114,8 @@ struct Registry {
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
     v = gemv_variants(&n);
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
+    v = tiny_variants(&n);
+    for (int i = 0; i < n; ++i) all.push_back(&v[i]);
   }
 };
 
@@ -192,12 +199,27 @@ bool gemv_shape(int64_t M, int64_t N, int64_t K, int64_t batch) {
   return M <= 4 && N <= (int64_t(1) << 30) && K <= int64_t(65535) * 1024 && batch <= 65535;
 }
 
+// Products the tiny kernel takes from the table: more than 16 rows (fewer
+// go to the few-row kernels, which do not fill 32-row tiles with padding),
+// K <= 512 and at most two of its 32 x 32 tiles per SM (over the whole
+// batch).  Measured against the
+// 128-row kernels and cuBLAS (TFLOP/s, L2 flushed): 128^3 0.52 (cuBLAS
+// 0.42), 256^3 3.4 (2.5), 384^3 11.0 (6.9), 512 x 512 x 128 6.7 (6.0),
+// 200 x 130 x 100 with odd ldb 0.63 (0.56); at 512^3 it ties the split
+// 128 x 64 tiles (14.6 against 14.4).
+bool tiny_shape(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms) {
+  return M > 16 && K <= 512 &&
+         std::max<int64_t>(batch, 1) * ((M + 31) / 32) * ((N + 31) / 32) <= 2 * static_cast<int64_t>(num_sms);
+}
+
 // a_span / b_span: elements one stored A / B spans (-1: M*lda / K*ldb, an
 // operand stored as the kernels read it)
 bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                       int64_t batch = 1, int64_t stride_a = 0, int64_t stride_b = 0, int64_t a_span = -1,
                       int64_t b_span = -1) {
   if (v->kind == kKindGemv) return gemv_shape(M, N, K, batch);
+  // whole K-panels in shared memory; tiles on grid x (columns) and y (rows)
+  if (v->kind == kKindTiny) return K <= v->bk && batch <= 65535 && (M + v->bm - 1) / v->bm <= 65535;
   if (batch > 1) {
     if (!v->batched) return false;
     if (v->kind == kKindGeneric) return batch <= 65535;
@@ -243,8 +265,16 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
 const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms) {
   const int64_t wide_tiles = batch * ((M + 127) / 128) * ((N + 255) / 256);
   const int64_t square_tiles = batch * ((M + 127) / 128) * ((N + 127) / 128);
+  const int64_t narrow_tiles = batch * ((M + 127) / 128) * ((N + 63) / 64);
   const int64_t KT = (K + 31) / 32;
   if (N > 128 && wide_tiles >= num_sms && K >= 256) return "tmat_128x256x32_s3_b1";
+  // few tiles and a short k loop: 128 x 64 tiles split into three or more
+  // pieces along K each (api_streamk_schedule) beat 128 x 128 tiles, whose
+  // finishers add twice the bytes per contributor (512^3: 14.2 TFLOP/s
+  // against 12.7; 640^3: 22.9 against 21.0; 256 x 256 x 2048: 10.7 against
+  // 8.6); with a long k loop the larger tile wins (512 x 512 x 8192: 49.0
+  // against 38.7)
+  if (KT >= 2 && KT <= 64 && 3 * narrow_tiles <= num_sms) return "tmat_128x64x32_s3_b2";
   if (N > 64 && (2 * square_tiles >= static_cast<int64_t>(num_sms) ||
                  (KT >= 8 && square_tiles * KT >= static_cast<int64_t>(num_sms))))
     return "tmat_128x128x32_s4_b1";
@@ -257,6 +287,8 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
                          int64_t stride_a = 0, int64_t stride_b = 0, int64_t a_span = -1, int64_t b_span = -1) {
   // one to four rows: B streamed once by plain loads, any layout
   if (gemv_shape(M, N, K, batch)) return "gemv_4x512";
+  // tiny products: whole K-panels in shared memory, any layout
+  if (tiny_shape(M, N, K, batch, num_sms)) return "tiny_32x32";
   if (batch > 1) {
     // Strided batches run on the batched variants only: the transposed-A
     // family when TMA can take the layout (tile counts over the whole batch),
@@ -285,10 +317,6 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
                                                                        : "skinny_16x128x32_w4_s3_b3_ef_pa";
   }
   if (lda % 4 != 0) return "cpa_128x128x32_s3_k8_b2";  // A copied 4 bytes at a time: any lda
-  // tiny products: the k-contiguous kernel, unless the K loop is long enough to
-  // split every 128 x 128 tile over the grid (256 x 256 x 2048: 6.8 TFLOP/s vs 2.4)
-  if (M * N <= 256 * 256 && ((M + 127) / 128) * ((N + 127) / 128) * ((K + 31) / 32) < num_sms)
-    return "tma_128x64x32_w64x32_s3_quad_b3";
   return tmat_choice(M, N, K, 1, num_sms);
 }
 
@@ -319,7 +347,8 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       // rows (one cudaMemcpy2DAsync), so the table's TMA kernels can read it:
       // measured at 4096^3, lda = 4097 ran 54.6 TFLOP/s on the cp.async kernel
       // and ldb = 4097 29.8 on the scalar-load kernel, against 68.8 aligned.
-      if (batch <= 1 && K > 0 && !gemv_shape(M, N, K, batch) && static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= 16777216.0) {
+      if (batch <= 1 && K > 0 && !gemv_shape(M, N, K, batch) && !tiny_shape(M, N, K, batch, sms) &&
+          static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= 16777216.0) {
         rp_a = lda % 4 != 0;
         rp_b = ldb % 4 != 0;
         if (rp_a) lda = (K + 3) / 4 * 4;
@@ -396,20 +425,12 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     return fail(SGEMM_ERR_CUDA);
   if (v->kind == kKindTma || v->kind == kKindCpa) {
     const int64_t slots = static_cast<int64_t>(sms) * ctas;
-    if (grid > slots) grid = slots;
-    // Stream-K tail: when the tiles do not fill the last wave, split the
-    // k-slices of the leftover tiles over every CTA of a resident grid.
-    // With fewer tiles than CTA slots every tile is a "leftover" (no
-    // data-parallel wave), as long as every CTA still gets a slice
-    // (measured: 768^3 from 20.7 to 31.5 TFLOP/s, 640^3 from 13.9 to 21.2,
-    // 512^3 from 8.6 to 11.9).
-    const int64_t KT = (K + v->bk - 1) / v->bk;
-    const bool tail = p->tiles > slots && p->tiles % slots != 0;
-    const bool small = p->tiles < slots && p->tiles * KT >= slots;
-    if (v->streamk && getenv("SGEMM_NO_STREAMK") == nullptr && (tail || small) && KT >= 8) {
-      grid = slots;
-      p->dp_waves = static_cast<int>(p->tiles / slots);
-      p->sk_iters = (p->tiles % slots) * KT;
+    const StreamKSchedule sk = api_streamk_schedule(p->tiles, (K + v->bk - 1) / v->bk, sms, ctas,
+                                                    v->streamk && getenv("SGEMM_NO_STREAMK") == nullptr);
+    grid = sk.grid;
+    if (sk.sk_iters > 0) {
+      p->dp_waves = sk.dp_waves;
+      p->sk_iters = sk.sk_iters;
       const size_t ws_bytes = static_cast<size_t>(slots) * v->bm * v->bn * sizeof(float);
       if (cudaMalloc(reinterpret_cast<void**>(&p->ws), ws_bytes) != cudaSuccess ||
           cudaMalloc(reinterpret_cast<void**>(&p->flags), static_cast<size_t>(slots) * sizeof(unsigned int)) !=
@@ -985,6 +1006,7 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   if (p->ex_native_ta && ((reinterpret_cast<uintptr_t>(A) & 15) != 0 || (reinterpret_cast<uintptr_t>(B) & 15) != 0))
     return SGEMM_ERR_UNSUPPORTED;  // A given transposed is read by TMA; the scalar kernel cannot take it
   if (v->kind != kKindGeneric && v->kind != kKindTc && v->kind != kKindTcFused && v->kind != kKindGemv &&
+      v->kind != kKindTiny &&
       ((a_needs_16 && (reinterpret_cast<uintptr_t>(A) & 15) != 0) || (reinterpret_cast<uintptr_t>(B) & 15) != 0)) {
     v = reg.all[p->generic_id];
     grid = 0;
@@ -1177,12 +1199,13 @@ sgemm_status_t sgemm_plan_describe(sgemm_plan_t plan, char* buf, size_t n) {
            "variant=%s kind=%s tile=%dx%dx%d stages=%d ffma2=%d threads=%d smem=%d grid=%d ctas_per_sm=%d "
            "tiles=%lld sms=%d split=%d streamk=%d dp_waves=%d sk_tiles=%lld k_order=%s M=%lld N=%lld K=%lld "
            "order=%s op=%c%c batch=%lld repack=%d",
-           v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : v->kind == kKindTc ? "tc" : v->kind == kKindTcFused ? "tcf" : v->kind == kKindGemv ? "gemv" : "skinny", v->bm, v->bn,
+           v->name, v->kind == kKindGeneric ? "generic" : v->kind == kKindTma ? "tma" : v->kind == kKindCpa ? "cpa" : v->kind == kKindTc ? "tc" : v->kind == kKindTcFused ? "tcf" : v->kind == kKindGemv ? "gemv" : v->kind == kKindTiny ? "tiny" : "skinny", v->bm, v->bn,
            v->bk, v->stages, v->ffma2, v->threads, v->smem_bytes, plan->grid, plan->ctas_per_sm,
            static_cast<long long>(plan->tiles), plan->num_sms, plan->split, plan->sk_iters > 0 ? 1 : 0, plan->dp_waves,
            static_cast<long long>(plan->sk_iters > 0 ? plan->tiles - static_cast<int64_t>(plan->dp_waves) * plan->grid : 0),
            (v->kind == kKindTc || v->kind == kKindTcFused) ? "tf32x3"
-           : (plan->split > 1 || v->kind == kKindSkinny || plan->sk_iters > 0) ? "split" : "sequential",
+           : (plan->split > 1 || v->kind == kKindSkinny || v->kind == kKindTiny || plan->sk_iters > 0) ? "split"
+                                                                                                     : "sequential",
            static_cast<long long>(plan->ex_swap ? plan->N : plan->M),
            static_cast<long long>(plan->ex_swap ? plan->M : plan->N), static_cast<long long>(plan->K),
            plan->ex_order == SGEMM_COL_MAJOR ? "col" : "row",
@@ -1301,6 +1324,40 @@ sgemm_status_t api_encode_maps(const Variant* v, int64_t M, int64_t N, int64_t K
 }
 
 uint64_t api_wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+
+// Stream-K schedules (measured on GB300, CUDA events, L2 flushed):
+//  * Tail: more tiles than resident CTAs and a partial last wave -- full
+//    waves run data-parallel and the leftover tiles' k-slices are split over
+//    every resident CTA (4096^3 on 128 x 256 tiles: 58.3 to 68.9 TFLOP/s).
+//  * Fewer tiles than resident CTAs: every tile is split along K into s
+//    pieces, one CTA each.  A piece's compute shrinks as KT / s, while the
+//    tile's finisher pays one round trip to L2 per contributor, s - 1 in
+//    all; the sweep's best s was about sqrt(3 KT), with an integer s and at
+//    most one CTA per SM (512^3 on 128 x 64 tiles: 14.6 TFLOP/s with 4
+//    pieces per tile on 128 CTAs, 11.9 spread over all 304 slots; 768^3 on
+//    128 x 128: 31.5 with 4 per tile on 144 CTAs, 29.4 on 152;
+//    256 x 256 x 2048: 8.4 with 16 per tile, 6.8 with 38).  When fewer than
+//    three pieces per tile fit on the SMs, the tiles' slices are shared by
+//    every resident CTA instead (1024^3 on 128 x 128: 43.8 on 152 CTAs,
+//    40.7 with 2 per tile on 128).
+StreamKSchedule api_streamk_schedule(int64_t tiles, int64_t KT, int sms, int ctas_per_sm, bool allowed) {
+  const int64_t slots = static_cast<int64_t>(sms) * ctas_per_sm;
+  StreamKSchedule s{tiles < slots ? tiles : slots, 0, 0};
+  if (!allowed || tiles <= 0) return s;
+  if (tiles > slots) {
+    if (tiles % slots != 0 && KT >= 8) s = {slots, static_cast<int>(tiles / slots), (tiles % slots) * KT};
+    return s;
+  }
+  const int64_t cap = sms / tiles;  // pieces per tile with at most one CTA per SM
+  if (cap >= 3) {
+    int64_t pieces = static_cast<int64_t>(std::sqrt(3.0 * static_cast<double>(KT)) + 0.5);
+    pieces = std::min(pieces, std::min(cap, KT));
+    if (pieces >= 2) s = {tiles * pieces, 0, tiles * KT};
+    return s;
+  }
+  if (tiles < slots && tiles * KT >= slots && KT >= 8) s = {slots, 0, tiles * KT};
+  return s;
+}
 
 bool api_c_overlaps_operands(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                              const float* A, const float* B, const float* C) {

@@ -46,7 +46,8 @@ struct DeviceState {
   float* ws = nullptr;
   unsigned int* flags = nullptr;
   unsigned int* status = nullptr;
-  int slots = 0;  // resident CTAs of the kernel: SMs x CTAs per SM
+  int sms = 0;          // SMs of the device
+  int ctas_per_sm = 0;  // resident CTAs of the kernel per SM
   std::atomic<unsigned int> epoch{0};
 };
 
@@ -82,7 +83,8 @@ sgemm_status_t setup(int device, cudaStream_t stream, DeviceState** out) {
       s.ws = reinterpret_cast<float*>(b);
       s.flags = flags;
       s.status = status;
-      s.slots = sms * ctas;
+      s.sms = sms;
+      s.ctas_per_sm = ctas;
       s.epoch.store(0, std::memory_order_relaxed);
       g_variant.store(v, std::memory_order_relaxed);
       s.ready.store(true, std::memory_order_release);
@@ -141,23 +143,20 @@ extern "C" sgemm_status_t sgemm_run_static_scratch(int64_t M, int64_t N, int64_t
   a.status = s->status;
   a.timeout_ns = api_wait_timeout_ns();
 
-  // The same schedule as a plan of this variant: full waves data-parallel;
-  // when the last wave is partial (and K has at least 8 slices), its tiles'
-  // k-slices are split over a grid of every resident CTA -- and with fewer
-  // tiles than CTA slots, every tile's, as long as every CTA gets a slice.
-  const int64_t slots = s->slots;
+  // The same schedule as a plan of this variant (api_streamk_schedule):
+  // full waves data-parallel and a partial last wave split along K; with
+  // fewer tiles than CTA slots, every tile split into pieces along K.
   const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
   const int64_t KT = (K + v->bk - 1) / v->bk;
-  int64_t grid = tiles < slots ? tiles : slots;
-  const bool tail = tiles > slots && tiles % slots != 0;
-  const bool small = tiles < slots && tiles * KT >= slots;
   // SGEMM_NO_STREAMK turns the split off here as it does for plans, so the
   // results stay bit-identical to a plan of the same variant
-  if ((tail || small) && KT >= 8 && getenv("SGEMM_NO_STREAMK") == nullptr) {
-    if (slots > SGEMM_STATIC_SCRATCH_MAX_CTAS) return SGEMM_ERR_UNSUPPORTED;  // more partial tiles than the array holds
-    grid = slots;
-    a.dp_waves = static_cast<int>(tiles / slots);
-    a.sk_iters = (tiles % slots) * KT;
+  const StreamKSchedule sk =
+      api_streamk_schedule(tiles, KT, s->sms, s->ctas_per_sm, getenv("SGEMM_NO_STREAMK") == nullptr);
+  int64_t grid = sk.grid;
+  if (sk.sk_iters > 0) {
+    if (grid > SGEMM_STATIC_SCRATCH_MAX_CTAS) return SGEMM_ERR_UNSUPPORTED;  // more partial tiles than the array holds
+    a.dp_waves = sk.dp_waves;
+    a.sk_iters = sk.sk_iters;
     a.ws = s->ws;
     a.flags = s->flags;
     unsigned int e = s->epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;

@@ -128,6 +128,7 @@ def test_shape_sweep_every_variant(sg, oracle_mod, variant_idx):
     if variant_idx >= len(names):
         pytest.skip("fewer variants in this build")
     name = names[variant_idx]
+    ran = 0
     for (M, N, K) in _shape_cases(36, seed=variant_idx):
         for alpha, beta in ((1.0, 0.0), (0.5, 3.0)):
             A, B, C0 = make_inputs(M, N, K, seed=M * 7 + N * 3 + K, dist_a=("normal", 1.0),
@@ -140,12 +141,15 @@ def test_shape_sweep_every_variant(sg, oracle_mod, variant_idx):
                 if e.status == sg.SGEMM_ERR_UNSUPPORTED:
                     break
                 raise
+            ran += 1
             Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
             assert_parity(C, Cref, S, K, f"{name} {M}x{N}x{K} a={alpha} b={beta}")
             if alpha == 1.0 and beta == 0.0 and run_gpu.last_info.get("k_order") == "sequential":
                 ii, jj = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
                 chain = oracle_mod.fp32_chain_entries(A, B, ii.ravel(), jj.ravel()).reshape(M, N)
                 assert np.array_equal(C, chain), f"{name} {M}x{N}x{K}: not the ascending-k fp32 chain"
+    # every variant takes some of the shapes: none passes by refusing them all
+    assert ran >= 4, f"{name} ran on {ran} of the sweep's shapes"
 
 
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024), (1000, 1100, 999), (300, 2000, 517)])
@@ -198,13 +202,16 @@ def test_skinny_rejects_tall_m(sg):
 # ---- layouts: leading dimensions, misaligned pointers, guard bands ------------
 
 @pytest.mark.parametrize("lds", [(0, 0, 0), (4, 8, 12), (1, 0, 0), (0, 3, 0), (0, 0, 5), (7, 9, 11)])
-def test_leading_dimensions(sg, oracle_mod, lds):
-    M, N, K = 200, 188, 148
+@pytest.mark.parametrize("shape", [(200, 188, 148), (100, 96, 1000)])
+def test_leading_dimensions(sg, oracle_mod, lds, shape):
+    M, N, K = shape
     A, B, C0 = make_inputs(M, N, K, seed=3)
     Cref, S = oracle_mod.sgemm_ref(A, B, C0, 1.5, -0.5)
     C, used = run_gpu(sg, A, B, C0, 1.5, -0.5, lda=K + lds[0], ldb=N + lds[1], ldc=N + lds[2])
     assert_parity(C, Cref, S, K, f"ld pads {lds} ({used})")
-    if lds[1] % 4:
+    if K <= 512:
+        assert used == "tiny_32x32", used      # tiny products: whole K-panels, any leading dimension
+    elif lds[1] % 4:
         assert used.startswith("generic")      # B's rows are not 16-byte multiples: scalar loads
     elif lds[0] % 4:
         assert used.startswith("cpa")          # A copied 4 bytes at a time: any lda
