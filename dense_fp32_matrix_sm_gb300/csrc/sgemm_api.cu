@@ -199,6 +199,18 @@ bool gemv_shape(int64_t M, int64_t N, int64_t K, int64_t batch) {
   return M <= 4 && N <= (int64_t(1) << 30) && K <= int64_t(65535) * 1024 && batch <= 65535;
 }
 
+// Products the table sends to the five-to-sixteen-row matrix-vector kernel
+// (gemv_16x1024): one product, B as stored, B of at least 16 MB (a stream
+// worth keeping at full bandwidth), any alignment and leading dimension.
+// Measured against the few-row stream-K kernel (L2 clean, median of 40):
+// 16 x 16384 x 8192 0.090 ms against 0.102; 8 x 16384 x 8192 0.084 against
+// 0.105; 12 x 8192 x 4096 0.037 against 0.039; 16 x 4096 x 4096 0.027
+// against 0.029.
+bool rows_shape(int64_t M, int64_t N, int64_t K, int64_t batch, int b_trans) {
+  return batch <= 1 && !b_trans && M > 4 && M <= 16 && N * K >= (int64_t(1) << 22) && N <= (int64_t(1) << 30) &&
+         K <= int64_t(65535) * 640;
+}
+
 // Products the tiny kernel takes from the table: more than 16 rows (fewer
 // go to the few-row kernels, which do not fill 32-row tiles with padding),
 // K <= 512 and at most two of its 32 x 32 tiles per SM (over the whole
@@ -217,7 +229,7 @@ bool tiny_shape(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms) {
 bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                       int64_t batch = 1, int64_t stride_a = 0, int64_t stride_b = 0, int64_t a_span = -1,
                       int64_t b_span = -1) {
-  if (v->kind == kKindGemv) return gemv_shape(M, N, K, batch);
+  if (v->kind == kKindGemv) return gemv_takes(v, M, N, K, batch);
   // whole K-panels in shared memory; tiles on grid x (columns) and y (rows)
   if (v->kind == kKindTiny) return K <= v->bk && batch <= 65535 && (M + v->bm - 1) / v->bm <= 65535;
   if (batch > 1) {
@@ -284,9 +296,13 @@ const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_
 // The per-shape config table.  Keys are shape classes; values are variant
 // names.  The entries come from the measured sweeps on GB300.
 const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int num_sms, int64_t batch = 1,
-                         int64_t stride_a = 0, int64_t stride_b = 0, int64_t a_span = -1, int64_t b_span = -1) {
+                         int64_t stride_a = 0, int64_t stride_b = 0, int64_t a_span = -1, int64_t b_span = -1,
+                         int b_trans = 0) {
   // one to four rows: B streamed once by plain loads, any layout
   if (gemv_shape(M, N, K, batch)) return "gemv_4x512";
+  // five to sixteen rows of one product, B as stored: B streamed once
+  // through per-warp cp.async rings, any layout
+  if (rows_shape(M, N, K, batch, b_trans)) return "gemv_16x1024";
   // tiny products: whole K-panels in shared memory, any layout
   if (tiny_shape(M, N, K, batch, num_sms)) return "tiny_32x32";
   if (batch > 1) {
@@ -320,9 +336,12 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   return tmat_choice(M, N, K, 1, num_sms);
 }
 
+// b_trans: the caller's B is stored transposed and a transpose buffer will
+// hold it unless the chosen kernel reads it as stored (the table then
+// prefers a kernel that does).
 sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int config_id,
                          sgemm_plan_t* out, int64_t batch = 1, int64_t stride_a = 0, int64_t stride_b = 0,
-                         int64_t stride_c = 0, int64_t a_span = -1, int64_t b_span = -1) {
+                         int64_t stride_c = 0, int64_t a_span = -1, int64_t b_span = -1, int b_trans = 0) {
   if (!out) return SGEMM_ERR_INVALID_ARG;
   sgemm_status_t st = check_dims(M, N, K, lda, ldb, ldc);
   if (st != SGEMM_OK) return st;
@@ -348,13 +367,15 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       // measured at 4096^3, lda = 4097 ran 54.6 TFLOP/s on the cp.async kernel
       // and ldb = 4097 29.8 on the scalar-load kernel, against 68.8 aligned.
       if (batch <= 1 && K > 0 && !gemv_shape(M, N, K, batch) && !tiny_shape(M, N, K, batch, sms) &&
+          !rows_shape(M, N, K, batch, b_trans) &&
           static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= 16777216.0) {
         rp_a = lda % 4 != 0;
         rp_b = ldb % 4 != 0;
         if (rp_a) lda = (K + 3) / 4 * 4;
         if (rp_b) ldb = (N + 3) / 4 * 4;
       }
-      config_id = find_variant(table_choice(M, N, K, lda, ldb, sms, batch, stride_a, stride_b, a_span, b_span));
+      config_id =
+          find_variant(table_choice(M, N, K, lda, ldb, sms, batch, stride_a, stride_b, a_span, b_span, b_trans));
       if (config_id < 0) config_id = reg.first_generic;
     }
   }
@@ -460,9 +481,10 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     // (more chunks when there are few column blocks); the workspace holds
     // the partial sums of the larger count of the two forms (B as stored,
     // B given transposed).  One chunk needs none.
-    const int64_t slots = static_cast<int64_t>(sms) * ctas;
-    grid = slots;
-    p->split = std::max(gemv_chunks(N, K, batch, 0, slots), gemv_chunks(N, K, batch, 1, slots));
+    grid = sms;
+    const int s_kn = gemv_plan_chunks(v, M, N, K, batch, 0, sms), s_nk = gemv_plan_chunks(v, M, N, K, batch, 1, sms);
+    if (s_kn < 1 || s_nk < 1) return fail(SGEMM_ERR_CUDA);
+    p->split = std::max(s_kn, s_nk);
     if (p->split > 1 && M > 0 && N > 0 && K > 0) {
       const double floats = static_cast<double>(std::max<int64_t>(batch, 1)) * p->split * M * ((N + 3) / 4 * 4);
       if (floats > kMaxSpan) return fail(SGEMM_ERR_UNSUPPORTED);
@@ -764,8 +786,8 @@ sgemm_status_t make_plan_ex(int order, int transa, int transb, int64_t M, int64_
     const int64_t a_span = nat_a ? K * lda2 : -1;
     const int64_t b_span = nat_b ? N2 * ldb2 : -1;
     st = batched ? make_plan(M2, N2, K, lda_eff, ldb_eff, ldc, config_id, &p, batch, ka_stride, kb_stride, stride_c,
-                             a_span, b_span)
-                 : make_plan(M2, N2, K, lda_eff, ldb_eff, ldc, config_id, &p);
+                             a_span, b_span, tb && !native ? 1 : 0)
+                 : make_plan(M2, N2, K, lda_eff, ldb_eff, ldc, config_id, &p, 1, 0, 0, 0, -1, -1, tb && !native ? 1 : 0);
     if (!batched || (!nat_a && !nat_b)) break;
     const Variant* got = st == SGEMM_OK ? registry().all[p->config_id] : nullptr;
     if (got && (!nat_a || got->a_trans_ok) && (!nat_b || got->b_trans_ok)) break;
@@ -1223,7 +1245,7 @@ sgemm_status_t sgemm_plan_launches(sgemm_plan_t plan, int* out) {
   *out = (plan->M == 0 || plan->N == 0 || plan->batch == 0) ? 0 : v->kind == kKindTc && plan->K > 0 ? 3 : 1;
   // the M <= 4 kernels add their chunks' partial sums in a second kernel
   if (*out > 0 && v->kind == kKindGemv && plan->K > 0 &&
-      gemv_chunks(plan->N, plan->K, plan->batch, plan->ex_native_tb, plan->grid) > 1)
+      gemv_plan_chunks(v, plan->M, plan->N, plan->K, plan->batch, plan->ex_native_tb, plan->num_sms) > 1)
     *out = 2;
   if (*out > 0 && plan->K > 0)
     *out += (plan->ex_wa ? 1 : 0) + (plan->ex_wb ? 1 : 0) + (plan->rp_a ? 1 : 0) + (plan->rp_b ? 1 : 0);

@@ -59,8 +59,8 @@
  * tile clears that tile's flag, so every run leaves the flags at zero.
  * A plan whose description says streamk=1 owns a device workspace (one
  * partial tile and one flag per CTA of its grid), allocated by sgemm_plan
- * and freed by sgemm_plan_destroy; so does an M <= 4 plan (kind=gemv) with
- * split > 1 (its partial sums).  Two runs of such a plan must not overlap
+ * and freed by sgemm_plan_destroy; so does a matrix-vector plan (kind=gemv)
+ * with split > 1 (its partial sums).  Two runs of such a plan must not overlap
  * in time (same stream, or streams ordered by events), since both would
  * write the same workspace.  Every other plan may run on several streams
  * at once.
@@ -103,11 +103,15 @@ typedef enum {
  * whole grid (stream-K; describe reports streamk=1).
  * That workspace makes the sum order along K for the tail tiles a fixed
  * split: results stay bit-identical from run to run.
- * For M <= 4 the table picks the matrix-vector kernels (kind=gemv): B is
+ * For M <= 4 the table picks the matrix-vector kernels (kind=gemv,
+ * gemv_4x512), and for one product of 5 <= M <= 16 rows with B as stored
+ * and at least 2^22 elements of B, the sixteen-row ones (gemv_16x1024,
+ * which stream B through per-warp cp.async rings in shared memory): B is
  * streamed once, K is cut into chunks that fill whole waves of the GPU,
  * and with more than one chunk (split > 1) the plan owns a workspace of
  * batch x split x M x N floats (N rounded up to 4) whose partial sums a
- * second kernel adds in an order fixed by the shape (bit-identical runs).
+ * second kernel adds in an order fixed by the shape (bit-identical runs);
+ * that kernel is launched as a programmatic dependent of the first.
  * These kernels take any alignment and leading dimension, so such plans are
  * never repacked ("Writing a Fast Matmul in CUDA", "Why decode doesn't
  * care": a matrix-vector product uses each weight once and is bound by
@@ -241,7 +245,9 @@ enum { SGEMM_NO_TRANS = 0, SGEMM_TRANS = 1 };
  *   - The split-TF32 variant reads either layout directly. So does the
  *     few-row stream-K kernel for B given transposed (stored N x K, the
  *     usual weight layout of decode) when ldb is a multiple of 4, and the
- *     M <= 4 kernels for any ldb.
+ *     M <= 4 kernels for any ldb.  (The 5-to-16-row matrix-vector kernels
+ *     read B only as stored, so with B given transposed the table keeps
+ *     the few-row stream-K kernel for those rows.)
  *   - A plan that reads a transposed operand natively needs A and B 16-byte
  *     aligned at run time, else SGEMM_ERR_UNSUPPORTED (the M <= 4 kernels
  *     excepted: they take any alignment).

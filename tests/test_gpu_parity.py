@@ -175,7 +175,7 @@ def test_skinny_variants(sg, oracle_mod, shape):
     M, N, K = shape
     A, B, C0 = make_inputs(M, N, K, seed=M + N + K, dist_a=("normal", 1.0), dist_b=("normal", 0.02))
     lda, ldb = (K + 3) // 4 * 4, (N + 3) // 4 * 4
-    for name in [n for n in sg.config_names() if n.startswith("skinny")] + [None]:
+    for name in [n for n in sg.config_names() if n.startswith("skinny")] + ["gemv_16x1024", None]:
         for alpha, beta in ((1.0, 0.0), (1.0, 1.0), (-0.75, 2.0)):
             try:
                 C, used = run_gpu(sg, A, B, C0, alpha, beta, config=name, lda=lda, ldb=ldb)
@@ -184,7 +184,11 @@ def test_skinny_variants(sg, oracle_mod, shape):
                     break  # this few-row variant does not take this shape
                 raise
             info = run_gpu.last_info
-            assert name is not None or used.startswith("gemv" if M <= 4 else "skinny"), used
+            if name is None:
+                # the table: one to four rows and (B of 16 MB or more) up to sixteen rows stream B
+                # through the matrix-vector kernels, the rest take the few-row kernels
+                expect = "gemv_4x512" if M <= 4 else "gemv_16x1024" if N * K >= 1 << 22 else "skinny"
+                assert used.startswith(expect), (used, expect)
             Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
             assert_parity(C, Cref, S, K, f"{used} {shape} split={info['split']} a={alpha} b={beta}")
             # a fixed reduction order: the same inputs give the same bits again
@@ -415,7 +419,7 @@ def test_misaligned_and_guarded_few_rows(sg, oracle_mod):
     M, N, K = 11, 700, 300
     A, B, C0 = make_inputs(M, N, K, seed=77)
     Cref, S = oracle_mod.sgemm_ref(A, B, None, 1.0, 0.0)
-    for name in [n for n in sg.config_names() if n.startswith("skinny")]:
+    for name in [n for n in sg.config_names() if n.startswith("skinny")] + ["gemv_16x1024"]:
         C, _ = run_gpu(sg, A, B, C0, 1.0, 0.0, config=name, ldc=N + 5, c_fill=np.nan)
         assert_parity(C, Cref, S, K, f"{name} nan C")
         C, used = run_gpu(sg, A, B, C0, 1.0, 0.0, config=name, off_a=1)
@@ -887,6 +891,71 @@ def test_gemv_refuses_more_than_four_rows(sg):
     assert e.value.status == sg.SGEMM_ERR_UNSUPPORTED
 
 
+# ---- five to sixteen rows: the cp.async-ring matrix-vector kernel ------------
+
+ROWS_CASES = [(5, 1, 1), (16, 1024, 640), (9, 1025, 641), (16, 4100, 2000), (8, 300, 7), (12, 16384, 1024),
+              (16, 3, 9000), (13, 2048, 4096)]
+
+
+@pytest.mark.parametrize("shape", ROWS_CASES)
+@pytest.mark.parametrize("layout", ["nn", "nn_odd"])
+def test_sixteen_rows(sg, oracle_mod, shape, layout):
+    """gemv_16x1024 (5 to 16 rows, B as stored): 16-byte and 4-byte copies
+    (odd row strides, A and B one float off a 16-byte boundary), one K chunk
+    and several (partial sums added by the reduce kernel), N and K ragged
+    against the 1024-column CTA and the 4-row copy groups; bit-identical on a
+    rerun; NaN in C ignored at beta = 0; the padding of C untouched."""
+    M, N, K = shape
+    odd = layout == "nn_odd"
+    A, B, C0 = make_inputs(M, N, K, seed=M * 3 + N + 7 * K + len(layout), dist_a=("normal", 1.0),
+                           dist_b=("normal", 0.05))
+    lda = K + (3 if odd else 0)
+    ldb = N + (1 if odd else 0)
+    ldc = N + 5
+    dA, pA, _ = _to_dev(A, lda, 1 if odd else 0)
+    dB, pB, _ = _to_dev(B, ldb, 1 if odd else 0)
+    for alpha, beta in ((1.0, 0.0), (-0.5, 2.0)):
+        dC, pC, _ = _to_dev(np.full((M, N), np.nan, np.float32) if beta == 0.0 else C0, ldc, 0, fill=7.0)
+        plan = sg.Plan(M, N, K, lda, ldb, ldc, config="gemv_16x1024")
+        info = plan.info()
+        assert info["variant"] == "gemv_16x1024", info
+        assert plan.launches in (1, 2) and (info["split"] > 1 or plan.launches == 1), (plan.launches, info)
+        outs = []
+        for _ in range(2):
+            if beta != 0.0:
+                dC.copy_(_to_dev(C0, ldc, 0, fill=7.0)[0])
+            plan.run(alpha, pA, pB, beta, pC)
+            torch.cuda.synchronize()
+            assert sg.device_status() == sg.SGEMM_OK
+            outs.append(dC.cpu().numpy().copy())
+        plan.close()
+        assert np.array_equal(outs[0], outs[1], equal_nan=True), "not reproducible"
+        host = outs[0]
+        C = np.stack([host[m * ldc: m * ldc + N] for m in range(M)])
+        for m in range(M):
+            assert np.all(host[m * ldc + N: (m + 1) * ldc if m + 1 < M else host.size] == 7.0), "padding written"
+        Cref, S = oracle_mod.sgemm_ref(A, B, C0 if beta != 0.0 else None, alpha, beta)
+        assert_parity(C, Cref, S, K, f"rows16 {layout} {shape} split={info['split']} a={alpha} b={beta}")
+
+
+def test_sixteen_rows_table_and_limits(sg):
+    """The table sends one product of 5 to 16 rows with B as stored and 16 MB
+    or more of B to gemv_16x1024 (no padding copy, even for odd ldb), B given
+    transposed to the few-row kernel that reads it as stored; the variant
+    refuses 17 rows."""
+    for (M, N, K, ldb) in ((16, 16384, 8192, 16384), (5, 4096, 1024, 4096), (16, 16384, 8192, 16385)):
+        plan = sg.Plan(M, N, K, ldb=ldb)
+        info = plan.info()
+        assert info["variant"] == "gemv_16x1024" and info["repack"] == 0, info
+        plan.close()
+    plan = sg.Plan(16, 16384, 8192, transb=True)
+    assert plan.info()["variant"].startswith("skinny_sk"), plan.info()
+    plan.close()
+    with pytest.raises(sg.SgemmError) as e:
+        sg.Plan(17, 256, 256, config="gemv_16x1024")
+    assert e.value.status == sg.SGEMM_ERR_UNSUPPORTED
+
+
 def test_ffma_probe(sg):
     """The FMA-only probe: its rate is near the nominal SMs x 128 x 2 x clock, and the clock read inside the
     kernel is a plausible SM clock."""
@@ -913,13 +982,14 @@ def test_c_overlapping_a_or_b_is_refused(sg):
     plan.close()
 
 
-@pytest.mark.parametrize("shape", [(2048, 2048, 1024), (4096, 4096, 1024), (16, 16384, 4096)])
-def test_stream_k_plan_replays_in_a_cuda_graph(sg, oracle_mod, shape):
+@pytest.mark.parametrize("shape,config", [((2048, 2048, 1024), None), ((4096, 4096, 1024), None),
+                                          ((16, 16384, 4096), "skinny_sk_16x128x32_w4_s3_b3_ef")])
+def test_stream_k_plan_replays_in_a_cuda_graph(sg, oracle_mod, shape, config):
     """A stream-K plan captured in a CUDA graph and replayed on new inputs: the
     finishers clear the flags they consumed, so the fixed epoch of the
     captured launch stays valid replay after replay."""
     M, N, K = shape
-    plan = sg.Plan(M, N, K)
+    plan = sg.Plan(M, N, K, config=config)
     info = plan.info()
     assert info["streamk"] == 1, info
     dA = torch.zeros(M, K, device="cuda")
@@ -945,6 +1015,40 @@ def test_stream_k_plan_replays_in_a_cuda_graph(sg, oracle_mod, shape):
         Cs = dC.cpu().numpy()[np.ix_(rows, cols)]
         Cref, S = oracle_mod.sgemm_ref(np.ascontiguousarray(A[rows]), np.ascontiguousarray(B[:, cols]), None, 1.0, 0.0)
         assert_parity(Cs, Cref, S, K, f"graph replay {rep} of {info['variant']}")
+    plan.close()
+
+
+@pytest.mark.parametrize("shape", [(1, 16384, 8192), (16, 16384, 4096), (7, 3000, 5000)])
+def test_matrix_vector_plan_replays_in_a_cuda_graph(sg, oracle_mod, shape):
+    """A matrix-vector plan whose K is cut into chunks (the chunk kernel, then
+    its reduce kernel as a programmatic dependent launch) captured in a CUDA
+    graph and replayed on new inputs with beta != 0."""
+    M, N, K = shape
+    plan = sg.Plan(M, N, K)
+    info = plan.info()
+    assert info["kind"] == "gemv" and info["split"] > 1 and plan.launches == 2, info
+    dA = torch.zeros(M, K, device="cuda")
+    dB = torch.zeros(K, N, device="cuda")
+    dC = torch.zeros(M, N, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        plan.run(1.0, dA, dB, 0.5, dC, stream=s)  # warm: kernel attributes and modules before capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        plan.run(-0.75, dA, dB, 0.5, dC, stream=s)
+    for rep in range(3):
+        A, B, C0 = make_inputs(M, N, K, seed=500 + rep, dist_a=("normal", 1.0), dist_b=("normal", 0.05))
+        dA.copy_(torch.from_numpy(A))
+        dB.copy_(torch.from_numpy(B))
+        dC.copy_(torch.from_numpy(C0))
+        g.replay()
+        torch.cuda.synchronize()
+        assert sg.device_status() == sg.SGEMM_OK
+        Cref, S = oracle_mod.sgemm_ref(A, B, C0, -0.75, 0.5)
+        assert_parity(dC.cpu().numpy(), Cref, S, K, f"graph replay {rep} of {info['variant']}")
     plan.close()
 
 
