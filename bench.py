@@ -67,6 +67,7 @@ KERNEL_SOURCES = {
     "tf32x3": ["tc_tf32x3.cu", "ptx.cuh", "kernels.h"],
     "generic": ["kernel_generic.cu", "kernels.h"],
     "gemv": ["kernel_gemv.cu", "kernel_gemv.h", "kernels.h"],
+    "tiny_": ["kernel_tiny.cu", "kernels.h"],
 }
 
 
