@@ -29,6 +29,7 @@ from ._lib import (  # noqa: F401
     run_static_scratch,
     selftest_wait_timeout,
     set_wait_timeout_ns,
+    wait_limit_ns,
     sgemm,
     status_string,
 )

@@ -42,6 +42,7 @@ SIGNATURES = {
     "sgemm_status_string": (ctypes.c_char_p, [_int]),
     "sgemm_device_status": (_int, [_int]),
     "sgemm_set_wait_timeout_ns": (_int, [ctypes.c_uint64]),
+    "sgemm_wait_limit_ns": (_int, [_i64, _i64, _i64, _i64, _int, ctypes.POINTER(ctypes.c_uint64)]),
     "sgemm_selftest_wait_timeout": (_int, [ctypes.c_uint64, _vp]),
     "sgemm_run_static_scratch": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "sgemm_plan_ex": (_int, [_int, _int, _int, _i64, _i64, _i64, _i64, _i64, _i64, _int, ctypes.POINTER(_vp)]),
@@ -125,6 +126,14 @@ def device_status(reset: bool = True) -> int:
 
 def set_wait_timeout_ns(ns: int) -> None:
     _check(lib().sgemm_set_wait_timeout_ns(int(ns)), "sgemm_set_wait_timeout_ns")
+
+
+def wait_limit_ns(M: int, N: int, K: int, batch: int = 1, num_sms: int = 152) -> int:
+    """The in-kernel wait limit a launch of this product gets (the setting, or its work-based floor)."""
+    out = ctypes.c_uint64()
+    _check(lib().sgemm_wait_limit_ns(int(M), int(N), int(K), int(batch), int(num_sms), ctypes.byref(out)),
+           "sgemm_wait_limit_ns")
+    return int(out.value)
 
 
 def selftest_wait_timeout(ns: int, stream=None) -> int:

@@ -22,8 +22,9 @@ bool api_encoder_ready();
 // Encode a->tmA / a->tmB for variant v on these operands.
 sgemm_status_t api_encode_maps(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                const float* A, const float* B, LaunchArgs* a);
-// The current limit for in-kernel waits.
-uint64_t api_wait_timeout_ns();
+// The limit for the in-kernel waits of an M x N x K launch on `sms` SMs:
+// the process-wide setting, or the launch's work-based floor if larger.
+uint64_t api_wait_timeout_ns(int64_t M, int64_t N, int64_t K, int sms);
 // The persistent grid of a transposed-A plan over `tiles` C tiles of KT
 // k-slices, SMs x CTAs per SM resident: full waves data-parallel and, when
 // stream-K is allowed, the last partial wave split along K (dp_waves full

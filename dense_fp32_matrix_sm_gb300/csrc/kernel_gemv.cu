@@ -334,7 +334,8 @@ __global__ void __launch_bounds__(kGvThreads) gemv_nk_kernel(const GemvParams p)
 // 4g .. 4g+3): lane q adds chunks q, q+4, q+8, ... in ascending order, the
 // four sums meet through two xor shuffles as (s0 + s1) + (s2 + s3), the
 // same bits in all four lanes, and lane q writes column 4g + q.  The order
-// is fixed by the shape, so reruns agree bit for bit.
+// is fixed by the shape, so reruns agree bit for bit.  Every lane issues
+// its loads (up to five per round) at once.
 constexpr int kRedThreads = 256;
 
 __global__ void __launch_bounds__(kRedThreads) gemv_reduce_kernel(const GemvParams p) {
@@ -343,10 +344,10 @@ __global__ void __launch_bounds__(kRedThreads) gemv_reduce_kernel(const GemvPara
   const int q = t & 3;
   const int n = 4 * (t >> 2);  // the quad's first column
   const bool mine = n + q < p.N;
-  float* d = p.C + z * p.stride_c + static_cast<int64_t>(m) * p.ldc + n + q;
+  const int64_t c_off = z * p.stride_c + static_cast<int64_t>(m) * p.ldc + n + q;
   // The chunk kernel never writes C, and whatever ran before it has
   // finished, so C is read before the wait.
-  const float c_old = mine && p.beta != 0.f ? *d : 0.f;
+  const float c_old = mine && p.beta != 0.f ? p.C[c_off] : 0.f;
   wait_primary();
   float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
   auto add = [](float4& a, const float4 b) {
@@ -359,13 +360,13 @@ __global__ void __launch_bounds__(kRedThreads) gemv_reduce_kernel(const GemvPara
     const float4* ws =
         reinterpret_cast<const float4*>(p.ws + (static_cast<int64_t>(z) * p.S * p.M + m) * p.n_pad + n);
     const int64_t step = static_cast<int64_t>(p.M) * p.n_pad / 4;  // one chunk to the next, in float4s
-    for (int s = q; s < p.S; s += 32) {  // up to eight loads in flight
-      float4 v[8];
+    for (int s = q; s < p.S; s += 20) {  // up to five loads in flight (one round for S <= 20)
+      float4 v[5];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
+      for (int u = 0; u < 5; ++u)
         if (s + 4 * u < p.S) v[u] = __ldcg(ws + (s + 4 * u) * step);
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
+      for (int u = 0; u < 5; ++u)
         if (s + 4 * u < p.S) add(sum, v[u]);
     }
   }
@@ -380,7 +381,7 @@ __global__ void __launch_bounds__(kRedThreads) gemv_reduce_kernel(const GemvPara
   }
   if (mine) {
     const float tot = q == 0 ? sum.x : q == 1 ? sum.y : q == 2 ? sum.z : sum.w;
-    *d = p.beta == 0.f ? p.alpha * tot : fmaf(p.alpha, tot, p.beta * c_old);
+    p.C[c_off] = p.beta == 0.f ? p.alpha * tot : fmaf(p.alpha, tot, p.beta * c_old);
   }
 }
 

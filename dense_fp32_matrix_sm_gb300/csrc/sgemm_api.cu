@@ -38,6 +38,7 @@ struct sgemm_plan_s {
   int ctas_per_sm;
   int grid;
   int split;        // CTAs per cluster along K (skinny variants), else 1
+  uint64_t wait_floor_ns;  // the plan's work-based floor for in-kernel wait limits
   int64_t tiles;
   // stream-K tail (tmat variants): dp_waves full waves, then sk_iters k-slices
   // split over the grid; ws/flags are device memory owned by the plan.
@@ -89,6 +90,26 @@ constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
 
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+
+// A launch's waits may legitimately last as long as the launch itself: a
+// stream-K finisher waits for contributors that run a K-range of their own
+// after their data-parallel tiles.  So the limit never goes below the time
+// the whole product would take at kFloorFlopsPerSm FLOP/s per SM, about
+// 1/45 of what the FFMA kernels sustain on GB300 (450 GFLOP/s per SM).
+constexpr double kFloorFlopsPerSm = 1e10;
+
+uint64_t work_floor_ns(int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
+  if (M <= 0 || N <= 0 || K <= 0 || sms <= 0) return 0;
+  const double flops = 2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) *
+                       static_cast<double>(batch > 1 ? batch : 1);
+  const double ns = flops / (static_cast<double>(sms) * kFloorFlopsPerSm) * 1e9;
+  return ns >= 1.8e19 ? UINT64_C(18000000000000000000) : static_cast<uint64_t>(ns);
+}
+
+uint64_t wait_limit_ns(uint64_t floor_ns) {
+  const uint64_t t = g_timeout_ns.load(std::memory_order_relaxed);
+  return t > floor_ns ? t : floor_ns;
+}
 std::mutex g_status_mutex;
 unsigned int* g_status_addr[kMaxDevices] = {};
 
@@ -416,6 +437,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->tiles = ((M + v->bm - 1) / v->bm) * ((N + v->bn - 1) / v->bn) * batch;
   int64_t grid = p->tiles;
   p->split = 1;
+  p->wait_floor_ns = work_floor_ns(M, N, K, batch, sms);
   p->dp_waves = 0;
   p->sk_iters = 0;
   p->ws = nullptr;
@@ -1077,7 +1099,7 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
     }
     a.epoch = e;
   }
-  a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  a.timeout_ns = wait_limit_ns(p->wait_floor_ns);
   sgemm_status_t st = status_addr(device, &a.status);
   if (st != SGEMM_OK) return st;
   if (v->kind == kKindTc) {
@@ -1293,6 +1315,12 @@ sgemm_status_t sgemm_device_status(int reset) {
   return v ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
 }
 
+sgemm_status_t sgemm_wait_limit_ns(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, uint64_t* out) {
+  if (!out || M < 0 || N < 0 || K < 0 || batch < 0 || num_sms < 1) return SGEMM_ERR_INVALID_ARG;
+  *out = wait_limit_ns(work_floor_ns(M, N, K, batch, num_sms));
+  return SGEMM_OK;
+}
+
 sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns) {
   g_timeout_ns.store(timeout_ns ? timeout_ns : kDefaultTimeoutNs, std::memory_order_relaxed);
   return SGEMM_OK;
@@ -1345,7 +1373,9 @@ sgemm_status_t api_encode_maps(const Variant* v, int64_t M, int64_t N, int64_t K
   return encode_maps(v, &shape, A, B, a);
 }
 
-uint64_t api_wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+uint64_t api_wait_timeout_ns(int64_t M, int64_t N, int64_t K, int sms) {
+  return wait_limit_ns(work_floor_ns(M, N, K, 1, sms));
+}
 
 // Stream-K schedules (measured on GB300, CUDA events, L2 flushed):
 //  * Tail: more tiles than resident CTAs and a partial last wave -- full

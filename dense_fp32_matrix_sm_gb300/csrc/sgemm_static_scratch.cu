@@ -141,7 +141,7 @@ extern "C" sgemm_status_t sgemm_run_static_scratch(int64_t M, int64_t N, int64_t
   a.beta = beta;
   a.split_k = 1;
   a.status = s->status;
-  a.timeout_ns = api_wait_timeout_ns();
+  a.timeout_ns = api_wait_timeout_ns(M, N, K, s->sms);
 
   // The same schedule as a plan of this variant (api_streamk_schedule):
   // full waves data-parallel and a partial last wave split along K; with

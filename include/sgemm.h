@@ -68,7 +68,8 @@
  * Errors: every entry point returns a status and never aborts.  Launch
  * failures map to SGEMM_ERR_CUDA.  Faults during execution surface at the
  * caller's next synchronisation, as with any CUDA launch.  Every wait inside
- * a kernel has a time limit (default 4 s, see sgemm_set_wait_timeout_ns);
+ * a kernel has a time limit (default 4 s, raised for long products; see
+ * sgemm_set_wait_timeout_ns);
  * a wait that runs out records SGEMM_ERR_TIMEOUT in a per-device status
  * word that sgemm_device_status reads.
  */
@@ -373,8 +374,24 @@ sgemm_status_t sgemm_device_status(int reset);
 /*
  * Time limit, in nanoseconds, for every wait inside the library's kernels
  * on later launches (process-wide; default 4e9).  0 restores the default.
+ * A launch never gets less than a floor that grows with its work: the time
+ * the whole product (2*M*N*K*batch FLOPs) would take at 1e10 FLOP/s per SM,
+ * about 1/45 of the rate the FFMA kernels sustain on GB300.  A stream-K
+ * finisher's wait for its contributors can legitimately last as long as
+ * their K-ranges, so the floor keeps long problems clear of the limit
+ * (4096^3: 0.09 s, below the 4 s default; 65536^3 on 152 SMs: 370 s).
  */
 sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/*
+ * The wait limit a launch of an M x N x K product (over `batch` products)
+ * gets on a device with num_sms SMs: the larger of the current setting and
+ * that work-based floor.  Pure host arithmetic, no CUDA call.  *out is set
+ * on SGEMM_OK; negative sizes, num_sms < 1 or out == NULL give
+ * SGEMM_ERR_INVALID_ARG.  (An operational aid; the pages have no
+ * counterpart.)
+ */
+sgemm_status_t sgemm_wait_limit_ns(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, uint64_t *out);
 
 /*
  * Self-test of the wait limit: launches one thread that waits, with limit

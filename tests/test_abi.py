@@ -174,3 +174,30 @@ def test_product_path_has_no_oracle_or_fallback():
         text = open(path).read()
         assert "import oracle" not in text and "from oracle" not in text, path
         assert "torch.matmul" not in text and "np.matmul" not in text, path
+
+
+def test_wait_limit_follows_the_work():
+    """The in-kernel wait limit of a launch is the larger of the process-wide
+    setting (default 4 s) and the time the product would take at 1e10 FLOP/s
+    per SM.  Values worked by hand: 2 * 4096^3 / (152 * 1e10) s = 0.0904 s,
+    under the 4 s default; 2 * 65536^3 / (152 * 1e10) s = 370.3 s."""
+    import dense_fp32_matrix_sm_gb300 as sg
+
+    assert sg.wait_limit_ns(4096, 4096, 4096, 1, 152) == 4_000_000_000
+    big = sg.wait_limit_ns(65536, 65536, 65536, 1, 152)
+    assert abs(big - 2 * 65536 ** 3 / (152 * 1e10) * 1e9) < 1e3 and 370e9 < big < 371e9
+    # the batch multiplies the work; fewer SMs raise the floor in proportion
+    assert sg.wait_limit_ns(16384, 16384, 16384, 8, 152) == sg.wait_limit_ns(32768, 32768, 16384, 2, 152)
+    assert abs(sg.wait_limit_ns(65536, 65536, 65536, 1, 76) - 2 * big) < 1e3
+    # empty products take the setting
+    assert sg.wait_limit_ns(0, 4096, 4096, 1, 152) == 4_000_000_000
+    try:
+        sg.set_wait_timeout_ns(10 ** 12)  # a longer setting wins over a smaller floor
+        assert sg.wait_limit_ns(4096, 4096, 4096, 1, 152) == 10 ** 12
+        assert sg.wait_limit_ns(65536, 65536, 65536, 1, 152) == 10 ** 12
+    finally:
+        sg.set_wait_timeout_ns(0)
+    assert sg.wait_limit_ns(4096, 4096, 4096, 1, 152) == 4_000_000_000
+    for bad in ((-1, 4, 4, 1, 152), (4, 4, 4, -1, 152), (4, 4, 4, 1, 0)):
+        with pytest.raises(sg.SgemmError):
+            sg.wait_limit_ns(*bad)
