@@ -13,7 +13,11 @@ import threading
 from typing import Optional
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
+# SGEMM_GB300_LIBRARY=checked loads the checked build (build.py: device-side
+# bounds checks that report SGEMM_ERR_BOUNDS instead of touching memory out
+# of range); the default is the normal build.
+LIB_PATH = os.path.join(_PKG, "libsgemm_gb300_checked.so" if os.environ.get("SGEMM_GB300_LIBRARY") == "checked"
+                        else "libsgemm_gb300.so")
 
 SGEMM_OK = 0
 SGEMM_ERR_INVALID_ARG = -1
@@ -21,6 +25,7 @@ SGEMM_ERR_UNSUPPORTED = -2
 SGEMM_ERR_CUDA = -3
 SGEMM_ERR_TIMEOUT = -4
 SGEMM_ERR_NOMEM = -5
+SGEMM_ERR_BOUNDS = -6
 SGEMM_TUNE_TENSOR_CORES = 1
 
 # Every function include/sgemm.h declares, with (restype, argtypes).

@@ -5,6 +5,12 @@ fast-math, -lineinfo for profiling), then nvcc links them into a shared
 library next to this file.  ptxas register/spill reports go to
 _build/ptxas_<unit>.log.  Rebuilds only when a source or header is newer
 than the library (or force=True).  Runs without a GPU.
+
+build(checked=True) makes the checked build, libsgemm_gb300_checked.so
+(objects in _build_checked/): the same sources compiled with
+-DSGEMM_CHECKED, whose kernels test every hand-computed shared-memory and
+workspace index before the access (csrc/checked.cuh).  Tests load it with
+SGEMM_GB300_LIBRARY=checked.
 """
 from __future__ import annotations
 
@@ -21,6 +27,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsgemm_gb300.so")
+# the checked build: the same sources with -DSGEMM_CHECKED (csrc/checked.cuh)
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libsgemm_gb300_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-Wformat,-Werror=format", "-Xptxas", "-v",
@@ -43,44 +52,49 @@ def _inputs():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(checked: bool = False) -> bool:
+    lib = LIB_CHECKED if checked else LIB
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def _compile(src: str) -> str:
+def _compile(src: str, checked: bool = False) -> str:
     unit = os.path.splitext(os.path.basename(src))[0]
-    obj = os.path.join(BUILD, unit + ".o")
-    cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+    out_dir = BUILD_CHECKED if checked else BUILD
+    obj = os.path.join(out_dir, unit + ".o")
+    cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *(["-DSGEMM_CHECKED"] if checked else []), "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
-    with open(os.path.join(BUILD, f"ptxas_{unit}.log"), "w") as f:
+    with open(os.path.join(out_dir, f"ptxas_{unit}.log"), "w") as f:
         f.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {unit}.cu:\n{r.stderr[-6000:]}")
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Build the library (checked=True: the checked build, libsgemm_gb300_checked.so)."""
+    lib = LIB_CHECKED if checked else LIB
+    out_dir = BUILD_CHECKED if checked else BUILD
+    if not force and up_to_date(checked):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     srcs = _sources()
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        objs = list(ex.map(_compile, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda src: _compile(src, checked), srcs))
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stderr[-4000:]}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        for log in sorted(glob.glob(os.path.join(BUILD, "ptxas_*.log"))):
+        for log in sorted(glob.glob(os.path.join(out_dir, "ptxas_*.log"))):
             with open(log) as f:
                 sys.stdout.write(f.read())
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

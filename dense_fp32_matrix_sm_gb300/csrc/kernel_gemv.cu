@@ -45,6 +45,7 @@
 #include <atomic>
 #include <type_traits>
 
+#include "checked.cuh"
 #include "kernel_gemv.h"
 
 namespace sgemm {
@@ -72,6 +73,8 @@ struct GemvParams {
   int direct;  // S == 1: apply alpha and beta to C here
   float alpha, beta;
   int64_t stride_a, stride_b, stride_c;
+  unsigned int* status;  // per-device status word (checked build: bounds)
+  int64_t ws_floats;     // floats the workspace holds (checked build)
 };
 
 // B is read exactly once: non-coherent loads that skip L1 and carry an L2
@@ -159,7 +162,8 @@ __device__ __forceinline__ void store_out(const GemvParams& p, int z, int s, int
     float* d = p.C + z * p.stride_c + static_cast<int64_t>(m) * p.ldc + n;
     *d = p.beta == 0.f ? p.alpha * acc : fmaf(p.alpha, acc, p.beta * *d);
   } else {
-    p.ws[((static_cast<int64_t>(z) * p.S + s) * p.M + m) * p.n_pad + n] = acc;
+    const int64_t wi = ((static_cast<int64_t>(z) * p.S + s) * p.M + m) * p.n_pad + n;
+    if (SG_CHK(SG_IN(wi, p.ws_floats), p.status)) p.ws[wi] = acc;
   }
 }
 
@@ -200,6 +204,7 @@ __global__ void __launch_bounds__(kGvThreads) gemv_kn_kernel(const GemvParams p)
     return make_float4(v[0], v[1], v[2], v[3]);
   };
   auto fma_row = [&](const float4 v, int k) {
+    if (!SG_CHK(SG_IN(k, kGvMaxChunk), p.status)) return;
 #pragma unroll
     for (int m = 0; m < MR; ++m) {
       const float x = xs[m][k];
@@ -221,11 +226,12 @@ __global__ void __launch_bounds__(kGvThreads) gemv_kn_kernel(const GemvParams p)
 
   if (!p.direct && vec) {
     // n_pad is a multiple of 4 and c + 3 < n_pad: one 16-byte store per row
-    float* w = p.ws + ((static_cast<int64_t>(z) * p.S + s) * p.M) * p.n_pad + c;
+    const int64_t w0 = ((static_cast<int64_t>(z) * p.S + s) * p.M) * p.n_pad + c;
 #pragma unroll
     for (int m = 0; m < MR; ++m)
-      *reinterpret_cast<float4*>(w + static_cast<int64_t>(m) * p.n_pad) =
-          make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+      if (SG_CHK(SG_IN(w0 + static_cast<int64_t>(m) * p.n_pad + 3, p.ws_floats), p.status))
+        *reinterpret_cast<float4*>(p.ws + w0 + static_cast<int64_t>(m) * p.n_pad) =
+            make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
     return;
   }
 #pragma unroll
@@ -263,6 +269,7 @@ __global__ void __launch_bounds__(kGvThreads) gemv_nk_kernel(const GemvParams p)
   // whenever its start is
   if (p.vec_b) {
     auto step = [&](const float4 (&v)[R], int k) {
+      if (!SG_CHK(SG_IN(k + 3, kGvMaxChunk), p.status)) return;
 #pragma unroll
       for (int m = 0; m < MR; ++m) {
         const float4 x = *reinterpret_cast<const float4*>(&xs[m][k]);
@@ -364,7 +371,12 @@ __global__ void __launch_bounds__(kRedThreads) gemv_reduce_kernel(const GemvPara
       float4 v[5];
 #pragma unroll
       for (int u = 0; u < 5; ++u)
-        if (s + 4 * u < p.S) v[u] = __ldcg(ws + (s + 4 * u) * step);
+        if (s + 4 * u < p.S)
+          v[u] = SG_CHK(SG_IN((static_cast<int64_t>(z) * p.S * p.M + m) * p.n_pad + n + 4 * (s + 4 * u) * step + 3,
+                              p.ws_floats),
+                        p.status)
+                     ? __ldcg(ws + (s + 4 * u) * step)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int u = 0; u < 5; ++u)
         if (s + 4 * u < p.S) add(sum, v[u]);
@@ -431,7 +443,8 @@ __global__ void __launch_bounds__(kRcThreads, 2) rows_cp_kernel(const GemvParams
   extern __shared__ __align__(16) float rsm[];
   float* at = rsm;  // [kRcMaxChunk][MR]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float4* slot0 = reinterpret_cast<float4*>(rsm + kRcMaxChunk * MR) + warp * kRcRing * 32 + lane;
+  float4* const ring = reinterpret_cast<float4*>(rsm + kRcMaxChunk * MR);  // [warps][kRcRing][32]
+  float4* slot0 = ring + warp * kRcRing * 32 + lane;
   allow_dependents();
   const int z = blockIdx.z, s = blockIdx.y;
   const int k0 = s * p.kc;
@@ -445,6 +458,7 @@ __global__ void __launch_bounds__(kRcThreads, 2) rows_cp_kernel(const GemvParams
   // row q of B (this lane's four columns) into ring slot d; columns past N
   // are zero
   auto fetch = [&](float4* d, const float* q) {
+    if (!SG_CHK(SG_IN(d - ring, kRcWarps * kRcRing * 32), p.status)) return;
     if (vec) {
       cpa16_hint(d, q, pol);
     } else {
@@ -464,6 +478,7 @@ __global__ void __launch_bounds__(kRcThreads, 2) rows_cp_kernel(const GemvParams
     const float* A = p.A + z * p.stride_a + k0;
     for (int i = threadIdx.x; i < MR * len; i += kRcThreads) {
       const int m = i % MR, k = i / MR;
+      if (!SG_CHK(SG_IN(k * MR + m, kRcMaxChunk * MR), p.status)) continue;
       if (m < p.M)
         cpa4(at + k * MR + m, A + static_cast<int64_t>(m) * p.lda + k);
       else
@@ -495,6 +510,7 @@ __global__ void __launch_bounds__(kRcThreads, 2) rows_cp_kernel(const GemvParams
     for (int j = 0; j < 4; ++j) acc[h][j] = make_float2(0.f, 0.f);
   // one row: A at ap (MR values, k-major), B's four columns in bv
   auto fma_row = [&](const float4 bv, const float* ap) {
+    if (!SG_CHK(SG_IN(ap - at + MR - 1, kRcMaxChunk * MR), p.status)) return;
     const float4* a4 = reinterpret_cast<const float4*>(ap);
     const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
@@ -515,6 +531,7 @@ __global__ void __launch_bounds__(kRcThreads, 2) rows_cp_kernel(const GemvParams
   auto run = [&](auto vec_c) {
     constexpr bool V = decltype(vec_c)::value;
     auto put = [&](float4* d, const float* src) {
+      if (!SG_CHK(SG_IN(d - ring, kRcWarps * kRcRing * 32), p.status)) return;
       if (V) {
         cpa16_hint(d, src, pol);
       } else {
@@ -536,6 +553,7 @@ __global__ void __launch_bounds__(kRcThreads, 2) rows_cp_kernel(const GemvParams
     for (; k < kfull; k += kRcGroup) {
       float4* sg = slot0 + (k & (kRcRing - 1)) * 32;
       cpa_wait_group<kRcGroups - 1>();
+      if (!SG_CHK(SG_IN(sg + (kRcGroup - 1) * 32 - ring, kRcWarps * kRcRing * 32), p.status)) break;
       // one row at a time: hoisting every row's shared loads (16 A words
       // and 4 B words per row) would not fit in the registers beside the
       // accumulators
@@ -568,16 +586,19 @@ __global__ void __launch_bounds__(kRcThreads, 2) rows_cp_kernel(const GemvParams
     run(std::true_type{});
   else
     run(std::false_type{});
+  cpa_wait_all();  // nothing real is in flight any more (only empty groups)
 
   if (!p.direct && vec) {
     // n_pad is a multiple of 4 and c + 3 < n_pad: one 16-byte store per row
-    float* wp = p.ws + ((static_cast<int64_t>(z) * p.S + s) * p.M) * p.n_pad + c;
+    const int64_t w0 = ((static_cast<int64_t>(z) * p.S + s) * p.M) * p.n_pad + c;
+    float* wp = p.ws + w0;
 #pragma unroll
     for (int h = 0; h < MR / 2; ++h) {
-      if (2 * h < p.M)
+      if (2 * h < p.M && SG_CHK(SG_IN(w0 + static_cast<int64_t>(2 * h) * p.n_pad + 3, p.ws_floats), p.status))
         *reinterpret_cast<float4*>(wp + static_cast<int64_t>(2 * h) * p.n_pad) =
             make_float4(acc[h][0].x, acc[h][1].x, acc[h][2].x, acc[h][3].x);
-      if (2 * h + 1 < p.M)
+      if (2 * h + 1 < p.M &&
+          SG_CHK(SG_IN(w0 + static_cast<int64_t>(2 * h + 1) * p.n_pad + 3, p.ws_floats), p.status))
         *reinterpret_cast<float4*>(wp + static_cast<int64_t>(2 * h + 1) * p.n_pad) =
             make_float4(acc[h][0].y, acc[h][1].y, acc[h][2].y, acc[h][3].y);
     }
@@ -750,6 +771,8 @@ cudaError_t launch_family(int f, const LaunchArgs& a, cudaStream_t stream) {
   p.stride_a = a.stride_a;
   p.stride_b = a.stride_b;
   p.stride_c = a.stride_c;
+  p.status = a.status;
+  p.ws_floats = a.ws_slots;
   const int64_t cols = a.b_trans ? (a.N + fam.trows - 1) / fam.trows : (a.N + fam.cols - 1) / fam.cols;
   if (cols > 0x7fffffff) return cudaErrorInvalidValue;
   int smem = 0;

@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "checked.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -37,6 +38,7 @@ struct GenericParams {
   int M, N, K;
   float alpha, beta;
   int64_t stride_a, stride_b, stride_c;  // batch z = blockIdx.z
+  unsigned int* status;                  // per-device status word (checked build: bounds)
 };
 
 __global__ void __launch_bounds__(kGThreads) sgemm_generic_kernel(GenericParams p) {
@@ -70,8 +72,10 @@ __global__ void __launch_bounds__(kGThreads) sgemm_generic_kernel(GenericParams 
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int idx = tid + kGThreads * r;
-      As[idx % kGBK][idx / kGBK] = ra[r];
-      Bs[idx / kGBN][idx % kGBN] = rb[r];
+      if (SG_CHK(SG_IN(idx, kGBM * kGBK) && SG_IN(idx, kGBK * kGBN), p.status)) {
+        As[idx % kGBK][idx / kGBK] = ra[r];
+        Bs[idx / kGBN][idx % kGBN] = rb[r];
+      }
     }
   };
 
@@ -90,9 +94,9 @@ __global__ void __launch_bounds__(kGThreads) sgemm_generic_kernel(GenericParams 
     for (int k = 0; k < kGBK; ++k) {
       float a[4], b[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[k][ty + 16 * i];
+      for (int i = 0; i < 4; ++i) a[i] = SG_CHK(SG_IN(ty + 16 * i, kGBM), p.status) ? As[k][ty + 16 * i] : 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = Bs[k][tx + 16 * j];
+      for (int j = 0; j < 4; ++j) b[j] = SG_CHK(SG_IN(tx + 16 * j, kGBN), p.status) ? Bs[k][tx + 16 * j] : 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -121,8 +125,9 @@ cudaError_t generic_occupancy(int* ctas) {
 }
 
 cudaError_t generic_launch(const LaunchArgs& a, cudaStream_t stream) {
-  GenericParams p{a.A, a.B, a.C, a.lda, a.ldb, a.ldc, a.M, a.N, a.K, a.alpha, a.beta, a.stride_a, a.stride_b,
-                  a.stride_c};
+  GenericParams p{a.A,       a.B,        a.C,        a.lda,      a.ldb,      a.ldc,      a.M,
+                  a.N,       a.K,        a.alpha,    a.beta,     a.stride_a, a.stride_b, a.stride_c,
+                  a.status};
   const int64_t tiles = static_cast<int64_t>((a.M + kGBM - 1) / kGBM) * ((a.N + kGBN - 1) / kGBN);
   const int batch = a.batch > 1 ? a.batch : 1;
   if (tiles > 0x7fffffff || batch > 65535) return cudaErrorInvalidConfiguration;

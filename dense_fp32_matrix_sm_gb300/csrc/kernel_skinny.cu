@@ -44,6 +44,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "checked.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -113,7 +114,7 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
 // group), accumulated into accp[p][j] = {C[2p][4l + j], C[2p + 1][4l + j]}.
 template <int BN, int GW>
 __device__ __forceinline__ void pa_slice(const float* As, const float4* Bs4, float* atw, int gw, int lane,
-                                         float2 (&accp)[kSBM / 2][4]) {
+                                         float2 (&accp)[kSBM / 2][4], unsigned int* status) {
 #pragma unroll
   for (int qq = 0; qq < (kSBK / 4) / GW; ++qq) {
     // Transpose this warp's k-quad of A (16 rows x 4 k) into atw[k][m]:
@@ -122,14 +123,18 @@ __device__ __forceinline__ void pa_slice(const float* As, const float4* Bs4, flo
     const int q = gw + GW * qq;
     {
       const int m = lane >> 1, h = lane & 1;
-      const float2 v = *reinterpret_cast<const float2*>(As + m * kSBK + ((q ^ (m & 7)) << 2) + 2 * h);
+      const int ai = m * kSBK + ((q ^ (m & 7)) << 2) + 2 * h;
+      const float2 v = SG_CHK(SG_IN(ai + 1, kSBM * kSBK) && SG_IN((2 * h + 1) * 32 + 16 * h + m, 128), status)
+                           ? *reinterpret_cast<const float2*>(As + ai)
+                           : make_float2(0.f, 0.f);
       atw[(2 * h) * 32 + 16 * h + m] = v.x;
       atw[(2 * h + 1) * 32 + 16 * h + m] = v.y;
     }
     __syncwarp();
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      const float4 b = Bs4[(4 * q + kk) * (BN / 4)];
+      const float4 b = SG_CHK(SG_IN(4 * q + kk, kSBK), status) ? Bs4[(4 * q + kk) * (BN / 4)]
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
       const float bb[4] = {b.x, b.y, b.z, b.w};
       const float* ak = atw + kk * 32 + 16 * ((kk >> 1) & 1);
 #pragma unroll
@@ -150,13 +155,16 @@ __device__ __forceinline__ void pa_slice(const float* As, const float4* Bs4, flo
 // of 4 k from each of its 4 rows; accp[p][j] = {C[2p][n_j], C[2p+1][n_j]}.
 template <int BN, int GW>
 __device__ __forceinline__ void pa_slice_bt(const float* As, const float* Bt, float* atw, int gw, int lane, int group,
-                                            float2 (&accp)[kSBM / 2][4]) {
+                                            float2 (&accp)[kSBM / 2][4], unsigned int* status) {
 #pragma unroll
   for (int qq = 0; qq < (kSBK / 4) / GW; ++qq) {
     const int q = gw + GW * qq;
     {
       const int m = lane >> 1, h = lane & 1;
-      const float2 v = *reinterpret_cast<const float2*>(As + m * kSBK + ((q ^ (m & 7)) << 2) + 2 * h);
+      const int ai = m * kSBK + ((q ^ (m & 7)) << 2) + 2 * h;
+      const float2 v = SG_CHK(SG_IN(ai + 1, kSBM * kSBK) && SG_IN((2 * h + 1) * 32 + 16 * h + m, 128), status)
+                           ? *reinterpret_cast<const float2*>(As + ai)
+                           : make_float2(0.f, 0.f);
       atw[(2 * h) * 32 + 16 * h + m] = v.x;
       atw[(2 * h + 1) * 32 + 16 * h + m] = v.y;
     }
@@ -164,7 +172,9 @@ __device__ __forceinline__ void pa_slice_bt(const float* As, const float* Bt, fl
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int n = 128 * group + lane + 32 * j;
-      bq[j] = *reinterpret_cast<const float4*>(Bt + n * kSBK + ((q ^ (n & 7)) << 2));
+      const int bi = n * kSBK + ((q ^ (n & 7)) << 2);
+      bq[j] = SG_CHK(SG_IN(bi + 3, BN * kSBK), status) ? *reinterpret_cast<const float4*>(Bt + bi)
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncwarp();
 #pragma unroll
@@ -273,7 +283,7 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
               ptx::mbar_test_wait(bar_full + 8 * ((it + 1) % STAGES), ((it + 1) / STAGES) & 1u);
       const float* As = reinterpret_cast<const float*>(smem + s * S::kStageBytes);
       const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + group * 32 + lane;
-      if constexpr (PAIRA) pa_slice<BN, GW>(As, Bs4, atw, gw, lane, accp);
+      if constexpr (PAIRA) pa_slice<BN, GW>(As, Bs4, atw, gw, lane, accp, p.status);
 #pragma unroll
       for (int qq = 0; qq < S::kQuadsPerWarp && !PAIRA; ++qq) {
         const int q = gw + GW * qq;
@@ -383,6 +393,7 @@ struct SkinnySkParams {
   float* ws;             // kSBM x BN floats per CTA
   unsigned int* flags;   // one per CTA
   unsigned int epoch;
+  int64_t ws_slots;      // partial tiles (and flags) the workspace holds (checked build)
   // strided batch (BATCHED): slabs are numbered product-major over all
   // products; A and B come through 3-D tensor maps (batch = third
   // coordinate, 0 for an operand every product shares), C is offset by stride_c
@@ -511,10 +522,10 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
       const float* As = reinterpret_cast<const float*>(smem + s * S::kStageBytes);
       if constexpr (BT) {
         pa_slice_bt<BN, GW>(As, reinterpret_cast<const float*>(smem + s * S::kStageBytes + S::kStageA), atw, gw, lane,
-                            group, accp);
+                            group, accp, p.status);
       } else {
         const float4* Bs4 = reinterpret_cast<const float4*>(smem + s * S::kStageBytes + S::kStageA) + group * 32 + lane;
-        pa_slice<BN, GW>(As, Bs4, atw, gw, lane, accp);
+        pa_slice<BN, GW>(As, Bs4, atw, gw, lane, accp, p.status);
       }
       __syncwarp();
       if (lane == 0) {
@@ -559,10 +570,12 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     const float4* part4 = reinterpret_cast<const float4*>(partial);
     float4* ws4 = reinterpret_cast<float4*>(p.ws);
     if (k1 < KT) {  // contributor: partial tile to slot b, then the flag
-      for (int i = threadIdx.x; i < kTile4; i += S::kThreads) ws4[static_cast<int64_t>(b) * kTile4 + i] = part4[i];
+      for (int i = threadIdx.x; i < kTile4; i += S::kThreads)
+        if (SG_CHK(SG_IN(static_cast<int64_t>(b) * kTile4 + i, p.ws_slots * kTile4), p.status))
+          ws4[static_cast<int64_t>(b) * kTile4 + i] = part4[i];
       __threadfence();
       __syncthreads();
-      if (threadIdx.x == 0) ptx::st_release_gpu(p.flags + b, p.epoch);
+      if (threadIdx.x == 0 && SG_CHK(SG_IN(b, p.ws_slots), p.status)) ptx::st_release_gpu(p.flags + b, p.epoch);
       continue;
     }
     int c_first = b;
@@ -572,6 +585,7 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
       bool timed_out = false;
       if (threadIdx.x == 0) {
         for (int c = c_first; c < b && !timed_out; ++c) {
+          if (!SG_CHK(SG_IN(c, p.ws_slots), p.status)) continue;
           if (ptx::ld_acquire_gpu(p.flags + c) == p.epoch) continue;
           const uint64_t t0 = ptx::globaltimer_ns();
           while (ptx::ld_acquire_gpu(p.flags + c) != p.epoch) {
@@ -592,7 +606,9 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
       for (int i = threadIdx.x; i < kTile4; i += S::kThreads) {
         float4 v = part4[i];
         for (int c = c_first; c < b; ++c) {
-          const float4 o = __ldcg(&ws4[static_cast<int64_t>(c) * kTile4 + i]);
+          const float4 o = SG_CHK(SG_IN(static_cast<int64_t>(c) * kTile4 + i, p.ws_slots * kTile4), p.status)
+                               ? __ldcg(&ws4[static_cast<int64_t>(c) * kTile4 + i])
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
           v.x += o.x;
           v.y += o.y;
           v.z += o.z;
@@ -611,7 +627,8 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
       }
       __syncthreads();  // the next piece rewrites `partial`
       if (threadIdx.x == 0)
-        for (int c = c_first; c < b; ++c) *reinterpret_cast<volatile unsigned int*>(p.flags + c) = 0u;
+        for (int c = c_first; c < b; ++c)
+          if (SG_CHK(SG_IN(c, p.ws_slots), p.status)) *reinterpret_cast<volatile unsigned int*>(p.flags + c) = 0u;
       continue;
     }
     // Every global read (a contributor's partials, then C) is issued for all
@@ -626,7 +643,11 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     for (int c = c_first; c < b; ++c) {
       float4 o[kIt];
 #pragma unroll
-      for (int t = 0; t < kIt; ++t) o[t] = __ldcg(&ws4[static_cast<int64_t>(c) * kTile4 + threadIdx.x + t * S::kThreads]);
+      for (int t = 0; t < kIt; ++t)
+        o[t] = SG_CHK(SG_IN(static_cast<int64_t>(c) * kTile4 + threadIdx.x + t * S::kThreads, p.ws_slots * kTile4),
+                      p.status)
+                   ? __ldcg(&ws4[static_cast<int64_t>(c) * kTile4 + threadIdx.x + t * S::kThreads])
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int t = 0; t < kIt; ++t) {
         v[t].x += o[t].x;
@@ -682,7 +703,8 @@ __global__ void __launch_bounds__(SkinnyShape<BN, GW, STAGES>::kThreads, MINB)
     // every thread has read the contributors' partials: clear their flags, so
     // each run (a replayed graph included, whose epoch is fixed) starts from zero
     if (threadIdx.x == 0)
-      for (int c = c_first; c < b; ++c) *reinterpret_cast<volatile unsigned int*>(p.flags + c) = 0u;
+      for (int c = c_first; c < b; ++c)
+          if (SG_CHK(SG_IN(c, p.ws_slots), p.status)) *reinterpret_cast<volatile unsigned int*>(p.flags + c) = 0u;
   }
   // After a failed wait, copies still in flight land before the CTA's shared
   // memory is released.  Every warp that sees the failure drains what has been
@@ -724,6 +746,7 @@ struct SkinnySkVariant {
     p.timeout_ns = a.timeout_ns;
     p.ws = a.ws;
     p.flags = a.flags;
+    p.ws_slots = a.ws_slots;
     p.epoch = a.epoch;
     p.batch = a.batch > 1 ? a.batch : 1;
     p.stride_c = a.stride_c;

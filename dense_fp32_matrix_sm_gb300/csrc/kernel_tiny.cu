@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "checked.cuh"
 #include "kernels.h"
 
 namespace sgemm {
@@ -47,6 +48,7 @@ struct TinyParams {
   float alpha, beta;
   int64_t stride_a, stride_b, stride_c;
   int vec;  // 16-byte copies: A, B 16-byte aligned, lda, ldb, strides multiples of 4
+  unsigned int* status;  // per-device status word (checked build: bounds)
 };
 
 __host__ __device__ constexpr int tiny_ka(int K) { return ((K + 3) & ~3) + 4; }  // A row stride in smem (floats)
@@ -91,24 +93,28 @@ __global__ void __launch_bounds__(kTyThreads) sgemm_tiny_kernel(const TinyParams
     for (int idx = t; idx < kTyT * qa; idx += kTyThreads) {
       const int m = idx / qa, k = 4 * (idx - m * qa);
       const uint32_t bytes = m0 + m < p.M && k < K ? (K - k >= 4 ? 16u : 4u * (K - k)) : 0u;
-      cp_async16(as + m * ka + k, bytes ? A + static_cast<int64_t>(m0 + m) * p.lda + k : A, bytes);
+      if (SG_CHK(SG_IN(m * ka + k + 3, kTyT * ka), p.status))
+        cp_async16(as + m * ka + k, bytes ? A + static_cast<int64_t>(m0 + m) * p.lda + k : A, bytes);
     }
     // B: kp rows x 8 chunks of 4 columns
     for (int idx = t; idx < kp * (kTyT / 4); idx += kTyThreads) {
       const int k = idx >> 3, n = 4 * (idx & 7);
       const uint32_t bytes = k < K && n0 + n < p.N ? (p.N - n0 - n >= 4 ? 16u : 4u * (p.N - n0 - n)) : 0u;
-      cp_async16(bs + k * kTyT + n, bytes ? B + static_cast<int64_t>(k) * p.ldb + n0 + n : B, bytes);
+      if (SG_CHK(SG_IN(k * kTyT + n + 3, kp * kTyT), p.status))
+        cp_async16(bs + k * kTyT + n, bytes ? B + static_cast<int64_t>(k) * p.ldb + n0 + n : B, bytes);
     }
   } else {
     // 4-byte copies along rows (coalesced); zeros outside the matrices
     for (int idx = t; idx < kTyT * kp; idx += kTyThreads) {
       const int m = idx / kp, k = idx - m * kp;
+      if (!SG_CHK(SG_IN(m * ka + k, kTyT * ka), p.status)) continue;
       float* d = as + m * ka + k;
       if (m0 + m < p.M && k < K) cp_async4(d, A + static_cast<int64_t>(m0 + m) * p.lda + k);
       else *d = 0.f;
     }
     for (int idx = t; idx < kp * kTyT; idx += kTyThreads) {
       const int k = idx >> 5, n = idx & (kTyT - 1);
+      if (!SG_CHK(SG_IN(k * kTyT + n, kp * kTyT), p.status)) continue;
       float* d = bs + k * kTyT + n;
       if (k < K && n0 + n < p.N) cp_async4(d, B + static_cast<int64_t>(k) * p.ldb + n0 + n);
       else *d = 0.f;
@@ -129,6 +135,9 @@ __global__ void __launch_bounds__(kTyThreads) sgemm_tiny_kernel(const TinyParams
   const float* bcol = bs + 4 * tx;
 #pragma unroll 2
   for (int q = g; q < kp / 4; q += kTyGroups) {
+    if (!SG_CHK(SG_IN(4 * ty * ka + 3 * ka + 4 * q + 3, kTyT * ka) && SG_IN((4 * q + 3) * kTyT + 4 * tx + 3, kp * kTyT),
+                p.status))
+      break;
     float4 a[4], b[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(arow + i * ka + 4 * q);
@@ -156,6 +165,7 @@ __global__ void __launch_bounds__(kTyThreads) sgemm_tiny_kernel(const TinyParams
         make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
   __syncthreads();
   const int r = t >> 3, c = 4 * (t & 7);  // output row r, columns c .. c + 3
+  if (!SG_CHK(SG_IN((kTyGroups - 1) * kTyT * kTyT + r * kTyT + c + 3, kTyGroups * kTyT * kTyT), p.status)) return;
   float4 s = *reinterpret_cast<const float4*>(part + r * kTyT + c);
 #pragma unroll
   for (int gg = 1; gg < kTyGroups; ++gg) {
@@ -209,6 +219,7 @@ cudaError_t tiny_launch(const LaunchArgs& a, cudaStream_t stream) {
   p.stride_a = batch > 1 ? a.stride_a : 0;
   p.stride_b = batch > 1 ? a.stride_b : 0;
   p.stride_c = batch > 1 ? a.stride_c : 0;
+  p.status = a.status;
   p.vec = (reinterpret_cast<uintptr_t>(a.A) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.B) & 15) == 0 &&
           p.lda % 4 == 0 && p.ldb % 4 == 0 && p.stride_a % 4 == 0 && p.stride_b % 4 == 0;
   const dim3 grid((a.N + kTyT - 1) / kTyT, (a.M + kTyT - 1) / kTyT, batch);

@@ -38,6 +38,7 @@ struct LaunchArgs {
   float* ws;
   unsigned int* flags;
   unsigned int epoch;
+  int64_t ws_slots;      // stream-K: partial tiles (and flags) ws holds; gemv: floats ws holds
   unsigned int* status;  // per-device status word (error bits)
   uint64_t timeout_ns;   // limit for every in-kernel wait
   // split-TF32 tensor-core variants: A_hi, A_lo (M x split_ld), then B_hi,

@@ -19,6 +19,7 @@
 
 #include "api_internal.h"
 #include "kernel_gemv.h"
+#include "checked.cuh"
 #include "kernels.h"
 #include "sgemm.h"
 
@@ -46,6 +47,7 @@ struct sgemm_plan_s {
   int64_t sk_iters;
   float* ws;
   unsigned int* flags;
+  int64_t ws_slots;  // what ws holds: partial tiles (and flags) for stream-K, floats for gemv
   std::atomic<unsigned int> epoch;
   // split-TF32 tensor-core variants: operand buffer and its four tensor maps
   float* tc_split;
@@ -441,6 +443,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   p->dp_waves = 0;
   p->sk_iters = 0;
   p->ws = nullptr;
+  p->ws_slots = 0;
   p->flags = nullptr;
   p->epoch.store(0);
   p->tc_split = nullptr;
@@ -475,6 +478,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       p->dp_waves = sk.dp_waves;
       p->sk_iters = sk.sk_iters;
       const size_t ws_bytes = static_cast<size_t>(slots) * v->bm * v->bn * sizeof(float);
+      p->ws_slots = slots;
       if (cudaMalloc(reinterpret_cast<void**>(&p->ws), ws_bytes) != cudaSuccess ||
           cudaMalloc(reinterpret_cast<void**>(&p->flags), static_cast<size_t>(slots) * sizeof(unsigned int)) !=
               cudaSuccess ||
@@ -492,6 +496,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
     if (units > 0) {
       p->sk_iters = units;
       const size_t ws_bytes = static_cast<size_t>(grid) * v->bm * v->bn * sizeof(float);
+      p->ws_slots = grid;
       if (cudaMalloc(reinterpret_cast<void**>(&p->ws), ws_bytes) != cudaSuccess ||
           cudaMalloc(reinterpret_cast<void**>(&p->flags), static_cast<size_t>(grid) * sizeof(unsigned int)) !=
               cudaSuccess ||
@@ -512,6 +517,7 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       if (floats > kMaxSpan) return fail(SGEMM_ERR_UNSUPPORTED);
       const size_t ws_bytes =
           static_cast<size_t>(std::max<int64_t>(batch, 1)) * p->split * M * ((N + 3) / 4 * 4) * sizeof(float);
+      p->ws_slots = static_cast<int64_t>(ws_bytes / sizeof(float));
       if (cudaMalloc(reinterpret_cast<void**>(&p->ws), ws_bytes) != cudaSuccess) return fail(SGEMM_ERR_CUDA);
     }
   } else if (v->kind == kKindTc) {
@@ -1079,6 +1085,7 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
   a.stride_c = p->stride_c;
   if (v->kind == kKindGemv) {
     a.ws = p->ws;
+    a.ws_slots = p->ws_slots;
     if (p->ex_native_tb) a.ldb = p->ex_ldb;  // read as stored (N x K)
   }
   if (v == reg.all[p->config_id] && p->sk_iters > 0) {
@@ -1086,6 +1093,7 @@ sgemm_status_t sgemm_run(sgemm_plan_t plan, float alpha, const float* A, const f
     a.sk_iters = p->sk_iters;
     a.ws = p->ws;
     a.flags = p->flags;
+    a.ws_slots = p->ws_slots;
     // each run publishes under a new epoch, so flags need no reset --
     // except when the counter wraps: then a flag may hold any earlier
     // value, so clear them all and start again from 1
@@ -1296,6 +1304,7 @@ const char* sgemm_status_string(sgemm_status_t s) {
     case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: a CUDA call failed";
     case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a kernel wait ran past its time limit";
     case SGEMM_ERR_NOMEM: return "SGEMM_ERR_NOMEM: host allocation failed";
+    case SGEMM_ERR_BOUNDS: return "SGEMM_ERR_BOUNDS: a device-side bounds check of the checked build failed";
   }
   return "unknown sgemm status";
 }
@@ -1312,6 +1321,7 @@ sgemm_status_t sgemm_device_status(int reset) {
   if (reset && v != 0) {
     if (cudaMemset(addr, 0, sizeof(v)) != cudaSuccess) return SGEMM_ERR_CUDA;
   }
+  if (v & kStatusBounds) return SGEMM_ERR_BOUNDS;
   return v ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
 }
 

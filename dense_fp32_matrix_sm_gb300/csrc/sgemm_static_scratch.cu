@@ -158,6 +158,7 @@ extern "C" sgemm_status_t sgemm_run_static_scratch(int64_t M, int64_t N, int64_t
     a.dp_waves = sk.dp_waves;
     a.sk_iters = sk.sk_iters;
     a.ws = s->ws;
+    a.ws_slots = SGEMM_STATIC_SCRATCH_MAX_CTAS;
     a.flags = s->flags;
     unsigned int e = s->epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
     if (e == 0u) {

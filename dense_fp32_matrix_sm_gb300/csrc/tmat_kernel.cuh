@@ -64,6 +64,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "checked.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tile_order.cuh"
@@ -85,6 +86,7 @@ struct Params {
   int64_t sk_iters;      // k-slices of tiles [dp_waves*grid, tiles), split evenly over the CTAs
   float* ws;             // one partial tile per CTA
   unsigned int* flags;   // flags[b] == epoch: CTA b's partial tile is published
+  int64_t ws_slots;      // partial tiles (and flags) the workspace holds (checked build)
   unsigned int epoch;
   // strided batch: tiles are numbered batch-outermost; A and B come through
   // 3-D tensor maps (batch = the third coordinate), C is offset by stride_c
@@ -278,10 +280,13 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
 #pragma unroll
     for (int q = q0; q < q1; ++q) {
       const int chunk = (S::kKPart / 4) * th + q;  // k = 4*chunk .. +3
-      const float4 v = *reinterpret_cast<const float4*>(As + ((chunk ^ (tr & 7)) << 2));
+      const int src = tr * BK + ((chunk ^ (tr & 7)) << 2);
+      const float4 v = SG_CHK(SG_IN(src + 3, BM * BK), p.status) ? *reinterpret_cast<const float4*>(As - tr * BK + src)
+                                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
       const float e4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) At[(4 * chunk + u) * BM + at_col] = e4[u];
+      for (int u = 0; u < 4; ++u)
+        if (SG_CHK(SG_IN((4 * chunk + u) * BM + at_col, BK * BM), p.status)) At[(4 * chunk + u) * BM + at_col] = e4[u];
     }
     return true;
   };
@@ -357,13 +362,13 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
         const int f = S::kSwz * (k / S::kKPart);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          if constexpr (AT)
-            ap[i] = *reinterpret_cast<const float2*>(At + k * BM + a_lo0 + 16 * i);
-          else
-            ap[i] = *reinterpret_cast<const float2*>(At + k * BM + ((f & 15) ? a_lo8 : a_lo0) + 16 * (i ^ (f >> 4)));
+          const int ai = AT ? k * BM + a_lo0 + 16 * i : k * BM + ((f & 15) ? a_lo8 : a_lo0) + 16 * (i ^ (f >> 4));
+          ap[i] = SG_CHK(SG_IN(ai + 1, BK * BM), p.status) ? *reinterpret_cast<const float2*>(At + ai)
+                                                           : make_float2(0.f, 0.f);
         }
-        b0 = Bs4[k * (BN / 4)];
-        b1 = Bs4[k * (BN / 4) + 4];
+        const int bi = k * (BN / 4) + (wn * 32 + 4 * c) / 4;  // Bs4 starts at float4 (wn * 32 + 4c) / 4
+        b0 = SG_CHK(SG_IN(bi, BK * BN / 4), p.status) ? Bs4[k * (BN / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+        b1 = SG_CHK(SG_IN(bi + 4, BK * BN / 4), p.status) ? Bs4[k * (BN / 4) + 4] : make_float4(0.f, 0.f, 0.f, 0.f);
       };
       float2 apn[4];
       float4 b0n, b1n;
@@ -431,12 +436,13 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
 #pragma unroll
       for (int q = 0; q < kQ; ++q) {
         const int i = q >> 2, j2 = 2 * (q & 3);
-        ws4[(static_cast<int64_t>(b) * kQ + q) * S::kThreads + threadIdx.x] =
-            make_float4(acc[i][j2].x, acc[i][j2].y, acc[i][j2 + 1].x, acc[i][j2 + 1].y);
+        const int64_t wi = (static_cast<int64_t>(b) * kQ + q) * S::kThreads + threadIdx.x;
+        if (SG_CHK(SG_IN(wi, p.ws_slots * (BM * BN / 4)), p.status))
+          ws4[wi] = make_float4(acc[i][j2].x, acc[i][j2].y, acc[i][j2 + 1].x, acc[i][j2 + 1].y);
       }
       __threadfence();
       __syncthreads();
-      if (threadIdx.x == 0) ptx::st_release_gpu(p.flags + b, p.epoch);
+      if (threadIdx.x == 0 && SG_CHK(SG_IN(b, p.ws_slots), p.status)) ptx::st_release_gpu(p.flags + b, p.epoch);
       continue;
     }
     if (seg_k0 > 0) {  // finisher of a shared tile: wait for the contributors, add them in CTA order
@@ -445,6 +451,7 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
       bool timed_out = false;
       if (threadIdx.x == 0) {
         for (int c = c_first; c < b && !timed_out; ++c) {
+          if (!SG_CHK(SG_IN(c, p.ws_slots), p.status)) continue;
           if (ptx::ld_acquire_gpu(p.flags + c) == p.epoch) continue;
           const uint64_t t0 = ptx::globaltimer_ns();
           while (ptx::ld_acquire_gpu(p.flags + c) != p.epoch) {
@@ -464,7 +471,9 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
 #pragma unroll
         for (int q = 0; q < kQ; ++q) {
           const int i = q >> 2, j2 = 2 * (q & 3);
-          const float4 v = __ldcg(&ws4[(static_cast<int64_t>(c) * kQ + q) * S::kThreads + threadIdx.x]);
+          const int64_t wi = (static_cast<int64_t>(c) * kQ + q) * S::kThreads + threadIdx.x;
+          const float4 v = SG_CHK(SG_IN(wi, p.ws_slots * (BM * BN / 4)), p.status) ? __ldcg(&ws4[wi])
+                                                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
           acc[i][j2].x += v.x;
           acc[i][j2].y += v.y;
           acc[i][j2 + 1].x += v.z;
@@ -475,7 +484,8 @@ __global__ void __launch_bounds__(Shape<BM_, BN, STAGES>::kThreads, MINB)
       // (a replayed graph included, whose epoch is fixed) starts from zero
       __syncthreads();
       if (threadIdx.x == 0)
-        for (int c = c_first; c < b; ++c) *reinterpret_cast<volatile unsigned int*>(p.flags + c) = 0u;
+        for (int c = c_first; c < b; ++c)
+          if (SG_CHK(SG_IN(c, p.ws_slots), p.status)) *reinterpret_cast<volatile unsigned int*>(p.flags + c) = 0u;
     }
 
     // ---------------- epilogue ----------------
@@ -601,6 +611,7 @@ struct Variant_ {
     p.sk_iters = a.sk_iters;
     p.ws = a.ws;
     p.flags = a.flags;
+    p.ws_slots = a.ws_slots;
     p.epoch = a.epoch;
     p.batch = a.batch > 1 ? a.batch : 1;
     p.stride_c = a.stride_c;

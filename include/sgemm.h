@@ -91,7 +91,8 @@ typedef enum {
     SGEMM_ERR_UNSUPPORTED = -2,  /* valid but outside what this build handles */
     SGEMM_ERR_CUDA = -3,         /* a CUDA runtime or driver call failed */
     SGEMM_ERR_TIMEOUT = -4,      /* a kernel wait ran past its time limit */
-    SGEMM_ERR_NOMEM = -5         /* host allocation failed */
+    SGEMM_ERR_NOMEM = -5,        /* host allocation failed */
+    SGEMM_ERR_BOUNDS = -6        /* checked build only: a kernel index failed its bounds check */
 } sgemm_status_t;
 
 /*
@@ -367,7 +368,10 @@ const char *sgemm_status_string(sgemm_status_t status);
 /*
  * Read (and with reset != 0, clear) the current device's kernel status
  * word.  Synchronises the device.  Returns SGEMM_OK, SGEMM_ERR_TIMEOUT if a
- * kernel wait ran out since the last reset, or SGEMM_ERR_CUDA.
+ * kernel wait ran out since the last reset, SGEMM_ERR_BOUNDS if (in the
+ * checked build, libsgemm_gb300_checked.so, compiled with -DSGEMM_CHECKED)
+ * a kernel's shared-memory or workspace index failed its bounds check and
+ * the access was skipped, or SGEMM_ERR_CUDA.
  */
 sgemm_status_t sgemm_device_status(int reset);
 

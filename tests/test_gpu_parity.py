@@ -28,9 +28,13 @@ _bound = oracle.acceptance_bound
 def sg():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    import os
+
     from dense_fp32_matrix_sm_gb300 import build as b
 
-    b.build()
+    # SGEMM_GB300_LIBRARY=checked: these tests run against the checked build
+    # (tests/test_zy_checked_build.py), whose bounds failures show in device_status()
+    b.build(checked=os.environ.get("SGEMM_GB300_LIBRARY") == "checked")
     import dense_fp32_matrix_sm_gb300 as s
 
     s.lib()
