@@ -488,6 +488,37 @@ def sustained_leg(torch, step, flush, stream, w, seconds: float, rounds: int, sm
 
 
 TC_VARIANT = "tf32x3p_128x128x32_s3"
+
+
+def tf32_peak_tflops(torch, stream, n: int = 8192, reps: int = 10):
+    """The TF32 tensor-core rate measured with cuBLAS on this GPU: the best of
+    `reps` torch.matmul calls on n^3 float32 operands with TF32 allowed
+    (2 n^3 / time).  The denominator of the split-TF32 leg's roofline, as
+    MEASURED_PEAKS.json's cuBLAS bf16 figure is for bf16."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    try:
+        torch.backends.cuda.matmul.allow_tf32 = True
+        a = torch.randn(n, n, device="cuda")
+        b = torch.randn(n, n, device="cuda")
+        c = torch.empty(n, n, device="cuda")
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = None
+        for _ in range(reps):
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            torch.matmul(a, b, out=c)
+            s1.record(stream)
+            s1.synchronize()
+            t = s0.elapsed_time(s1)
+            best = t if best is None or t < best else best
+        del a, b, c
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except RuntimeError:
+        return None
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
 TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tensor rates, TF32 over BF16
 
 
@@ -521,15 +552,20 @@ def tc_leg(torch, sg, w, dA, dB, dC0, stream, flush, warmup, steps, dist, peaks)
     desc = plan.describe()
     plan.close()
     bf16 = peaks.get("bf16_tflops")
-    peak = round((bf16 if bf16 else 1900.0) * TF32_PER_BF16, 1)
+    derived = round((bf16 if bf16 else 1900.0) * TF32_PER_BF16, 1)
+    measured = tf32_peak_tflops(torch, stream)
+    peak = round(measured, 1) if measured else derived
     tensor_tflops = 3 * w.flops / (ms * 1e-3) / 1e12  # three TF32 products per FP32 multiply-add
     return {"variant": TC_VARIANT, "value": round(w.flops / (ms * 1e-3) / 1e9, 1), "unit": "GFLOP/s",
             "ms_per_step": round(ms, 4), "steps": steps, "gpu_launches": launches * steps,
             "k_order": "tf32x3", "max_abs_diff_vs_ffma_rel_to_max_abs_c": rel,
             "roofline": {"bound": "tensor", "achieved": round(tensor_tflops, 1), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(tensor_tflops / peak, 4), "traffic": None,
-                         "peak_basis": ("MEASURED_PEAKS.json bf16_tflops (burst) x nominal TF32/BF16 ratio 1.1/2.25 "
+                         "peak_basis": ("cuBLAS TF32 GEMM measured in this run: torch.matmul 8192^3 with allow_tf32, "
+                                        "best of 10, CUDA events (of measured)" if measured else
+                                        "MEASURED_PEAKS.json bf16_tflops (burst) x nominal TF32/BF16 ratio 1.1/2.25 "
                                         "(of measured)" if bf16 else "fallback 1.9 PF bf16 x 1.1/2.25 (of fallback)"),
+                         "peak_derived_from_bf16": derived,
                          "achieved_basis": "3 x 2MNK TF32 tensor FLOPs over the whole step (the two split kernels "
                                            "included)"},
             "plan": desc}

@@ -16,6 +16,12 @@ name):
   square4092   4092 x 4092 x 4092,    A,B ~ N(0,1), C0 ~ U[-1,1], seed 2, alpha 0.5, beta 3
   mlp          8192 x 14336 x 4096,   A ~ N(0,1), B ~ N(0,0.02),  seed 3, alpha 1,   beta 0
   decode16     16 x 16384 x 8192,     A ~ N(0,1), B ~ N(0,0.02), C0 ~ U[-1,1], seed 4, alpha 1, beta 1
+
+Two more measured beside them: decode1 (the one-token case of decode16:
+1 x 16384 x 8192, same distributions, seed 5) and square512 (512^3,
+A,B ~ U[-1,1], seed 6: a small problem between 128^3 and 4096^3, where a
+partial wave decides the speed -- "Writing a Fast Matmul in CUDA", "Size
+effects").
 """
 from __future__ import annotations
 
@@ -70,6 +76,7 @@ WORKLOADS: Dict[str, Workload] = {
                  1.0, 1.0),
         Workload("decode1", 1, 16384, 8192, ("normal", 1.0), ("normal", 0.02), ("uniform", 1.0), 5,
                  1.0, 1.0),
+        Workload("square512", 512, 512, 512, ("uniform", 1.0), ("uniform", 1.0), None, 6, 1.0, 0.0),
     )
 }
 
