@@ -223,15 +223,17 @@ bool gemv_shape(int64_t M, int64_t N, int64_t K, int64_t batch) {
 }
 
 // Products the table sends to the five-to-sixteen-row matrix-vector kernel
-// (gemv_16x1024): one product, B as stored, B of at least 16 MB (a stream
-// worth keeping at full bandwidth), any alignment and leading dimension.
-// Measured against the few-row stream-K kernel (L2 clean, median of 40):
-// 16 x 16384 x 8192 0.090 ms against 0.102; 8 x 16384 x 8192 0.084 against
-// 0.105; 12 x 8192 x 4096 0.037 against 0.039; 16 x 4096 x 4096 0.027
-// against 0.029.
+// (gemv_16x1024): B as stored, at least 16 MB of B over the batch (a stream
+// worth keeping at full bandwidth), any alignment, leading dimension or
+// batch stride.  Measured against the few-row stream-K kernel (L2 clean,
+// median of 30-40): 16 x 16384 x 8192 0.090 ms against 0.102; 8 x 16384 x
+// 8192 0.084 against 0.105; 12 x 8192 x 4096 0.037 against 0.039; 16 x 4096
+// x 4096 0.027 against 0.029; batches 8 x (16 x 8192 x 4096) 0.181 against
+// 0.284, 32 x (16 x 4096 x 1024) 0.115 against 0.125, 16 x (8 x 16384 x
+// 2048) 0.323 against 0.414, 64 x (12 x 4096 x 1024) 0.209 against 0.216.
 bool rows_shape(int64_t M, int64_t N, int64_t K, int64_t batch, int b_trans) {
-  return batch <= 1 && !b_trans && M > 4 && M <= 16 && N * K >= (int64_t(1) << 22) && N <= (int64_t(1) << 30) &&
-         K <= int64_t(65535) * 640;
+  return !b_trans && M > 4 && M <= 16 && std::max<int64_t>(batch, 1) * N * K >= (int64_t(1) << 22) &&
+         N <= (int64_t(1) << 30) && K <= int64_t(65535) * 640 && batch <= 65535;
 }
 
 // Products the tiny kernel takes from the table: more than 16 rows (fewer
@@ -288,9 +290,13 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
 // Measured on GB300 with stream-K (which removes the partial-wave loss once
 // there is at least one full wave, and with fewer tiles than CTA slots
 // splits every tile along K once every CTA gets a k-slice):
-//  * 128 x 256 tiles from one full wave of them on, with K >= 256 (eight or
-//    more k-slices per tile, the stream-K threshold): 66.3-69.6 TFLOP/s from
-//    2560^3 up, 1-2% above 128 x 128 (4096 x 4096 x 256: a tie);
+//  * 128 x 256 tiles from a third of a wave of them on (with stream-K
+//    splitting the tiles that do not fill a wave), K >= 256: 66.3-69.6
+//    TFLOP/s from 2560^3 up, 1-2% above 128 x 128; below a wave (measured
+//    against 128 x 128): 1280^3 53.9 vs 52.5, 1536^3 59.0 vs 58.0, 1792^3
+//    62.4 vs 58.5, 2048^3 65.5 vs 61.2, 2048 x 1024 x 2048 61.6 vs 59.1,
+//    2048 x 2048 x 512 53.8 vs 52.4; 1024 x 2048 x 1024 53.1 vs 53.8 and
+//    1152^3 (45 tiles) 42.7 vs 48.2 stay on the other side of the line;
 //  * 128 x 128 tiles down to half a wave (1536^3: 61.2 vs 56.2 for 128 x 64),
 //    or below that when every tile can be split along K: 1024^3 45.8 vs
 //    43.6, 512 x 512 x 8192 52.3 vs 49.8, 2048 x 640 x 2048 58.1 vs 53.4;
@@ -302,7 +308,7 @@ const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_
   const int64_t square_tiles = batch * ((M + 127) / 128) * ((N + 127) / 128);
   const int64_t narrow_tiles = batch * ((M + 127) / 128) * ((N + 63) / 64);
   const int64_t KT = (K + 31) / 32;
-  if (N > 128 && wide_tiles >= num_sms && K >= 256) return "tmat_128x256x32_s3_b1";
+  if (N > 128 && 3 * wide_tiles >= num_sms && K >= 256) return "tmat_128x256x32_s3_b1";
   // few tiles and a short k loop: 128 x 64 tiles split into three or more
   // pieces along K each (api_streamk_schedule) beat 128 x 128 tiles, whose
   // finishers add twice the bytes per contributor (512^3: 14.2 TFLOP/s

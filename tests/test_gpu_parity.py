@@ -656,8 +656,11 @@ def test_plan_ex_argument_errors(sg):
     (640, 1024, 256, 9, "tmat_128x256x32_s3_b1", False),  # 180 tiles: a stream-K tail over batches 7 and 8
     (640, 768, 256, 4, "tmat_128x128x32_s4_b1", True),  # A shared by every product (stride 0)
     (65, 33, 17, 9, "generic_64x64x16", False),
-    # few rows: the stream-K few-row kernel over (product, slab, k-slice) units
+    # few rows with 2^22 or more elements of B over the batch: the sixteen-row matrix-vector kernel
     (16, 1024, 512, 8, None, False),
+    (12, 2048, 700, 6, None, True),                     # ragged K, A shared
+    # fewer: the stream-K few-row kernel over (product, slab, k-slice) units
+    (16, 512, 256, 4, None, False),
     (7, 300, 520, 5, None, True),                       # ragged N and K, A shared
     (1, 4096, 256, 3, None, False),
 ])
@@ -683,7 +686,8 @@ def test_strided_batch(sg, oracle_mod, case):
     info = plan.info()
     assert info["batch"] == batch
     if config is None and M <= 16:
-        assert info["variant"].startswith("gemv" if M <= 4 else "skinny_sk"), info
+        expect = "gemv_4x512" if M <= 4 else "gemv_16x1024" if batch * N * K >= 1 << 22 else "skinny_sk"
+        assert info["variant"].startswith(expect), info
     plan.run(alpha, dA, dB, beta, dC)
     torch.cuda.synchronize()
     assert sg.device_status() == sg.SGEMM_OK
