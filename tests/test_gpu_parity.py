@@ -946,6 +946,46 @@ def test_sixteen_rows(sg, oracle_mod, shape, layout):
         assert_parity(C, Cref, S, K, f"rows16 {layout} {shape} split={info['split']} a={alpha} b={beta}")
 
 
+@pytest.mark.parametrize("shared_a", [False, True])
+def test_sixteen_rows_batched_any_stride(sg, oracle_mod, shared_a):
+    """gemv_16x1024 over a strided batch whose strides are not multiples of 4
+    (B's rows are then copied 4 bytes at a time) and whose A may be shared
+    (stride 0), product by product against the oracle; the padding between
+    the products' C untouched; bit-identical on a rerun."""
+    M, N, K, batch = 11, 1500, 700, 3
+    rng = np.random.default_rng(1611)
+    A = rng.standard_normal((batch, M, K), dtype=np.float32)
+    B = (rng.standard_normal((batch, K, N), dtype=np.float32) * np.float32(0.05)).astype(np.float32)
+    C0 = rng.uniform(-1, 1, (batch, M, N)).astype(np.float32)
+    sa = 0 if shared_a else M * K + 5
+    sb, sc = K * N + 3, M * N + 7
+    dA = torch.zeros(max(1, (0 if shared_a else batch - 1) * sa + M * K), device="cuda")
+    dB = torch.zeros((batch - 1) * sb + K * N, device="cuda")
+    dC = torch.zeros((batch - 1) * sc + M * N, device="cuda")
+    for z in range(batch):
+        if not shared_a or z == 0:
+            dA[z * sa: z * sa + M * K] = torch.from_numpy(A[z].ravel())
+        dB[z * sb: z * sb + K * N] = torch.from_numpy(B[z].ravel())
+        dC[z * sc: z * sc + M * N] = torch.from_numpy(C0[z].ravel())
+    c_init = dC.clone()
+    plan = sg.Plan(M, N, K, config="gemv_16x1024", batch=batch, stride_a=sa, stride_b=sb, stride_c=sc)
+    outs = []
+    for _ in range(2):
+        dC.copy_(c_init)
+        plan.run(-0.5, dA, dB, 2.0, dC)
+        torch.cuda.synchronize()
+        assert sg.device_status() == sg.SGEMM_OK
+        outs.append(dC.cpu().numpy().copy())
+    plan.close()
+    assert np.array_equal(outs[0], outs[1]), "not reproducible"
+    out = outs[0]
+    for z in range(batch):
+        Cref, S = oracle_mod.sgemm_ref(A[0 if shared_a else z], B[z], C0[z], -0.5, 2.0)
+        assert_parity(out[z * sc: z * sc + M * N].reshape(M, N), Cref, S, K, f"rows16 batch {z} shared_a={shared_a}")
+        if z + 1 < batch:
+            assert np.all(out[z * sc + M * N: (z + 1) * sc] == 0.0)
+
+
 def test_sixteen_rows_table_and_limits(sg):
     """The table sends one product of 5 to 16 rows with B as stored and 16 MB
     or more of B to gemv_16x1024 (no padding copy, even for odd ldb), B given
