@@ -59,6 +59,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 # The sources a variant family's kernel is built from: a traffic figure in
 # profiles/traffic.json stays valid while their hash is unchanged.
 KERNEL_SOURCES = {
+    "tmat_64x": ["tmat_kernel.cuh", "tmat_variants_rows.cu", "tile_order.cuh", "ptx.cuh", "kernels.h"],
     "tmat_": ["tmat_kernel.cuh", "tmat_variants.cu", "tile_order.cuh", "ptx.cuh", "kernels.h"],
     "skinny": ["kernel_skinny.cu", "ptx.cuh", "kernels.h"],
     "tma_": ["tma_kernel.cuh", "tma_variants_a.cu", "tma_variants_b.cu", "tma_variants_c.cu", "tile_order.cuh", "ptx.cuh",

@@ -86,6 +86,11 @@ struct sgemm_plan_s {
 // is looked up once per device with that device current.
 __device__ unsigned int g_sgemm_status_word;
 
+namespace sgemm {
+// the 64-row instantiations of the transposed-A kernel (tmat_variants_rows.cu)
+const Variant* tmat_rows_variants(int* count);
+}  // namespace sgemm
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -132,6 +137,8 @@ struct Registry {
     v = cpa_variants(&n);
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
     v = tmat_variants(&n);
+    for (int i = 0; i < n; ++i) all.push_back(&v[i]);
+    v = tmat_rows_variants(&n);
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
     v = tc_variants(&n);
     for (int i = 0; i < n; ++i) all.push_back(&v[i]);
@@ -238,15 +245,20 @@ bool rows_shape(int64_t M, int64_t N, int64_t K, int64_t batch, int b_trans) {
 
 // Products the tiny kernel takes from the table: more than 16 rows (fewer
 // go to the few-row kernels, which do not fill 32-row tiles with padding),
-// K <= 512 and at most two of its 32 x 32 tiles per SM (over the whole
-// batch).  Measured against the
-// 128-row kernels and cuBLAS (TFLOP/s, L2 flushed): 128^3 0.52 (cuBLAS
-// 0.42), 256^3 3.4 (2.5), 384^3 11.0 (6.9), 512 x 512 x 128 6.7 (6.0),
-// 200 x 130 x 100 with odd ldb 0.63 (0.56); at 512^3 it ties the split
-// 128 x 64 tiles (14.6 against 14.4).
-bool tiny_shape(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms) {
-  return M > 16 && K <= 512 &&
-         std::max<int64_t>(batch, 1) * ((M + 31) / 32) * ((N + 31) / 32) <= 2 * static_cast<int64_t>(num_sms);
+// and either K <= 512 with at most two of its 32 x 32 tiles per SM (over
+// the whole batch: one wave), or at most 32 rows with rows that allow its
+// 16-byte copies (`rows16`: lda, ldb multiples of 4) and at least 3/4 of a
+// tile per SM (it does not split K).  Measured against the 128-row kernels
+// and cuBLAS (TFLOP/s, L2 flushed): 128^3 0.54 (cuBLAS 0.41), 256^3 4.1
+// (2.7), 384^3 11.1 (7.5), 512^3 18.8 (14.4), 512 x 512 x 128 8.2 (6.3),
+// 608 x 512 x 512 22.2 (16.9), 200 x 130 x 100 with odd ldb 0.64 (0.59);
+// 32 x 4096 x 4096 21.9 (128 x 128 tiles 11.6, cuBLAS 16.6), 24 x 8192 x
+// 4096 21.3 (10.9, 15.7), 32 x 9728 x 1024 26.0 (12.3, 20.8).
+bool tiny_shape(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, bool rows16) {
+  const int64_t tiles = std::max<int64_t>(batch, 1) * ((M + 31) / 32) * ((N + 31) / 32);
+  if (M <= 16) return false;
+  if (K <= 512) return tiles <= 2 * static_cast<int64_t>(num_sms);
+  return rows16 && M <= 32 && 4 * tiles >= 3 * static_cast<int64_t>(num_sms);
 }
 
 // a_span / b_span: elements one stored A / B spans (-1: M*lda / K*ldb, an
@@ -255,8 +267,8 @@ bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t
                       int64_t batch = 1, int64_t stride_a = 0, int64_t stride_b = 0, int64_t a_span = -1,
                       int64_t b_span = -1) {
   if (v->kind == kKindGemv) return gemv_takes(v, M, N, K, batch);
-  // whole K-panels in shared memory; tiles on grid x (columns) and y (rows)
-  if (v->kind == kKindTiny) return K <= v->bk && batch <= 65535 && (M + v->bm - 1) / v->bm <= 65535;
+  // K streamed through a shared-memory ring; tiles on grid x (columns) and y (rows)
+  if (v->kind == kKindTiny) return batch <= 65535 && (M + v->bm - 1) / v->bm <= 65535;
   if (batch > 1) {
     if (!v->batched) return false;
     if (v->kind == kKindGeneric) return batch <= 65535;
@@ -308,6 +320,13 @@ const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_
   const int64_t square_tiles = batch * ((M + 127) / 128) * ((N + 127) / 128);
   const int64_t narrow_tiles = batch * ((M + 127) / 128) * ((N + 63) / 64);
   const int64_t KT = (K + 31) / 32;
+  // up to 64 rows: 64-row tiles, so at most half of a tile is padding (the
+  // 128-row tiles' is three quarters at 32 rows).  Measured (TFLOP/s, L2
+  // flushed; 128-row table choice, cuBLAS): 64 x 16384 x 8192 62.6 (33.7,
+  // 55.9), 64 x 4096 x 4096 41.6 (23.3, 21.0), 48 x 4096 x 4096 31.2 (17.4,
+  // 15.7), 64 x 9728 x 2048 47.5 (27.5, 41.5), 64 x 8192 x 8192 51.0 (30.6,
+  // 37.8), 32 x 16384 x 8192 31.4 (16.8, 38.4)
+  if (M <= 64) return "tmat_64x256x32_s3_b1";
   if (N > 128 && 3 * wide_tiles >= num_sms && K >= 256) return "tmat_128x256x32_s3_b1";
   // few tiles and a short k loop: 128 x 64 tiles split into three or more
   // pieces along K each (api_streamk_schedule) beat 128 x 128 tiles, whose
@@ -332,8 +351,8 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   // five to sixteen rows of one product, B as stored: B streamed once
   // through per-warp cp.async rings, any layout
   if (rows_shape(M, N, K, batch, b_trans)) return "gemv_16x1024";
-  // tiny products: whole K-panels in shared memory, any layout
-  if (tiny_shape(M, N, K, batch, num_sms)) return "tiny_32x32";
+  // tiny products, and long-K products of 17 to 32 rows: 32 x 32 tiles, any layout
+  if (tiny_shape(M, N, K, batch, num_sms, lda % 4 == 0 && ldb % 4 == 0)) return "tiny_32x32";
   if (batch > 1) {
     // Strided batches run on the batched variants only: the transposed-A
     // family when TMA can take the layout (tile counts over the whole batch),
@@ -395,7 +414,8 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       // rows (one cudaMemcpy2DAsync), so the table's TMA kernels can read it:
       // measured at 4096^3, lda = 4097 ran 54.6 TFLOP/s on the cp.async kernel
       // and ldb = 4097 29.8 on the scalar-load kernel, against 68.8 aligned.
-      if (batch <= 1 && K > 0 && !gemv_shape(M, N, K, batch) && !tiny_shape(M, N, K, batch, sms) &&
+      if (batch <= 1 && K > 0 && !gemv_shape(M, N, K, batch) &&
+          !tiny_shape(M, N, K, batch, sms, lda % 4 == 0 && ldb % 4 == 0) &&
           !rows_shape(M, N, K, batch, b_trans) &&
           static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= 16777216.0) {
         rp_a = lda % 4 != 0;

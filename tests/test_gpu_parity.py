@@ -225,6 +225,67 @@ def test_leading_dimensions(sg, oracle_mod, lds, shape):
         assert used.startswith("cpa")          # A copied 4 bytes at a time: any lda
 
 
+@pytest.mark.parametrize("shape", [(32, 32, 256), (31, 33, 257), (100, 70, 511), (64, 96, 512), (512, 512, 512),
+                                   (45, 200, 300)])
+def test_tiny_k_chunks(sg, oracle_mod, shape):
+    # K up to 256 is one staged chunk, K in (256, 512] two; 16-byte copies,
+    # then 4-byte copies (odd lda), and a strided batch of the same shape
+    M, N, K = shape
+    A, B, C0 = make_inputs(M, N, K, seed=M * 7 + K, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
+    for lda, alpha, beta in ((K + (-K) % 4, 1.0, 0.0), (K + 1, -0.5, 2.0)):
+        C, used = run_gpu(sg, A, B, C0, alpha, beta, config="tiny_32x32", lda=lda)
+        Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
+        assert_parity(C, Cref, S, K, f"tiny {shape} lda={lda}")
+        C2, _ = run_gpu(sg, A, B, C0, alpha, beta, config="tiny_32x32", lda=lda)
+        assert np.array_equal(C, C2)
+    if M * N <= 64 * 96:
+        batch = 3
+        As = np.stack([A * (z + 1) for z in range(batch)])
+        Bs = np.stack([B - z for z in range(batch)])
+        Cs0 = np.stack([C0 + z for z in range(batch)])
+        dA, dB, dC = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (As, Bs, Cs0))
+        plan = sg.Plan(M, N, K, config="tiny_32x32", batch=batch, stride_a=M * K, stride_b=K * N, stride_c=M * N)
+        try:
+            plan.run(1.0, dA, dB, 1.0, dC)
+            torch.cuda.synchronize()
+            assert sg.device_status() == 0
+        finally:
+            plan.close()
+        out = dC.cpu().numpy()
+        for z in range(batch):
+            Cref, S = oracle_mod.sgemm_ref(As[z], Bs[z], Cs0[z], 1.0, 1.0)
+            assert_parity(out[z], Cref, S, K, f"tiny batch {z} {shape}")
+
+
+@pytest.mark.parametrize("case", [
+    # (M, N, K, the table's variant): 17 to 64 rows past the tiny kernel's K <= 512 range
+    (32, 4096, 4096, "tiny_32x32"),        # 128 tiles of 32 x 32: K streamed, no split
+    (30, 4000, 700, "tiny_32x32"),
+    (20, 3000, 2000, "tmat_64x256x32_s3_b1"),  # 94 tiles: too few for the tiny kernel, which does not split K
+    (48, 4096, 4096, "tmat_64x256x32_s3_b1"),
+    (64, 1000, 1500, "tmat_64x256x32_s3_b1"),  # ragged N and K
+    (40, 700, 3001, "tmat_64x256x32_s3_b1"),
+    (65, 4096, 4096, None),                # more than 64 rows: the 128-row tiles
+])
+def test_seventeen_to_sixtyfour_rows(sg, oracle_mod, case):
+    M, N, K, expect = case
+    plan = sg.Plan(M, N, K)
+    used = plan.info()["variant"]
+    plan.close()
+    if expect is None:
+        assert used.startswith("tmat_128"), used
+    else:
+        assert used == expect, (used, expect)
+    A, B, C0 = make_inputs(M, N, K, seed=M + N + K, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
+    for alpha, beta in ((1.0, 0.0), (0.5, -2.0)):
+        C, used2 = run_gpu(sg, A, B, C0, alpha, beta)
+        assert used2 == used
+        Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
+        assert_parity(C, Cref, S, K, f"{used} {case} a={alpha} b={beta}")
+    C2, _ = run_gpu(sg, A, B, C0, 0.5, -2.0)
+    assert np.array_equal(C, C2)
+
+
 @pytest.mark.parametrize("offs", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (2, 3, 1)])
 def test_misaligned_pointers(sg, oracle_mod, offs):
     M, N, K = 140, 260, 96
@@ -656,6 +717,9 @@ def test_plan_ex_argument_errors(sg):
     (640, 1024, 256, 9, "tmat_128x256x32_s3_b1", False),  # 180 tiles: a stream-K tail over batches 7 and 8
     (640, 768, 256, 4, "tmat_128x128x32_s4_b1", True),  # A shared by every product (stride 0)
     (65, 33, 17, 9, "generic_64x64x16", False),
+    # up to 64 rows with a long k loop: 64-row tiles over the batch; 17 to 32 rows: 32 x 32 tiles
+    (48, 2048, 1024, 3, None, False),
+    (24, 1024, 2048, 5, None, True),
     # few rows with 2^22 or more elements of B over the batch: the sixteen-row matrix-vector kernel
     (16, 1024, 512, 8, None, False),
     (12, 2048, 700, 6, None, True),                     # ragged K, A shared
