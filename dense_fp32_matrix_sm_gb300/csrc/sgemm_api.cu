@@ -327,7 +327,15 @@ const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_
   // 15.7), 64 x 9728 x 2048 47.5 (27.5, 41.5), 64 x 8192 x 8192 51.0 (30.6,
   // 37.8), 32 x 16384 x 8192 31.4 (16.8, 38.4)
   if (M <= 64) return "tmat_64x256x32_s3_b1";
-  if (N > 128 && 3 * wide_tiles >= num_sms && K >= 256) return "tmat_128x256x32_s3_b1";
+  // 128 x 256 tiles from 0.3 of a wave on (20 wide tiles per 6 SMs), unless
+  // the last column of tiles would be mostly empty below N = 4096 (1408^3:
+  // 51.4 TFLOP/s against 55.6 on 128 x 128), or a 256-deep k loop with less
+  // than 3/4 of a wave (1536 x 1536 x 256: 34.3 against 39.3; 2048 x 1024 x
+  // 256: 30.2 against 36.7; 2048^2 x 256 with a whole wave: 45.6 against 43.7)
+  const bool wide_fits = N % 256 == 0 || N % 256 > 128 || N >= 4096;
+  if (N > 128 && wide_fits && 20 * wide_tiles >= 6 * num_sms && K >= 256 &&
+      (K >= 512 || 4 * wide_tiles >= 3 * num_sms))
+    return "tmat_128x256x32_s3_b1";
   // few tiles and a short k loop: 128 x 64 tiles split into three or more
   // pieces along K each (api_streamk_schedule) beat 128 x 128 tiles, whose
   // finishers add twice the bytes per contributor (512^3: 14.2 TFLOP/s
