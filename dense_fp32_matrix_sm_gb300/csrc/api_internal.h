@@ -28,7 +28,10 @@ uint64_t api_wait_timeout_ns(int64_t M, int64_t N, int64_t K, int sms);
 // The persistent grid of a transposed-A plan over `tiles` C tiles of KT
 // k-slices, SMs x CTAs per SM resident: full waves data-parallel and, when
 // stream-K is allowed, the last partial wave split along K (dp_waves full
-// waves, then sk_iters k-slices shared by the grid).  Pure host arithmetic.
+// waves, then sk_iters k-slices shared by the grid).  A split always gives
+// every CTA at least one k-slice (sk_iters >= grid): the kernel's finishers
+// wait on every CTA between the first one holding a slice of their tile and
+// themselves.  Pure host arithmetic.
 struct StreamKSchedule {
   int64_t grid;
   int dp_waves;

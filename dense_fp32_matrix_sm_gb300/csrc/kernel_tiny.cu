@@ -1,34 +1,38 @@
-// kernel_tiny.cu -- SGEMM for tiny products: small C tiles, K streamed
-// through a shared-memory ring (any K).
+// kernel_tiny.cu -- SGEMM for tiny and small products: small square C
+// tiles, K streamed through a shared-memory ring (any K).
 //
 // At 128^3 a product is 4 MFLOP, a few microseconds of one SM: the time
 // goes to the launch, to the round trips that bring A and B in, and to how
 // many SMs share the work ("Writing a Fast Matmul in CUDA, Step by Step",
 // "Size effects": small sizes leave most of the machine idle; the remedy
 // is more, smaller pieces of work).  The 128-row tiles of the main kernels
-// give 128^3 two CTAs.  Here:
-//  * A CTA owns a 32 x 32 tile of C and all of K.  K goes through a ring
-//    of kTyStages chunks of 64 k: the A panel (32 x 64) and the B panel
-//    (64 x 32) of a chunk are copied with cp.async -- 16-byte copies when
-//    both operands' rows allow them, coalesced 4-byte copies otherwise (any
+// give 128^3 two CTAs.  Here (template on the tile side T = 32 or 64):
+//  * A CTA owns a T x T tile of C and all of K.  K goes through a ring of
+//    STAGES chunks of 64 k: the A panel (T x 64) and the B panel (64 x T)
+//    of a chunk are copied with cp.async -- 16-byte copies when both
+//    operands' rows allow them, coalesced 4-byte copies otherwise (any
 //    alignment and leading dimension) -- one commit group per chunk, the
-//    first kTyStages - 1 chunks before any math, so their round trips
-//    overlap each other and the math.  82 KB per CTA: two CTAs per SM, so
-//    up to 2 x SMs tiles run in one wave.
+//    first STAGES - 1 chunks before any math, so their round trips overlap
+//    each other and the math.  One CTA barrier per chunk.
 //  * 256 threads in four k-groups of 64.  Group g takes the k-quads
 //    q = g, g + 4, ... (interleaved, so every group has work for any K);
-//    a thread of a group holds 4 rows (ty + 8i) x 4 columns.  Per k-quad:
-//    four 16-byte reads of A (one per row, four k) and four of B (one per
-//    k, four columns), then 32 FFMA2: a broadcast A element times a pair
-//    of adjacent B columns (each half an IEEE fma, so the sums are those
-//    of fmaf).  The A rows' smem stride (68 words, 4 mod 8) puts the four
-//    rows a warp reads at once in different banks.
-//  * The four groups' partial tiles go to shared memory and every thread
-//    finishes four outputs, adding the groups in order 0..3 -- a fixed
-//    order, so reruns are bit-identical (k_order=split) -- then alpha*sum
-//    (beta == 0, C not read) or fmaf(alpha, sum, beta*C).
+//    a thread of a group holds T/8 rows (ty + 8i) x T/8 columns (4 tx + 32h
+//    + j), read KSTEP k at a time: per step one KSTEP-wide read of A per
+//    row and two... T/32 16-byte reads of B per k, then FFMA2s, each a
+//    broadcast A element times a pair of adjacent B columns (each half an
+//    IEEE fma, so the sums are those of fmaf).  The A rows' stride in a
+//    stage (68 words, 4 mod 8) puts the four rows a warp reads at once in
+//    different banks.
+//  * The four groups' partial tiles go to shared memory (over the ring,
+//    which is idle by then) and every thread finishes T*T/256 outputs,
+//    adding the groups in order 0..3 -- a fixed order, so reruns are
+//    bit-identical (k_order=split) -- then alpha*sum (beta == 0, C not
+//    read) or fmaf(alpha, sum, beta*C).
 //  * Rows past M, columns past N and k past K are zero-filled and never
 //    stored.  Strided batches run on grid z.
+//  * tiny_32x32: 4 stages, 66 KB, KSTEP 4; small_64x64: 3 stages, 99 KB,
+//    KSTEP 2 (so that 64 accumulators and the operands fit 128 registers:
+//    two CTAs per SM).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -38,17 +42,22 @@
 namespace sgemm {
 namespace {
 
-constexpr int kTyT = 32;       // tile rows and columns
-constexpr int kTyGroups = 4;   // k-groups
+constexpr int kTyGroups = 4;  // k-groups
 constexpr int kTyGroupThreads = 64;
 constexpr int kTyThreads = kTyGroups * kTyGroupThreads;
-constexpr int kTyChunk = 64;                 // k per ring stage (16 k-quads: 4 per group)
-constexpr int kTyStages = 4;
-constexpr int kTyKa = kTyChunk + 4;          // A row stride in a stage (floats), 4 mod 8
-constexpr int kTyStageA = kTyT * kTyKa;      // floats
-constexpr int kTyStage = kTyStageA + kTyChunk * kTyT;
-constexpr int kTySmemFloats = kTyStages * kTyStage + kTyGroups * kTyT * kTyT;
-static_assert(kTyKa % 8 == 4 && kTyStageA % 4 == 0 && kTyStage % 4 == 0, "16-byte rows, conflict-free A reads");
+constexpr int kTyChunk = 64;       // k per ring stage (16 k-quads: 4 per group)
+constexpr int kTyKa = kTyChunk + 4;  // A row stride in a stage (floats), 4 mod 8
+static_assert(kTyKa % 8 == 4, "conflict-free A reads");
+
+template <int T, int STAGES>
+struct TyShape {
+  static constexpr int kStageA = T * kTyKa;            // floats
+  static constexpr int kStage = kStageA + kTyChunk * T;
+  static constexpr int kSmemFloats = STAGES * kStage;
+  static constexpr int kSmemBytes = kSmemFloats * static_cast<int>(sizeof(float));
+  static_assert(kStageA % 4 == 0 && kStage % 4 == 0, "16-byte rows");
+  static_assert(kSmemFloats >= kTyGroups * T * T, "the partial tiles fit over the ring");
+};
 
 struct TinyParams {
   const float* A;
@@ -61,8 +70,6 @@ struct TinyParams {
   int vec;  // 16-byte copies: A, B 16-byte aligned, lda, ldb, strides multiples of 4
   unsigned int* status;  // per-device status word (checked build: bounds)
 };
-
-constexpr int kTySmemBytes = kTySmemFloats * static_cast<int>(sizeof(float));
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -86,13 +93,31 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
 }
 
-__global__ void __launch_bounds__(kTyThreads) sgemm_tiny_kernel(const TinyParams p) {
+template <int KSTEP>
+struct AVec;
+template <>
+struct AVec<4> {
+  using type = float4;
+  __device__ static float at(const float4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+};
+template <>
+struct AVec<2> {
+  using type = float2;
+  __device__ static float at(const float2& v, int i) { return i == 0 ? v.x : v.y; }
+};
+
+template <int T, int STAGES, int KSTEP, int MINB>
+__global__ void __launch_bounds__(kTyThreads, MINB) sgemm_tiny_kernel(const TinyParams p) {
+  using S = TyShape<T, STAGES>;
+  constexpr int RPT = T / 8;   // rows per thread: ty + 8i
+  constexpr int HN = T / 32;   // column quads per thread: 4 tx + 32h
+  constexpr int TQ = T / 4;    // column quads per tile row
+  using AV = typename AVec<KSTEP>::type;
   extern __shared__ __align__(16) float ty_smem[];
   const int K = p.K;
   const int nchunks = (K + kTyChunk - 1) / kTyChunk;
-  float* part = ty_smem + kTyStages * kTyStage;  // [4 groups][32][32]
   const int z = blockIdx.z;
-  const int m0 = blockIdx.y * kTyT, n0 = blockIdx.x * kTyT;
+  const int m0 = blockIdx.y * T, n0 = blockIdx.x * T;
   const float* A = p.A + z * p.stride_a;
   const float* B = p.B + z * p.stride_b;
   float* C = p.C + z * p.stride_c;
@@ -100,168 +125,196 @@ __global__ void __launch_bounds__(kTyThreads) sgemm_tiny_kernel(const TinyParams
 
   // copy chunk c (k in [64c, 64c + 64)) into its ring stage; zeros outside the matrices
   auto issue = [&](int c) {
-    float* as = ty_smem + (c % kTyStages) * kTyStage;  // [32][kTyKa]
-    float* bs = as + kTyStageA;                        // [64][32]
+    const int so = (c % STAGES) * S::kStage;  // stage offset (floats)
+    float* as = ty_smem + so;                 // [T][kTyKa]
+    float* bs = as + S::kStageA;              // [64][T]
     const int c0 = c * kTyChunk;
     if (p.vec) {
 #pragma unroll
-      for (int u = 0; u < kTyT * kTyChunk / 4 / kTyThreads; ++u) {  // A: 32 rows x 16 quads
+      for (int u = 0; u < T * kTyChunk / 4 / kTyThreads; ++u) {  // A: T rows x 16 quads
         const int idx = t + u * kTyThreads;
         const int m = idx >> 4, kl = 4 * (idx & 15), k = c0 + kl;
         const uint32_t bytes = m0 + m < p.M && k < K ? (K - k >= 4 ? 16u : 4u * (K - k)) : 0u;
-        if (SG_CHK(SG_IN((c % kTyStages) * kTyStage + m * kTyKa + kl + 3, kTySmemFloats), p.status))
+        if (SG_CHK(SG_IN(so + m * kTyKa + kl + 3, S::kSmemFloats), p.status))
           cp_async16(as + m * kTyKa + kl, bytes ? A + static_cast<int64_t>(m0 + m) * p.lda + k : A, bytes);
       }
 #pragma unroll
-      for (int u = 0; u < kTyChunk * kTyT / 4 / kTyThreads; ++u) {  // B: 64 rows x 8 quads of columns
+      for (int u = 0; u < kTyChunk * T / 4 / kTyThreads; ++u) {  // B: 64 rows x T/4 quads of columns
         const int idx = t + u * kTyThreads;
-        const int kl = idx >> 3, n = 4 * (idx & 7), k = c0 + kl;
+        const int kl = idx / TQ, n = 4 * (idx % TQ), k = c0 + kl;
         const uint32_t bytes = k < K && n0 + n < p.N ? (p.N - n0 - n >= 4 ? 16u : 4u * (p.N - n0 - n)) : 0u;
-        if (SG_CHK(SG_IN((c % kTyStages) * kTyStage + kTyStageA + kl * kTyT + n + 3, kTySmemFloats), p.status))
-          cp_async16(bs + kl * kTyT + n, bytes ? B + static_cast<int64_t>(k) * p.ldb + n0 + n : B, bytes);
+        if (SG_CHK(SG_IN(so + S::kStageA + kl * T + n + 3, S::kSmemFloats), p.status))
+          cp_async16(bs + kl * T + n, bytes ? B + static_cast<int64_t>(k) * p.ldb + n0 + n : B, bytes);
       }
     } else {
 #pragma unroll 4
-      for (int u = 0; u < kTyT * kTyChunk / kTyThreads; ++u) {  // A: along rows (coalesced)
+      for (int u = 0; u < T * kTyChunk / kTyThreads; ++u) {  // A: along rows (coalesced)
         const int idx = t + u * kTyThreads;
         const int m = idx >> 6, kl = idx & 63, k = c0 + kl;
-        if (!SG_CHK(SG_IN((c % kTyStages) * kTyStage + m * kTyKa + kl, kTySmemFloats), p.status)) continue;
+        if (!SG_CHK(SG_IN(so + m * kTyKa + kl, S::kSmemFloats), p.status)) continue;
         float* d = as + m * kTyKa + kl;
         if (m0 + m < p.M && k < K) cp_async4(d, A + static_cast<int64_t>(m0 + m) * p.lda + k);
         else *d = 0.f;
       }
 #pragma unroll 4
-      for (int u = 0; u < kTyChunk * kTyT / kTyThreads; ++u) {
+      for (int u = 0; u < kTyChunk * T / kTyThreads; ++u) {
         const int idx = t + u * kTyThreads;
-        const int kl = idx >> 5, n = idx & (kTyT - 1), k = c0 + kl;
-        if (!SG_CHK(SG_IN((c % kTyStages) * kTyStage + kTyStageA + kl * kTyT + n, kTySmemFloats), p.status)) continue;
-        float* d = bs + kl * kTyT + n;
+        const int kl = idx / T, n = idx % T, k = c0 + kl;
+        if (!SG_CHK(SG_IN(so + S::kStageA + kl * T + n, S::kSmemFloats), p.status)) continue;
+        float* d = bs + kl * T + n;
         if (k < K && n0 + n < p.N) cp_async4(d, B + static_cast<int64_t>(k) * p.ldb + n0 + n);
         else *d = 0.f;
       }
     }
   };
 
-  // group g, thread (ty, tx): rows ty + 8i, columns 4 tx .. 4 tx + 3 as two pairs
+  // group g, thread (ty, tx): rows ty + 8i, columns 4 tx + 32h + j as pairs (j = 0, 1), (2, 3)
   const int g = t / kTyGroupThreads, gt = t % kTyGroupThreads;
   const int tx = gt & 7, ty = gt >> 3;
-  float2 acc[4][2];
+  float2 acc[RPT][2 * HN];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
+  for (int i = 0; i < RPT; ++i)
+#pragma unroll
+    for (int h = 0; h < 2 * HN; ++h) acc[i][h] = make_float2(0.f, 0.f);
 
 #pragma unroll
-  for (int c = 0; c < kTyStages - 1; ++c) {
+  for (int c = 0; c < STAGES - 1; ++c) {
     if (c < nchunks) issue(c);
     cp_async_commit();  // one group per chunk slot, empty past the last chunk
   }
   for (int c = 0; c < nchunks; ++c) {
-    cp_async_wait<kTyStages - 2>();  // chunk c's copies (this thread's) have landed
-    __syncthreads();                 // everyone's have; everyone is done with chunk c - 1
-    if (c + kTyStages - 1 < nchunks) issue(c + kTyStages - 1);  // into chunk c - 1's stage
+    cp_async_wait<STAGES - 2>();  // chunk c's copies (this thread's) have landed
+    __syncthreads();              // everyone's have; everyone is done with chunk c - 1
+    if (c + STAGES - 1 < nchunks) issue(c + STAGES - 1);  // into chunk c - 1's stage
     cp_async_commit();
-    const float* as = ty_smem + (c % kTyStages) * kTyStage;
-    const float* arow = as + ty * kTyKa;
-    const float* bcol = as + kTyStageA + 4 * tx;
+    const int so = (c % STAGES) * S::kStage;
+    const float* arow = ty_smem + so + ty * kTyKa;
+    const float* bcol = ty_smem + so + S::kStageA + 4 * tx;
     // a chunk is 16 k-quads, so group g's quads are q = g, g + 4, g + 8, g + 12 in every chunk
-#pragma unroll
+    // (the 64-wide tile keeps one quad's operands live at a time: 128 registers)
+    constexpr int kQuadUnroll = T == 64 ? 1 : 4;
+#pragma unroll kQuadUnroll
     for (int qq = 0; qq < kTyChunk / 4 / kTyGroups; ++qq) {
       const int q = g + kTyGroups * qq;
-      if (!SG_CHK(SG_IN((c % kTyStages) * kTyStage + (ty + 24) * kTyKa + 4 * q + 3, kTySmemFloats) &&
-                      SG_IN((c % kTyStages) * kTyStage + kTyStageA + (4 * q + 3) * kTyT + 4 * tx + 3, kTySmemFloats),
-                  p.status))
-        break;
-      float4 a[4], b[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(arow + 8 * i * kTyKa + 4 * q);
+      for (int st = 0; st < 4 / KSTEP; ++st) {
+        const int k0 = 4 * q + KSTEP * st;  // first k of this step within the chunk
+        if (!SG_CHK(SG_IN(so + (ty + 8 * (RPT - 1)) * kTyKa + k0 + KSTEP - 1, S::kSmemFloats) &&
+                        SG_IN(so + S::kStageA + (k0 + KSTEP - 1) * T + 4 * tx + 32 * (HN - 1) + 3, S::kSmemFloats),
+                    p.status))
+          break;
+        AV a[RPT];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = *reinterpret_cast<const float4*>(bcol + (4 * q + j) * kTyT);
+        for (int i = 0; i < RPT; ++i) a[i] = *reinterpret_cast<const AV*>(arow + 8 * i * kTyKa + k0);
+        float4 b[KSTEP][HN];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const float4 bk = kk == 0 ? b[0] : kk == 1 ? b[1] : kk == 2 ? b[2] : b[3];
+        for (int kk = 0; kk < KSTEP; ++kk)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-          acc[i][0] = __ffma2_rn(make_float2(av, av), make_float2(bk.x, bk.y), acc[i][0]);
-          acc[i][1] = __ffma2_rn(make_float2(av, av), make_float2(bk.z, bk.w), acc[i][1]);
-        }
+          for (int h = 0; h < HN; ++h) b[kk][h] = *reinterpret_cast<const float4*>(bcol + (k0 + kk) * T + 32 * h);
+#pragma unroll
+        for (int kk = 0; kk < KSTEP; ++kk)
+#pragma unroll
+          for (int i = 0; i < RPT; ++i) {
+            const float av = AVec<KSTEP>::at(a[i], kk);
+#pragma unroll
+            for (int h = 0; h < HN; ++h) {
+              acc[i][2 * h] = __ffma2_rn(make_float2(av, av), make_float2(b[kk][h].x, b[kk][h].y), acc[i][2 * h]);
+              acc[i][2 * h + 1] =
+                  __ffma2_rn(make_float2(av, av), make_float2(b[kk][h].z, b[kk][h].w), acc[i][2 * h + 1]);
+            }
+          }
       }
     }
   }
   cp_async_wait<0>();
-  // partial tiles, then each thread adds one float4 of outputs over the groups in order
-  float* mine = part + g * kTyT * kTyT;
+  __syncthreads();  // every thread is done with the ring: the partial tiles go over it
+  // partial tiles [4 groups][T][T], then each thread adds T*T/256 outputs over the groups in order
+  float* part = ty_smem;
+  float* mine = part + g * T * T;
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    *reinterpret_cast<float4*>(mine + (ty + 8 * i) * kTyT + 4 * tx) =
-        make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
+  for (int i = 0; i < RPT; ++i)
+#pragma unroll
+    for (int h = 0; h < HN; ++h)
+      *reinterpret_cast<float4*>(mine + (ty + 8 * i) * T + 4 * tx + 32 * h) =
+          make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
   __syncthreads();
-  const int r = t >> 3, c = 4 * (t & 7);  // output row r, columns c .. c + 3
-  if (!SG_CHK(SG_IN((kTyGroups - 1) * kTyT * kTyT + r * kTyT + c + 3, kTyGroups * kTyT * kTyT), p.status)) return;
-  float4 s = *reinterpret_cast<const float4*>(part + r * kTyT + c);
 #pragma unroll
-  for (int gg = 1; gg < kTyGroups; ++gg) {
-    const float4 o = *reinterpret_cast<const float4*>(part + gg * kTyT * kTyT + r * kTyT + c);
-    s.x += o.x;
-    s.y += o.y;
-    s.z += o.z;
-    s.w += o.w;
+  for (int u = 0; u < T * T / 4 / kTyThreads; ++u) {
+    const int idx = t + u * kTyThreads;
+    const int r = idx / TQ, c = 4 * (idx % TQ);  // output row r, columns c .. c + 3
+    if (!SG_CHK(SG_IN((kTyGroups - 1) * T * T + r * T + c + 3, S::kSmemFloats), p.status)) return;
+    float4 s = *reinterpret_cast<const float4*>(part + r * T + c);
+#pragma unroll
+    for (int gg = 1; gg < kTyGroups; ++gg) {
+      const float4 o = *reinterpret_cast<const float4*>(part + gg * T * T + r * T + c);
+      s.x += o.x;
+      s.y += o.y;
+      s.z += o.z;
+      s.w += o.w;
+    }
+    const int m = m0 + r;
+    if (m >= p.M) continue;
+    float* crow = C + static_cast<int64_t>(m) * p.ldc + n0 + c;
+    const float sv[4] = {s.x, s.y, s.z, s.w};
+    if (p.beta == 0.f) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (n0 + c + j < p.N) crow[j] = p.alpha * sv[j];
+    } else {
+      float old[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) old[j] = n0 + c + j < p.N ? crow[j] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (n0 + c + j < p.N) crow[j] = fmaf(p.alpha, sv[j], p.beta * old[j]);
+    }
   }
-  const int m = m0 + r;
-  if (m >= p.M) return;
-  float* crow = C + static_cast<int64_t>(m) * p.ldc + n0 + c;
-  const float sv[4] = {s.x, s.y, s.z, s.w};
-  if (p.beta == 0.f) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (n0 + c + j < p.N) crow[j] = p.alpha * sv[j];
-  } else {
-    float old[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) old[j] = n0 + c + j < p.N ? crow[j] : 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (n0 + c + j < p.N) crow[j] = fmaf(p.alpha, sv[j], p.beta * old[j]);
+}
+
+template <int T, int STAGES, int KSTEP, int MINB>
+struct TinyVariant {
+  using S = TyShape<T, STAGES>;
+  static constexpr auto kernel = sgemm_tiny_kernel<T, STAGES, KSTEP, MINB>;
+  static cudaError_t prepare() {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   }
-}
-
-cudaError_t tiny_prepare() {
-  return cudaFuncSetAttribute(sgemm_tiny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kTySmemBytes);
-}
-
-cudaError_t tiny_occupancy(int* ctas) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, sgemm_tiny_kernel, kTyThreads, kTySmemBytes);
-}
-
-cudaError_t tiny_launch(const LaunchArgs& a, cudaStream_t stream) {
-  TinyParams p;
-  p.A = a.A;
-  p.B = a.B;
-  p.C = a.C;
-  p.lda = a.lda;
-  p.ldb = a.ldb;
-  p.ldc = a.ldc;
-  p.M = a.M;
-  p.N = a.N;
-  p.K = a.K;
-  p.alpha = a.alpha;
-  p.beta = a.beta;
-  const int batch = a.batch > 1 ? a.batch : 1;
-  p.stride_a = batch > 1 ? a.stride_a : 0;
-  p.stride_b = batch > 1 ? a.stride_b : 0;
-  p.stride_c = batch > 1 ? a.stride_c : 0;
-  p.status = a.status;
-  p.vec = (reinterpret_cast<uintptr_t>(a.A) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.B) & 15) == 0 &&
-          p.lda % 4 == 0 && p.ldb % 4 == 0 && p.stride_a % 4 == 0 && p.stride_b % 4 == 0;
-  const dim3 grid((a.N + kTyT - 1) / kTyT, (a.M + kTyT - 1) / kTyT, batch);
-  sgemm_tiny_kernel<<<grid, kTyThreads, kTySmemBytes, stream>>>(p);
-  return cudaGetLastError();
-}
+  static cudaError_t occupancy(int* ctas) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kernel, kTyThreads, S::kSmemBytes);
+  }
+  static cudaError_t launch(const LaunchArgs& a, cudaStream_t stream) {
+    TinyParams p;
+    p.A = a.A;
+    p.B = a.B;
+    p.C = a.C;
+    p.lda = a.lda;
+    p.ldb = a.ldb;
+    p.ldc = a.ldc;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    const int batch = a.batch > 1 ? a.batch : 1;
+    p.stride_a = batch > 1 ? a.stride_a : 0;
+    p.stride_b = batch > 1 ? a.stride_b : 0;
+    p.stride_c = batch > 1 ? a.stride_c : 0;
+    p.status = a.status;
+    p.vec = (reinterpret_cast<uintptr_t>(a.A) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.B) & 15) == 0 &&
+            p.lda % 4 == 0 && p.ldb % 4 == 0 && p.stride_a % 4 == 0 && p.stride_b % 4 == 0;
+    const dim3 grid((a.N + T - 1) / T, (a.M + T - 1) / T, batch);
+    kernel<<<grid, kTyThreads, S::kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+  }
+  static Variant describe(const char* name) {
+    // any alignment, leading dimension and K, strided batches on grid z
+    return Variant{name, kKindTiny, T, T, kTyChunk, STAGES, 1, kTyThreads, S::kSmemBytes, -1, &prepare, &occupancy,
+                   &launch, 0, 0, 1};
+  }
+};
 
 const Variant kTinyVariants[] = {
-    // any alignment, leading dimension and K, strided batches on grid z
-    Variant{"tiny_32x32", kKindTiny, kTyT, kTyT, kTyChunk, kTyStages, 1, kTyThreads, kTySmemBytes, -1, &tiny_prepare,
-            &tiny_occupancy, &tiny_launch, 0, 0, 1},
+    TinyVariant<32, 4, 4, 1>::describe("tiny_32x32"),
+    TinyVariant<64, 3, 2, 2>::describe("small_64x64"),
 };
 
 }  // namespace

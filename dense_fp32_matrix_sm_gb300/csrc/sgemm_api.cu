@@ -261,6 +261,24 @@ bool tiny_shape(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, boo
   return rows16 && M <= 32 && 4 * tiles >= 3 * static_cast<int64_t>(num_sms);
 }
 
+// Products the 64 x 64 form of the tiny kernel takes from the table: more
+// than 16 rows, K <= 512 and at most two of its tiles per SM over the whole
+// batch (one wave, no split along K), when the tiny kernel's rule does not
+// apply; and either at most one tile per SM, a k loop of at most 256, or
+// at least 0.9 of the two-per-SM slots filled (between those the SMs that
+// get two tiles set the time).  Measured (TFLOP/s, L2 flushed; the 128-row
+// choice and cuBLAS in brackets): 768 x 768 x 512 29.5 (25.8, 31.9), 768 x
+// 768 x 256 21.2 (16.0, 22.7), 1024 x 512 x 512 26.3 (23.4, 26.3), 1024 x
+// 1024 x 256 26.3 (23.8, 29.1), 2048 x 512 x 256 26.3 (23.4, 29.0), 1088 x
+// 1088 x 448 34.6 (32.0, 39.5), 1536 x 768 x 384 34.1 (33.1, 39.5); left
+// to the 128-row tiles: 1024 x 1024 x 512 (32.8 against 34.4), 896 x 896 x
+// 512 (25.1 against 32.8), 960 x 960 x 384 (26.7 against 28.2).
+bool small_shape(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms) {
+  const int64_t tiles = std::max<int64_t>(batch, 1) * ((M + 63) / 64) * ((N + 63) / 64);
+  const int64_t sms = num_sms;
+  return M > 16 && K <= 512 && tiles <= 2 * sms && (tiles <= sms || K <= 256 || 5 * tiles >= 9 * sms);
+}
+
 // a_span / b_span: elements one stored A / B spans (-1: M*lda / K*ldb, an
 // operand stored as the kernels read it)
 bool variant_supports(const Variant* v, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
@@ -361,6 +379,8 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   if (rows_shape(M, N, K, batch, b_trans)) return "gemv_16x1024";
   // tiny products, and long-K products of 17 to 32 rows: 32 x 32 tiles, any layout
   if (tiny_shape(M, N, K, batch, num_sms, lda % 4 == 0 && ldb % 4 == 0)) return "tiny_32x32";
+  // a short k loop and at most two 64 x 64 tiles per SM: the same ring with 64 x 64 tiles
+  if (small_shape(M, N, K, batch, num_sms)) return "small_64x64";
   if (batch > 1) {
     // Strided batches run on the batched variants only: the transposed-A
     // family when TMA can take the layout (tile counts over the whole batch),
@@ -1441,7 +1461,13 @@ StreamKSchedule api_streamk_schedule(int64_t tiles, int64_t KT, int sms, int cta
   StreamKSchedule s{tiles < slots ? tiles : slots, 0, 0};
   if (!allowed || tiles <= 0) return s;
   if (tiles > slots) {
-    if (tiles % slots != 0 && KT >= 8) s = {slots, static_cast<int>(tiles / slots), (tiles % slots) * KT};
+    // The tail's k-slices go to every CTA only when there is at least one
+    // slice per CTA: a finisher waits on every CTA between the first one that
+    // holds a slice of its tile and itself, so no CTA may have an empty range.
+    // (1152 x 1152 x 256 on 64 x 128 tiles: 10 tail tiles x 8 slices for 152
+    // CTAs; the tail then runs as a plain partial wave.)
+    const int64_t tail = tiles % slots;
+    if (tail != 0 && KT >= 8 && tail * KT >= slots) s = {slots, static_cast<int>(tiles / slots), tail * KT};
     return s;
   }
   const int64_t cap = sms / tiles;  // pieces per tile with at most one CTA per SM

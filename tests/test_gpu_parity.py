@@ -225,18 +225,20 @@ def test_leading_dimensions(sg, oracle_mod, lds, shape):
         assert used.startswith("cpa")          # A copied 4 bytes at a time: any lda
 
 
+@pytest.mark.parametrize("config", ["tiny_32x32", "small_64x64"])
 @pytest.mark.parametrize("shape", [(32, 32, 256), (31, 33, 257), (100, 70, 511), (64, 96, 512), (512, 512, 512),
-                                   (45, 200, 300)])
-def test_tiny_k_chunks(sg, oracle_mod, shape):
-    # K up to 256 is one staged chunk, K in (256, 512] two; 16-byte copies,
-    # then 4-byte copies (odd lda), and a strided batch of the same shape
+                                   (45, 200, 300), (130, 65, 1000)])
+def test_tiny_k_chunks(sg, oracle_mod, config, shape):
+    # K streamed in 64-deep chunks through the ring (one chunk, several, a
+    # ragged last one); 16-byte copies, then 4-byte copies (odd lda), and a
+    # strided batch of the same shape
     M, N, K = shape
     A, B, C0 = make_inputs(M, N, K, seed=M * 7 + K, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
     for lda, alpha, beta in ((K + (-K) % 4, 1.0, 0.0), (K + 1, -0.5, 2.0)):
-        C, used = run_gpu(sg, A, B, C0, alpha, beta, config="tiny_32x32", lda=lda)
+        C, used = run_gpu(sg, A, B, C0, alpha, beta, config=config, lda=lda)
         Cref, S = oracle_mod.sgemm_ref(A, B, C0, alpha, beta)
-        assert_parity(C, Cref, S, K, f"tiny {shape} lda={lda}")
-        C2, _ = run_gpu(sg, A, B, C0, alpha, beta, config="tiny_32x32", lda=lda)
+        assert_parity(C, Cref, S, K, f"{config} {shape} lda={lda}")
+        C2, _ = run_gpu(sg, A, B, C0, alpha, beta, config=config, lda=lda)
         assert np.array_equal(C, C2)
     if M * N <= 64 * 96:
         batch = 3
@@ -244,7 +246,7 @@ def test_tiny_k_chunks(sg, oracle_mod, shape):
         Bs = np.stack([B - z for z in range(batch)])
         Cs0 = np.stack([C0 + z for z in range(batch)])
         dA, dB, dC = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (As, Bs, Cs0))
-        plan = sg.Plan(M, N, K, config="tiny_32x32", batch=batch, stride_a=M * K, stride_b=K * N, stride_c=M * N)
+        plan = sg.Plan(M, N, K, config=config, batch=batch, stride_a=M * K, stride_b=K * N, stride_c=M * N)
         try:
             plan.run(1.0, dA, dB, 1.0, dC)
             torch.cuda.synchronize()
@@ -254,7 +256,7 @@ def test_tiny_k_chunks(sg, oracle_mod, shape):
         out = dC.cpu().numpy()
         for z in range(batch):
             Cref, S = oracle_mod.sgemm_ref(As[z], Bs[z], Cs0[z], 1.0, 1.0)
-            assert_parity(out[z], Cref, S, K, f"tiny batch {z} {shape}")
+            assert_parity(out[z], Cref, S, K, f"{config} batch {z} {shape}")
 
 
 @pytest.mark.parametrize("case", [
@@ -266,6 +268,8 @@ def test_tiny_k_chunks(sg, oracle_mod, shape):
     (64, 1000, 1500, "tmat_64x256x32_s3_b1"),  # ragged N and K
     (40, 700, 3001, "tmat_64x256x32_s3_b1"),
     (65, 4096, 4096, None),                # more than 64 rows: the 128-row tiles
+    (768, 768, 512, "small_64x64"),        # a short k loop, at most two 64 x 64 tiles per SM
+    (1000, 1100, 333, "small_64x64"),
 ])
 def test_seventeen_to_sixtyfour_rows(sg, oracle_mod, case):
     M, N, K, expect = case
@@ -504,14 +508,30 @@ def test_transposed_a_variants_take_any_lda(sg, oracle_mod):
             assert_parity(C, Cref, S, K, f"{name} lda={lda} off_a={off_a}")
 
 
+TAIL_SHORTER_THAN_GRID = [(1152, 1152, 256), (1152, 2176, 256), (1152, 4352, 256)]
+
+
 @pytest.mark.parametrize("shape", [(2048, 2048, 1024), (1500, 3000, 780), (2560, 1408, 256),
                                    # fewer tiles than CTA slots: every tile split along K
-                                   (1024, 1024, 1024), (512, 520, 8200), (1000, 300, 3000)])
+                                   (1024, 1024, 1024), (512, 520, 8200), (1000, 300, 3000),
+                                   # a tail with fewer k-slices than CTAs (64 x 128 tiles: 10 x 8; 128 x 128
+                                   # and 128 x 256 tiles: 1 x 8) runs as a plain partial wave
+                                   (1152, 1152, 256), (1152, 2176, 256), (1152, 4352, 256)])
 def test_stream_k_tail(sg, oracle_mod, shape):
     """Tile counts that overshoot the resident grid: full waves run
     data-parallel and the leftover tiles are split along K across all CTAs
     (partials through a workspace, added in CTA order).  With fewer tiles
-    than CTA slots there is no data-parallel wave: every tile is split."""
+    than CTA slots there is no data-parallel wave: every tile is split.
+    Waits are limited to 0.5 s here, so a schedule that leaves a finisher
+    waiting fails fast with SGEMM_ERR_TIMEOUT."""
+    sg.set_wait_timeout_ns(500_000_000)
+    try:
+        _stream_k_tail(sg, oracle_mod, shape)
+    finally:
+        sg.set_wait_timeout_ns(0)  # back to the default
+
+
+def _stream_k_tail(sg, oracle_mod, shape):
     M, N, K = shape
     A, B, C0 = make_inputs(M, N, K, seed=M + 3 * N + K, dist_a=("normal", 1.0), dist_b=("normal", 1.0))
     dA = torch.from_numpy(A).cuda()
@@ -540,7 +560,8 @@ def test_stream_k_tail(sg, oracle_mod, shape):
         Cref, S = oracle_mod.sgemm_ref(np.ascontiguousarray(A[rows]), np.ascontiguousarray(B[:, cols]),
                                        np.ascontiguousarray(C0[np.ix_(rows, cols)]), 0.5, 3.0)
         assert_parity(Cs, Cref, S, K, f"{name} {shape} streamk={info['streamk']} dp_waves={info['dp_waves']}")
-    assert saw_streamk, "no variant split its tail for these shapes"
+    if shape not in TAIL_SHORTER_THAN_GRID:
+        assert saw_streamk, "no variant split its tail for these shapes"
 
 
 # ---- split-TF32 tensor-core variant (reported apart from the FFMA path) -------
