@@ -11,7 +11,9 @@ Timing: W >= 3 untimed warm-up steps, then K steps; before every step a
 256 MiB buffer is written to flush the 129 MB L2 and then read back, so
 that L2 holds neither the inputs nor dirty lines whose write-back would
 land inside the step, outside that step's CUDA event pair on the launching
-stream.  ms_per_step is the mean event time;
+stream.  ms_per_step is the mean event time (the "workloads" records rate
+each configuration by the median step instead, since a single host-side
+stall among thousands of microsecond steps moves a mean of them);
 under torchrun the max over ranks (each rank runs its own independent
 problem: weak scaling, no collective on the data path).
 
@@ -411,13 +413,14 @@ def workloads_leg(torch, sg, names, stream, flush, warmup, steps, sms, peaks, sa
             raise SystemExit(f"kernel status word set during the {name} steps (a wait timed out)")
         launches += plan.launches * (len(times) + warmup)
         ms = statistics.fmean(times)
+        ms_med = statistics.median(times)
         clk = sampler.summary(window=(t0 - 0.05, t1 + 0.05)) if sampler else {}
         mhz = clk.get("sm_mhz") or peaks.get("sm_max_mhz") or 2070.0
         rec = {"workload": f"{w.name}: {w.describe()}", "ms_per_step": round(ms, 5),
-               "ms_median": round(statistics.median(times), 5), "ms_min": round(min(times), 5),
+               "ms_median": round(ms_med, 5), "ms_min": round(min(times), 5),
                "steps": len(times), "timed_seconds": round(t1 - t0, 2),
-               "gflops": round(w.flops / (ms * 1e-3) / 1e9, 1),
-               "roofline": roofline_for(w, ms, sms, mhz, peaks, traffic_for(info.get("variant"), w.name)),
+               "gflops": round(w.flops / (ms_med * 1e-3) / 1e9, 1), "rate_from": "median step",
+               "roofline": roofline_for(w, ms_med, sms, mhz, peaks, traffic_for(info.get("variant"), w.name)),
                "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
                "plan": plan.describe(), "gpu_launches_per_step": plan.launches}
         plan.close()
@@ -426,7 +429,7 @@ def workloads_leg(torch, sg, names, stream, flush, warmup, steps, sms, peaks, sa
         cb = cublas_step_fn(torch, w, dA, dB, dC0, out)
         for _ in range(warmup):
             cb()
-        cb_ms = statistics.fmean(time_steps(torch, cb, steps, flush, stream))
+        cb_ms = statistics.median(time_steps(torch, cb, steps, flush, stream))
         rec["cublas_context"] = {"gflops": round(w.flops / (cb_ms * 1e-3) / 1e9, 1), "ms": round(cb_ms, 5),
                                  "call": "torch.matmul/addmm fp32, allow_tf32=False"}
         del dA, dB, dC0, dC, out
