@@ -30,6 +30,8 @@ from ._lib import (  # noqa: F401
     selftest_wait_timeout,
     set_wait_timeout_ns,
     wait_limit_ns,
+    table_choice,
+    streamk_schedule,
     sgemm,
     status_string,
 )

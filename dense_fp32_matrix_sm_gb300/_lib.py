@@ -49,6 +49,10 @@ SIGNATURES = {
     "sgemm_set_wait_timeout_ns": (_int, [ctypes.c_uint64]),
     "sgemm_wait_limit_ns": (_int, [_i64, _i64, _i64, _i64, _int, ctypes.POINTER(ctypes.c_uint64)]),
     "sgemm_selftest_wait_timeout": (_int, [ctypes.c_uint64, _vp]),
+    "sgemm_table_choice": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _int, _int, ctypes.c_char_p,
+                                  ctypes.c_size_t, ctypes.POINTER(_int), ctypes.POINTER(_int)]),
+    "sgemm_streamk_schedule": (_int, [_i64, _i64, _int, _int, ctypes.POINTER(_i64), ctypes.POINTER(_int),
+                                      ctypes.POINTER(_i64)]),
     "sgemm_run_static_scratch": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "sgemm_plan_ex": (_int, [_int, _int, _int, _i64, _i64, _i64, _i64, _i64, _i64, _int, ctypes.POINTER(_vp)]),
     "sgemm_plan_ex_batched": (_int, [_int, _int, _int, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
@@ -139,6 +143,27 @@ def wait_limit_ns(M: int, N: int, K: int, batch: int = 1, num_sms: int = 152) ->
     _check(lib().sgemm_wait_limit_ns(int(M), int(N), int(K), int(batch), int(num_sms), ctypes.byref(out)),
            "sgemm_wait_limit_ns")
     return int(out.value)
+
+
+def table_choice(M: int, N: int, K: int, lda: Optional[int] = None, ldb: Optional[int] = None, batch: int = 1,
+                 stride_a: int = 0, stride_b: int = 0, b_trans: bool = False, num_sms: int = 152):
+    """The shape table's variant for a row-major product on a device with num_sms SMs, and whether the
+    plan would first copy A / B into padded rows: (name, repack_a, repack_b).  No CUDA call."""
+    buf = ctypes.create_string_buffer(128)
+    ra, rb = _int(), _int()
+    _check(lib().sgemm_table_choice(int(M), int(N), int(K), int(K if lda is None else lda),
+                                    int(N if ldb is None else ldb), int(batch), int(stride_a), int(stride_b),
+                                    1 if b_trans else 0, int(num_sms), buf, len(buf), ctypes.byref(ra),
+                                    ctypes.byref(rb)), "sgemm_table_choice")
+    return buf.value.decode(), bool(ra.value), bool(rb.value)
+
+
+def streamk_schedule(tiles: int, k_slices: int, num_sms: int = 152, ctas_per_sm: int = 1):
+    """The persistent grid of a transposed-A plan: (grid, dp_waves, sk_iters).  No CUDA call."""
+    g, d, i = _i64(), _int(), _i64()
+    _check(lib().sgemm_streamk_schedule(int(tiles), int(k_slices), int(num_sms), int(ctas_per_sm), ctypes.byref(g),
+                                        ctypes.byref(d), ctypes.byref(i)), "sgemm_streamk_schedule")
+    return int(g.value), int(d.value), int(i.value)
 
 
 def selftest_wait_timeout(ns: int, stream=None) -> int:

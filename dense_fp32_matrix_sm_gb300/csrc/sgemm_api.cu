@@ -412,6 +412,28 @@ const char* table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
   return tmat_choice(M, N, K, 1, num_sms);
 }
 
+// The table's variant for a product on `sms` SMs, after the padding-copy
+// rule: TMA needs rows that are 16-byte multiples.  From 256^3 of work on,
+// an operand without them is copied each run into a plan buffer with padded
+// rows, so the table's TMA kernels can read it (measured at 4096^3, lda =
+// 4097 ran 54.6 TFLOP/s on the cp.async kernel and ldb = 4097 29.8 on the
+// scalar-load kernel, against 68.8 aligned).  *lda / *ldb become the padded
+// leading dimensions when *rp_a / *rp_b are set.  Pure host arithmetic.
+const char* plan_table_choice(int64_t M, int64_t N, int64_t K, int64_t* lda, int64_t* ldb, int sms, int64_t batch,
+                              int64_t stride_a, int64_t stride_b, int64_t a_span, int64_t b_span, int b_trans,
+                              bool* rp_a, bool* rp_b) {
+  *rp_a = *rp_b = false;
+  if (batch <= 1 && K > 0 && !gemv_shape(M, N, K, batch) &&
+      !tiny_shape(M, N, K, batch, sms, *lda % 4 == 0 && *ldb % 4 == 0) && !rows_shape(M, N, K, batch, b_trans) &&
+      static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= 16777216.0) {
+    *rp_a = *lda % 4 != 0;
+    *rp_b = *ldb % 4 != 0;
+    if (*rp_a) *lda = (K + 3) / 4 * 4;
+    if (*rp_b) *ldb = (N + 3) / 4 * 4;
+  }
+  return table_choice(M, N, K, *lda, *ldb, sms, batch, stride_a, stride_b, a_span, b_span, b_trans);
+}
+
 // b_trans: the caller's B is stored transposed and a transpose buffer will
 // hold it unless the chosen kernel reads it as stored (the table then
 // prefers a kernel that does).
@@ -437,22 +459,8 @@ sgemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t l
       config_id = find_variant(forced);
       if (config_id < 0) return SGEMM_ERR_INVALID_ARG;
     } else {
-      // TMA needs rows that are 16-byte multiples.  From 256^3 of work on, an
-      // operand without them is copied each run into a plan buffer with padded
-      // rows (one cudaMemcpy2DAsync), so the table's TMA kernels can read it:
-      // measured at 4096^3, lda = 4097 ran 54.6 TFLOP/s on the cp.async kernel
-      // and ldb = 4097 29.8 on the scalar-load kernel, against 68.8 aligned.
-      if (batch <= 1 && K > 0 && !gemv_shape(M, N, K, batch) &&
-          !tiny_shape(M, N, K, batch, sms, lda % 4 == 0 && ldb % 4 == 0) &&
-          !rows_shape(M, N, K, batch, b_trans) &&
-          static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) >= 16777216.0) {
-        rp_a = lda % 4 != 0;
-        rp_b = ldb % 4 != 0;
-        if (rp_a) lda = (K + 3) / 4 * 4;
-        if (rp_b) ldb = (N + 3) / 4 * 4;
-      }
-      config_id =
-          find_variant(table_choice(M, N, K, lda, ldb, sms, batch, stride_a, stride_b, a_span, b_span, b_trans));
+      config_id = find_variant(
+          plan_table_choice(M, N, K, &lda, &ldb, sms, batch, stride_a, stride_b, a_span, b_span, b_trans, &rp_a, &rp_b));
       if (config_id < 0) config_id = reg.first_generic;
     }
   }
@@ -1382,6 +1390,34 @@ sgemm_status_t sgemm_device_status(int reset) {
 sgemm_status_t sgemm_wait_limit_ns(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, uint64_t* out) {
   if (!out || M < 0 || N < 0 || K < 0 || batch < 0 || num_sms < 1) return SGEMM_ERR_INVALID_ARG;
   *out = wait_limit_ns(work_floor_ns(M, N, K, batch, num_sms));
+  return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t batch,
+                                  int64_t stride_a, int64_t stride_b, int b_trans, int num_sms, char* name,
+                                  size_t name_size, int* repack_a, int* repack_b) {
+  if (!name || name_size == 0 || num_sms < 1 || batch < 0) return SGEMM_ERR_INVALID_ARG;
+  sgemm_status_t st = check_dims(M, N, K, lda, ldb, N);
+  if (st != SGEMM_OK) return st;
+  bool rp_a = false, rp_b = false;
+  const char* v = plan_table_choice(M, N, K, &lda, &ldb, num_sms, batch, stride_a, stride_b, -1, -1, b_trans ? 1 : 0,
+                                    &rp_a, &rp_b);
+  if (find_variant(v) < 0) v = registry().all[registry().first_generic]->name;
+  if (strlen(v) + 1 > name_size) return SGEMM_ERR_INVALID_ARG;
+  memcpy(name, v, strlen(v) + 1);
+  if (repack_a) *repack_a = rp_a ? 1 : 0;
+  if (repack_b) *repack_b = rp_b ? 1 : 0;
+  return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_streamk_schedule(int64_t tiles, int64_t k_slices, int num_sms, int ctas_per_sm, int64_t* grid,
+                                      int* dp_waves, int64_t* sk_iters) {
+  if (!grid || !dp_waves || !sk_iters || tiles < 0 || k_slices < 0 || num_sms < 1 || ctas_per_sm < 1)
+    return SGEMM_ERR_INVALID_ARG;
+  const StreamKSchedule s = api_streamk_schedule(tiles, k_slices, num_sms, ctas_per_sm, true);
+  *grid = s.grid;
+  *dp_waves = s.dp_waves;
+  *sk_iters = s.sk_iters;
   return SGEMM_OK;
 }
 

@@ -398,6 +398,40 @@ sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns);
 sgemm_status_t sgemm_wait_limit_ns(int64_t M, int64_t N, int64_t K, int64_t batch, int num_sms, uint64_t *out);
 
 /*
+ * The variant the shape table picks for a row-major, untransposed product
+ * (M x K times K x N, leading dimensions lda and ldb; `batch` products with
+ * element strides stride_a and stride_b, 0 = shared, when batch > 1) on a
+ * device with num_sms SMs -- the choice sgemm_plan / sgemm_plan_batched make
+ * for that device.  b_trans != 0: B is given transposed (stored N x K), as
+ * sgemm_plan_ex passes it.  `name` (name_size bytes, caller-owned) receives
+ * the variant's name; *repack_a / *repack_b (either may be NULL) are set to
+ * 1 when the plan would first copy that operand into rows padded to 16
+ * bytes.  Pure host arithmetic, no CUDA call.  Invalid sizes or leading
+ * dimensions, num_sms < 1, or a name buffer too small give
+ * SGEMM_ERR_INVALID_ARG.  (An introspection aid; the per-shape choice
+ * follows "How a Matmul Kernel Gets Fast": configurations measured per shape
+ * class.)
+ */
+sgemm_status_t sgemm_table_choice(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t batch,
+                                  int64_t stride_a, int64_t stride_b, int b_trans, int num_sms, char *name,
+                                  size_t name_size, int *repack_a, int *repack_b);
+
+/*
+ * The persistent grid a transposed-A plan uses for `tiles` C tiles of
+ * k_slices 32-deep k-slices each, with ctas_per_sm CTAs of the variant
+ * resident on each of num_sms SMs ("Writing a Fast Matmul in CUDA, Step by
+ * Step", "Size effects" and "What cuBLAS and CUTLASS add": a partial last
+ * wave split along K).  *grid = CTAs launched; *dp_waves = whole waves of
+ * tiles run data-parallel first; *sk_iters = k-slices of the remaining tiles
+ * shared out over the grid (0: no split).  Whenever *sk_iters > 0 it is at
+ * least *grid, so every CTA holds at least one slice.  Pure host arithmetic,
+ * no CUDA call; negative counts, num_sms < 1, ctas_per_sm < 1 or a NULL
+ * output give SGEMM_ERR_INVALID_ARG.
+ */
+sgemm_status_t sgemm_streamk_schedule(int64_t tiles, int64_t k_slices, int num_sms, int ctas_per_sm, int64_t *grid,
+                                      int *dp_waves, int64_t *sk_iters);
+
+/*
  * Self-test of the wait limit: launches one thread that waits, with limit
  * timeout_ns, on a barrier phase that nothing completes, then synchronises
  * the stream.  Returns SGEMM_ERR_TIMEOUT (and clears the status word) when
