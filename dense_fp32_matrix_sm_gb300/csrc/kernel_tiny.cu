@@ -18,9 +18,9 @@
 //    q = g, g + 4, ... (interleaved, so every group has work for any K);
 //    a thread of a group holds T/8 rows (ty + 8i) x T/8 columns (4 tx + 32h
 //    + j), read KSTEP k at a time: per step one KSTEP-wide read of A per
-//    row and two... T/32 16-byte reads of B per k, then FFMA2s, each a
-//    broadcast A element times a pair of adjacent B columns (each half an
-//    IEEE fma, so the sums are those of fmaf).  The A rows' stride in a
+//    row and T/32 16-byte reads of B per k, then FFMA2s, each a broadcast
+//    A element times a pair of adjacent B columns (each half an IEEE fma,
+//    so the sums are those of fmaf).  The A rows' stride in a
 //    stage (68 words, 4 mod 8) puts the four rows a warp reads at once in
 //    different banks.
 //  * The four groups' partial tiles go to shared memory (over the ring,
