@@ -1241,3 +1241,23 @@ def test_sgemm_helper_reuses_its_plan(sg, oracle_mod):
     assert sg.plan_cache_size() == 2
     sg.clear_plan_cache()
     assert sg.plan_cache_size() == 0
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096, None, None), (4096, 4096, 4096, 4097, None),
+                                   (16, 16384, 8192, None, None), (1, 4096, 4096, None, None),
+                                   (128, 128, 128, None, None), (32, 4096, 4096, None, None),
+                                   (64, 4096, 4096, None, None), (768, 768, 512, None, None),
+                                   (1408, 1408, 1408, None, None), (200, 130, 100, 101, 131),
+                                   (100, 96, 1000, None, 97), (8, 300, 520, None, None)])
+def test_plan_follows_the_host_table(sg, shape):
+    # a plan's variant is the one sgemm_table_choice computes on the host for this device's SM count
+    M, N, K, lda, ldb = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    expect, rp_a, rp_b = sg.table_choice(M, N, K, lda=lda, ldb=ldb, num_sms=sms)
+    plan = sg.Plan(M, N, K, lda or K, ldb or N, N)
+    try:
+        info = plan.info()
+        assert info["variant"] == expect, (shape, info["variant"], expect)
+        assert info["repack"] == (1 if rp_a else 0) | (2 if rp_b else 0), (shape, info["repack"], rp_a, rp_b)
+    finally:
+        plan.close()
