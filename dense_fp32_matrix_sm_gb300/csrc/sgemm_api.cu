@@ -343,7 +343,8 @@ const char* tmat_choice(int64_t M, int64_t N, int64_t K, int64_t batch, int num_
   // flushed; 128-row table choice, cuBLAS): 64 x 16384 x 8192 62.6 (33.7,
   // 55.9), 64 x 4096 x 4096 41.6 (23.3, 21.0), 48 x 4096 x 4096 31.2 (17.4,
   // 15.7), 64 x 9728 x 2048 47.5 (27.5, 41.5), 64 x 8192 x 8192 51.0 (30.6,
-  // 37.8), 32 x 16384 x 8192 31.4 (16.8, 38.4)
+  // 37.8).  Up to 32 rows with enough 32-column tiles the tiny kernel's
+  // rule comes first (32 x 16384 x 8192: 30.4 there, 31.4 here).
   if (M <= 64) return "tmat_64x256x32_s3_b1";
   // 128 x 256 tiles from 0.3 of a wave on (20 wide tiles per 6 SMs), unless
   // the last column of tiles would be mostly empty below N = 4096 (1408^3:
