@@ -7,10 +7,10 @@
 namespace sgemm {
 namespace {
 const Variant kRowVariants[] = {
-    // <BM, BN, stages, CTAs per SM, transpose step, -, split-phase slice sync>
+    // <BM, BN, stages, CTAs per SM, transpose step, second step (-1: none), split-phase slice sync>
     // 8 warps of 64 x 32, 168 registers: the table's choice up to 64 rows
     tmat::Variant_<64, 256, 3, 1, 24, -1, true>::describe("tmat_64x256x32_s3_b1"),
-    // 4 warps, two CTAs per SM: more, narrower tiles
+    // 4 warps, more and narrower tiles (113 KB: one CTA per SM in practice; autotuning only)
     tmat::Variant_<64, 128, 4, 2, 16>::describe("tmat_64x128x32_s4_b2"),
 };
 }  // namespace
